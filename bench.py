@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the paged, quantized KV store on GB300.
+
+One step = the whole hot path over one batch: block tables from the
+ReqToTokenPool rows, the quantizing store of each request's new token, and
+paged split-K decode attention (plus its combine), all through the C ABI.
+
+Default workload: INT8 KV (per-token, per-head asymmetric), MHA 32 q / 32 kv
+heads, head_dim 128, block size 16, 128 requests at context 4096, K/V drawn
+from N(0,1) with 1% of the channels scaled by 8. The pool (4.4 GB) is larger
+than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle
+instead (the reference arm of this build: there is no reference code to
+install), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "decode attn tokens/s and HBM GB/s (% of GB300 peak) over paged INT8/INT4 KV"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="cfg3", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5"])
+    p.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
+    p.add_argument("--num-splits", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--json-out", default="")
+    return p.parse_args()
+
+
+def make_workload(name: str, batch: int, rank: int):
+    kw = {}
+    if batch:
+        kw["batch"] = batch
+    wl = synthetic.by_name(name, **kw)
+    if rank:  # each rank serves its own requests: a different seed
+        kw["seed"] = wl.seed + 1000 * rank
+        wl = synthetic.by_name(name, **kw)
+    return wl
+
+
+def workload_desc(wl) -> dict:
+    return {
+        "workload": f"{wl.name}: {wl.description}",
+        "kv_dtype": wl.kv_dtype, "q_dtype": wl.q_dtype, "batch": wl.batch,
+        "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
+        "block_size": wl.block_size, "max_context": wl.max_seq_len,
+        "mean_context": float(np.mean(wl.seq_lens)),
+        "prefill_chunk_tokens": 0 if wl.chunk_slots is None else len(wl.chunk_slots),
+    }
+
+
+def decode_algorithmic_bytes(wl) -> int:
+    """Bytes the decode call must move: KV codes + scale/zero of every context
+    token, Q, the output, the block tables and the lengths."""
+    kv = int(np.sum(wl.seq_lens, dtype=np.int64)) * wl.kv_token_bytes()
+    q = wl.batch * wl.q_heads * wl.head_dim * 2
+    nblk = int(np.sum((wl.seq_lens + 15) // 16))
+    return kv + 2 * q + 4 * nblk + 4 * wl.batch
+
+
+def unique_decode_bytes(wl) -> int:
+    """As above but counting each physical block once (shared prefixes)."""
+    seen = set()
+    total = 0
+    for b in range(wl.batch):
+        L = int(wl.seq_lens[b])
+        for j in range((L + 15) // 16):
+            blk = int(wl.block_tables[b, j])
+            if blk in seen:
+                continue
+            seen.add(blk)
+            total += min(16, L - 16 * j) * wl.kv_token_bytes()
+    q = wl.batch * wl.q_heads * wl.head_dim * 2
+    return total + 2 * q
+
+
+# ---- clocks (NVML through ctypes, read-only) -----------------------------------
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons of one GPU during a region."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, uuid: str, period_s: float = 0.005):
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        self.max_mhz = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(),
+                                                   ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reason_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except OSError:
+            pass
+
+    def _poll(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0 and \
+                    self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((mhz.value, rs.value))
+            time.sleep(self.period)
+
+    def start(self):
+        if not self.ok:
+            return
+        self._stop = threading.Event()
+        self._t = threading.Thread(target=self._poll, daemon=True)
+        self._t.start()
+
+    def stop(self) -> dict:
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        self._stop.set()
+        self._t.join()
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    src = hashlib.sha256()
+    for fn in ("kvq_decode.cu", "kvq_device.cuh"):
+        with open(os.path.join(ROOT, "paged_quantized_kv_store_gb300", "csrc", fn), "rb") as f:
+            src.update(f.read())
+    sha = src.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, sha
+    m_sha = re.search(r"kernel_source_sha:\s*(\w+)", text)
+    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None, sha
+    return float(m_b.group(1)), sha
+
+
+# ---- our arm ---------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+
+    import paged_quantized_kv_store_gb300 as kvq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    kvq.load()
+    wl = make_workload(args.workload, args.batch, rank)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+    def to_dev(bits, dt):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt[dt]).to(dev)
+
+    # ---- setup (untimed): pool, stored context, per-step inputs -------------------
+    pool = kvq.KVPool.allocate(wl.num_blocks, wl.kv_heads, wl.kv_dtype, device=dev)
+    for slots, k, v in wl.setup_chunks(max_tokens=1 << 17):
+        kvq.kv_store_quant(pool, to_dev(k, wl.in_dtype), to_dev(v, wl.in_dtype),
+                           torch.from_numpy(slots).to(dev))
+    torch.cuda.synchronize()
+    slots, k_new, v_new = wl.step_store()
+    h_inputs = {
+        "q": wl.q().view(np.int16), "k_new": k_new.view(np.int16), "v_new": v_new.view(np.int16),
+        "slot_mapping": slots, "seq_lens": wl.seq_lens.astype(np.int32),
+        "req_pool_indices": wl.req_pool_indices.astype(np.int32),
+    }
+    views = {"q": tdt[wl.q_dtype], "k_new": tdt[wl.in_dtype], "v_new": tdt[wl.in_dtype]}
+
+    def typed(raw):
+        return {k: (t.view(views[k]) if k in views else t) for k, t in raw.items()}
+
+    d_raw = {k: torch.from_numpy(np.ascontiguousarray(a)).to(dev) for k, a in h_inputs.items()}
+    d_in = typed(d_raw)
+    r2t = torch.from_numpy(wl.req_to_token).to(dev)
+    step = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq, wl.max_seq_len,
+                          tdt[wl.q_dtype], num_splits=args.num_splits, device=dev)
+    plan = kvq.paged_decode_attn_plan(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
+                                      args.num_splits)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(inp, ev0=None, ev1=None):
+        kvq.kvq_block_tables_from_req_to_token(r2t, inp["req_pool_indices"], inp["seq_lens"],
+                                               step.block_tables, step.dev_err)
+        kvq.kv_store_quant(pool, inp["k_new"], inp["v_new"], inp["slot_mapping"], step.dev_err)
+        if ev0 is not None:
+            ev0.record(stream)
+        kvq.paged_decode_attn(pool, inp["q"], step.out, step.block_tables, inp["seq_lens"],
+                              wl.max_seq_len, wl.sm_scale, args.num_splits, step.workspace,
+                              step.dev_err)
+        if ev1 is not None:
+            ev1.record(stream)
+
+    launches_per_step = 3 + (1 if plan["max_splits"] > 1 else 0)
+
+    for _ in range(args.warmup):
+        one_step(d_in)
+    torch.cuda.synchronize()
+    bits = kvq.kvq_check_error(step.dev_err)
+    if bits:
+        raise RuntimeError(f"device error word {bits:#x} after warm-up")
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(uuid)
+    K = args.steps
+    ev_d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0.record(stream)
+    for i in range(K):
+        one_step(d_in, ev_d0[i], ev_d1[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    decode_ms = [ev_d0[i].elapsed_time(ev_d1[i]) for i in range(K)]
+    if dist is not None:
+        t = torch.tensor([ms_total], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    tokens_per_step = wl.batch * world
+    value = tokens_per_step / (ms_step / 1e3)
+
+    # ---- end to end through the public API with host buffers -------------------------
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                  for k, a in h_inputs.items()}
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        e_raw = {k: torch.empty_like(v) for k, v in d_raw.items()}
+        e_in = typed(e_raw)
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for key, t in pinned.items():
+                e_raw[key].copy_(t, non_blocking=True)
+            one_step(e_in)
+            out_host.copy_(step.out, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if not torch.equal(out_host.to(dev), step.out):
+            raise RuntimeError("end-to-end output differs from the device-resident step")
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ms_e2e], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": tokens_per_step / (ms_e2e / K / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    bits = kvq.kvq_check_error(step.dev_err)
+    if bits:
+        raise RuntimeError(f"device error word {bits:#x} after the timed steps")
+
+    # ---- roofline of the dominant call (decode + combine) ---------------------------
+    alg = decode_algorithmic_bytes(wl)
+    uniq = unique_decode_bytes(wl)
+    mean_decode_ms = float(np.mean(decode_ms))
+    peak, peak_kind = measured_peak()
+    achieved = alg / (mean_decode_ms / 1e3) / 1e9
+    traffic, sha = traffic_from_profile(wl.name)
+    roofline = {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4), "traffic": traffic,
+        "kernel": "paged_decode_attn (decode_kernel + combine_kernel)",
+        "peak_kind": f"{peak_kind} (hbm_gbs)",
+        "algorithmic_bytes_per_launch": alg, "unique_bytes_per_launch": uniq,
+        "decode_ms_mean": round(mean_decode_ms, 5),
+        "decode_ms_median": round(float(np.median(decode_ms)), 5),
+        "decode_ms_min": round(float(np.min(decode_ms)), 5),
+        "decode_ms_max": round(float(np.max(decode_ms)), 5),
+        "unique_frac": round(uniq / (mean_decode_ms / 1e3) / 1e9 / peak, 4),
+        "kernel_source_sha": sha,
+    }
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"int8": "u8", "int4": "u4", "f16": "f16", "bf16": "bf16"}[wl.kv_dtype],
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {**workload_desc(wl), "l2": "no flush: the pool is larger than L2",
+                   "plan": plan, "parallelism": f"replicas x{world} (no data-path collective)"},
+        "roofline": roofline, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "decode_hbm_gbs": round(achieved, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, budget_s=20.0)
+    return result
+
+
+# ---- the oracle as the CPU baseline / reference arm ---------------------------------
+
+def _oracle_sample(wl, n_req: int):
+    """Compact oracle pools of the first n_req requests, context stored (setup)."""
+    import oracle
+    reqs = []
+    for b in range(n_req):
+        L = int(wl.seq_lens[b])
+        nblk = max(1, (L + 15) // 16)
+        pool = oracle.Pool(nblk, wl.kv_heads, wl.head_dim, wl.kv_dtype)
+        if L > 1:
+            k = wl.ctx_rows("k", b, 0, L - 1)
+            v = wl.ctx_rows("v", b, 0, L - 1)
+            oracle.kv_store(pool, k, v, wl.in_dtype, np.arange(L - 1, dtype=np.int64))
+        r2t = np.arange(max(L, 16), dtype=np.int32)[None]
+        reqs.append((b, L, pool, r2t))
+    return reqs
+
+
+def _oracle_step(wl, reqs, q, k_new, v_new):
+    """One step of the oracle over the sampled requests: block table, store of
+    the new token, decode of every q head."""
+    import oracle
+    outs = []
+    for b, L, pool, r2t in reqs:
+        nblk = max(1, (L + 15) // 16)
+        bt, err = oracle.block_tables(r2t, np.array([0], np.int32), np.array([L], np.int32),
+                                      nblk)
+        if L > 0:
+            oracle.kv_store(pool, k_new[b:b + 1], v_new[b:b + 1], wl.in_dtype,
+                            np.array([L - 1], np.int64))
+        outs.append(oracle.paged_decode(pool, q[b:b + 1], wl.q_dtype, bt,
+                                        np.array([L], np.int32), wl.sm_scale))
+    return outs
+
+
+def cpu_baseline(wl, budget_s: float = 20.0, n_req: int = 0) -> dict:
+    q = wl.q()
+    k_new, v_new = wl.new_rows("k"), wl.new_rows("v")
+    if n_req <= 0:
+        probe = _oracle_sample(wl, 1)
+        t = time.perf_counter()
+        _oracle_step(wl, probe, q, k_new, v_new)
+        per_req = time.perf_counter() - t
+        n_req = int(max(1, min(wl.batch, budget_s / max(per_req, 1e-6))))
+    reqs = _oracle_sample(wl, n_req)
+    t = time.perf_counter()
+    _oracle_step(wl, reqs, q, k_new, v_new)
+    dt = time.perf_counter() - t
+    return {"value": round(n_req / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_req} of the {wl.batch} requests of one step (block table, store of "
+                      f"the new token, fp64 decode of all {wl.q_heads} q heads), "
+                      f"{dt:.1f} s on one host core"}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    wl = make_workload(args.workload, args.batch, 0)
+    q = wl.q()
+    k_new, v_new = wl.new_rows("k"), wl.new_rows("v")
+    probe = _oracle_sample(wl, 1)
+    t = time.perf_counter()
+    _oracle_step(wl, probe, q, k_new, v_new)
+    per_req = time.perf_counter() - t
+    budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    n_req = int(max(1, min(wl.batch, budget / max(per_req, 1e-6))))
+    reqs = _oracle_sample(wl, n_req)
+    for _ in range(args.warmup):
+        _oracle_step(wl, reqs, q, k_new, v_new)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        _oracle_step(wl, reqs, q, k_new, v_new)
+        times.append(time.perf_counter() - t)
+    ms = float(np.mean(times)) * 1e3
+    value = n_req / (ms / 1e3)
+    sample = (f"{n_req} of the {wl.batch} requests per step (block table, store of the new "
+              f"token, fp64 decode of all {wl.q_heads} q heads)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {**workload_desc(wl), "reference": "CPU oracle (oracle/kvq_oracle.cpp), "
+                   "single-threaded; the pages ship no code to install"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+    else:
+        res = run_ours(args, rank, world, dist)
+    if rank == 0 and res is not None:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(line + "\n")
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

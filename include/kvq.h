@@ -1,0 +1,226 @@
+/*
+ * kvq.h -- C ABI of libkvq: a paged, quantized KV store and paged decode
+ * attention for one GPU (NVIDIA GB300, sm_103a).
+ *
+ * Problem model (as the source pages describe it):
+ *  - "pymllm Runtime Design", section "KV cache 与 prefix cache": a
+ *    ReqToTokenPool maps (request slot, position) to an integer kv index, a
+ *    free list hands those indices out, and a KVPool keeps each layer's K and
+ *    V tensors on the GPU, written by a store kernel (store_cache).
+ *  - LMDeploy article (devpress.csdn.net), §2.2 "分块 KV 缓存": the cache is
+ *    split into blocks of 16 tokens; each sequence keeps a table of physical
+ *    block ids; the per-layer shape is [num_blocks, block_size, kv_heads,
+ *    head_dim].
+ *  - same article, §2.4 "KV Cache 在线量化": K/V may be stored as INT8 or INT4
+ *    with per-head, per-token asymmetric min/max quantization computed online
+ *    (quant_policy 8 or 4).
+ *  - same article, §3.2 item 3 and §4.2: decode ("generation") attention reads
+ *    the non-contiguous cache through indirect block pointers in a kernel of
+ *    its own.
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument except the ones documented as host pointers is a
+ *    DEVICE pointer on the current CUDA device. The caller owns all memory;
+ *    the library never allocates, frees or synchronizes (except
+ *    kvq_check_error, which synchronizes its stream).
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream. Work is enqueued asynchronously on it.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a KVQ_ERR_* status and launches nothing.
+ *  - Data-dependent faults (a slot past the pool, a block id outside the
+ *    pool, a length past the table) are never trapped on the device: the
+ *    offending access is skipped and a bit is OR-ed into the caller's device
+ *    error word `dev_err` (an int32 in device memory; NULL disables the
+ *    report). Read it with kvq_check_error.
+ *  - Block size is 16 tokens and head_dim is 128.
+ *  - Pool and tensor base pointers must be 16-byte aligned.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  KVQ_ERR_UNSUPPORTED = 2,   /* valid but unsupported combination (dtype, head_dim...) */
+  KVQ_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed */
+  KVQ_ERR_OUT_OF_RANGE = 4,  /* kvq_check_error: the device error word was non-zero */
+  KVQ_ERR_WORKSPACE = 5      /* workspace missing or smaller than required */
+} kvq_status;
+
+/* Element kinds. INT8/INT4 use the pages' quant_policy numbers. */
+typedef enum kvq_dtype {
+  KVQ_F16 = 0,
+  KVQ_BF16 = 1,
+  KVQ_INT4 = 4,
+  KVQ_INT8 = 8
+} kvq_dtype;
+
+/* Bits of the device error word. */
+#define KVQ_DEV_ERR_REQ_SLOT 1u    /* block tables: request slot outside the ReqToTokenPool */
+#define KVQ_DEV_ERR_LENGTH 2u      /* a length past the pool row, the table or max_seq_len */
+#define KVQ_DEV_ERR_KV_INDEX 4u    /* block tables: negative kv index in a used position */
+#define KVQ_DEV_ERR_NOT_BLOCKED 8u /* block tables: row not block-contiguous */
+#define KVQ_DEV_ERR_SLOT 16u       /* store: slot >= num_blocks * 16 (token skipped) */
+#define KVQ_DEV_ERR_BLOCK_ID 32u   /* decode: block id outside [0, num_blocks) (block skipped) */
+
+/*
+ * One layer's KV pool (KVPool of "pymllm Runtime Design"; shape from LMDeploy
+ * article §2.2). slot = block_id * 16 + offset is the pool's kv index.
+ *  k, v   : [num_blocks, 16, kv_heads, row] where row is head_dim 16-bit
+ *           elements (F16/BF16), head_dim bytes (INT8 codes) or head_dim / 2
+ *           bytes (INT4, two codes per byte, even index in the low nibble).
+ *  k_sz, v_sz : INT8/INT4 only, else NULL. Pairs of fp16 (scale, zero), scale
+ *           first, laid out [num_blocks, kv_heads, 16]: the 16 pairs of one
+ *           (block, head) are contiguous. A code c stands for c * scale + zero
+ *           (LMDeploy article §2.4: per-head, per-token asymmetric).
+ */
+typedef struct kvq_pool {
+  void* k;
+  void* v;
+  void* k_sz;
+  void* v_sz;
+  int64_t num_blocks;
+  int32_t block_size; /* must be 16 */
+  int32_t kv_heads;
+  int32_t head_dim;   /* must be 128 */
+  int32_t kv_dtype;   /* kvq_dtype */
+} kvq_pool;
+
+/*
+ * kv_store_quant -- write the K/V rows of num_tokens new tokens into the pool
+ * ("pymllm Runtime Design": KVPool.set_kv through the store_cache kernel;
+ * LMDeploy article §2.4 for the quantization).
+ *
+ *  k_new, v_new : [num_tokens, kv_heads, head_dim] elements of in_dtype
+ *                 (KVQ_F16 or KVQ_BF16), contiguous.
+ *  slot_mapping : [num_tokens] int64 kv indices ("out_cache_loc"); a negative
+ *                 slot skips the token; a slot >= num_blocks * 16 is skipped
+ *                 and reported as KVQ_DEV_ERR_SLOT.
+ *  For F16/BF16 pools in_dtype must equal the pool dtype and rows are copied.
+ *  For INT8/INT4 pools each (token, head) row x of K and of V is quantized:
+ *    mn = min x, mx = max x (a signed zero taken as +0), in fp32
+ *    scale = fp16_rne((mx - mn) / (2^b - 1)),  zero = fp16_rne(mn)
+ *    code_i = clamp(rne((x_i - zero) / scale), 0, 2^b - 1)   (IEEE fp32)
+ *    and all codes are 0 when scale is 0 or not finite or zero not finite.
+ *  Inputs must be finite; bf16 inputs beyond the fp16 range are outside the
+ *  contract (their scale/zero saturate). Tokens that share a slot race.
+ *  Returns KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED or KVQ_ERR_CUDA.
+ */
+kvq_status kv_store_quant(const kvq_pool* pool, const void* k_new, const void* v_new,
+                          int32_t in_dtype, const int64_t* slot_mapping, int64_t num_tokens,
+                          int32_t* dev_err, void* stream);
+
+/*
+ * kvq_block_tables_from_req_to_token -- derive each request's block table
+ * from its ReqToTokenPool row ("pymllm Runtime Design": (request slot,
+ * position) -> kv index; LMDeploy article §2.2: per-sequence block table,
+ * block size 16).
+ *
+ *  req_to_token     : [num_req_slots, max_context_len] int32, row-major.
+ *  req_pool_indices : [batch] int32 request slot of each request.
+ *  seq_lens         : [batch] int32 tokens of each request (device).
+ *  block_tables     : [batch, max_blocks_per_seq] int32 output:
+ *                     entry j = req_to_token[r][16 j] / 16 for j < ceil(L/16),
+ *                     -1 after that.
+ *  The row must be block-contiguous (req_to_token[r][16 j + i] == 16 * entry j
+ *  + i for every position below L); violations set KVQ_DEV_ERR_NOT_BLOCKED,
+ *  negative indices KVQ_DEV_ERR_KV_INDEX, a request slot out of range
+ *  KVQ_DEV_ERR_REQ_SLOT (its row is left all -1) and a length past the row or
+ *  the table KVQ_DEV_ERR_LENGTH (the length is clamped).
+ */
+kvq_status kvq_block_tables_from_req_to_token(const int32_t* req_to_token,
+                                              int32_t num_req_slots, int32_t max_context_len,
+                                              const int32_t* req_pool_indices,
+                                              const int32_t* seq_lens, int32_t batch,
+                                              int32_t max_blocks_per_seq, int32_t* block_tables,
+                                              int32_t* dev_err, void* stream);
+
+/*
+ * Launch plan of paged_decode_attn (host-only arithmetic; no device access
+ * when num_sms > 0). The context of each request is cut into chunks of
+ * chunk_blocks blocks; each (request, kv head, chunk) is one work item of a
+ * persistent grid of grid_ctas CTAs. Requests longer than one chunk write
+ * partial results (running max, sum, unnormalised output) to the workspace
+ * and a combine kernel merges them (log-sum-exp).
+ *  num_splits      : 0 = choose automatically; else the wanted number of
+ *                    chunks for the longest request (clamped to [1, blocks]).
+ *  num_sms         : SMs to plan for; 0 = ask the current device.
+ */
+typedef struct kvq_decode_plan {
+  int32_t chunk_blocks;     /* blocks (of 16 tokens) per work item */
+  int32_t max_splits;       /* chunks of the longest request */
+  int32_t head_groups;      /* q heads of one kv head are taken 8 at a time */
+  int32_t grid_ctas;        /* persistent CTAs launched */
+  int32_t num_sms;
+  int32_t reserved;
+  size_t workspace_bytes;   /* 0 when max_splits == 1 */
+} kvq_decode_plan;
+
+kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len, int32_t num_splits,
+                                  int32_t num_sms, kvq_decode_plan* plan);
+
+/* Workspace bytes paged_decode_attn needs for these sizes on the current
+ * device (0 if none). Returns 0 as well for invalid sizes. */
+size_t paged_decode_attn_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                        int32_t head_dim, int32_t max_seq_len,
+                                        int32_t num_splits);
+
+/*
+ * paged_decode_attn -- single-token decode attention for a continuous batch
+ * over the paged pool (LMDeploy article §3.2 item 3 and §4.2; §2.2 for the
+ * block tables).
+ *
+ *  q            : [batch, q_heads, head_dim] of q_dtype (KVQ_F16/KVQ_BF16).
+ *                 For F16/BF16 pools q_dtype must equal the pool dtype.
+ *  out          : [batch, q_heads, head_dim] of q_dtype.
+ *  block_tables : [batch, max_blocks_per_seq] int32 physical block ids.
+ *  seq_lens     : [batch] int32 context length of each request, counting the
+ *                 token just stored; 0 gives an all-zero output row.
+ *  max_seq_len  : host upper bound of seq_lens (sizes the plan); longer
+ *                 requests are clamped and flagged KVQ_DEV_ERR_LENGTH.
+ *  sm_scale     : softmax scale (e.g. 1/sqrt(head_dim)).
+ *  num_splits   : as in paged_decode_attn_plan.
+ *  workspace    : device scratch of at least
+ *                 paged_decode_attn_workspace_size(...) bytes (may be NULL
+ *                 when that is 0), 16-byte aligned.
+ * For request b and q head h (kv head h / (q_heads / kv_heads)):
+ *   out[b][h] = sum_t softmax_t(sm_scale * q . k_t) v_t over t < seq_lens[b],
+ * with k_t, v_t read from slot block_tables[b][t / 16] * 16 + t % 16 and
+ * dequantized (c * scale + zero) for INT8/INT4 pools. Accumulation is fp32,
+ * the result is rounded once to q_dtype. Block ids outside the pool are
+ * skipped and flagged KVQ_DEV_ERR_BLOCK_ID.
+ */
+kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+                             int32_t max_seq_len, float sm_scale, int32_t num_splits,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                             void* stream);
+
+/*
+ * kvq_check_error -- synchronize `stream`, read the device error word and
+ * clear it. Returns KVQ_OK if it was 0, KVQ_ERR_OUT_OF_RANGE otherwise (the
+ * bits are stored to *bits_out when bits_out is not NULL), KVQ_ERR_CUDA if the
+ * stream reported an error.
+ */
+kvq_status kvq_check_error(int32_t* dev_err, uint32_t* bits_out, void* stream);
+
+/* Short text for a status code (static storage). */
+const char* kvq_status_string(kvq_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,276 @@
+"""Python binding of libkvq: paged, quantized KV store + paged decode attention.
+
+A thin ctypes layer over the C ABI declared in ``include/kvq.h``. Functions
+keep the C names; they take torch tensors (device memory) and pass raw
+pointers, sizes and the current CUDA stream. Every step of the computation
+runs in libkvq's CUDA kernels; this module only marshals arguments. If the
+shared library is missing or cannot be loaded, ``load()`` raises: there is no
+fallback.
+
+Pages followed (see the header for details): "pymllm Runtime Design"
+(ReqToTokenPool / KVPool / store_cache) and the LMDeploy article on
+devpress.csdn.net (§2.2 blocked KV cache, §2.4 online INT8/INT4 KV
+quantization, §3.2 and §4.2 paged decode attention).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+KVQ_F16, KVQ_BF16, KVQ_INT4, KVQ_INT8 = 0, 1, 4, 8
+DTYPE_CODES = {"f16": KVQ_F16, "bf16": KVQ_BF16, "int4": KVQ_INT4, "int8": KVQ_INT8}
+BLOCK_SIZE = 16
+HEAD_DIM = 128
+
+DEV_ERR_BITS = {
+    "req_slot": 1, "length": 2, "kv_index": 4, "not_blocked": 8, "slot": 16, "block_id": 32,
+}
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+           4: "device reported an out-of-range index or length", 5: "workspace"}
+
+_lib = None
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_sz", ctypes.c_void_p),
+                ("v_sz", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+                ("block_size", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("chunk_blocks", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("head_groups", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decode_attn_plan",
+            "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
+            "kvq_status_string", "kvq_version"]
+
+
+def load(build_if_missing: bool = False):
+    """Load libkvq.so (optionally building it first). Raises when unavailable."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkvq is not built ({LIB_PATH} missing); run "
+                          "__graft_entry__.build() or paged_quantized_kv_store_gb300._build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, SZ, F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t,
+                          ctypes.c_float)
+    lib.kv_store_quant.argtypes = [ctypes.POINTER(_Pool), P, P, I32, P, I64, P, P]
+    lib.kv_store_quant.restype = ctypes.c_int
+    lib.kvq_block_tables_from_req_to_token.argtypes = [P, I32, I32, P, P, I32, I32, P, P, P]
+    lib.kvq_block_tables_from_req_to_token.restype = ctypes.c_int
+    lib.paged_decode_attn_plan.argtypes = [I32, I32, I32, I32, I32, I32, I32,
+                                           ctypes.POINTER(_Plan)]
+    lib.paged_decode_attn_plan.restype = ctypes.c_int
+    lib.paged_decode_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32]
+    lib.paged_decode_attn_workspace_size.restype = SZ
+    lib.paged_decode_attn.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, I32, P, I32, I32, I32,
+                                      F, I32, P, SZ, P, P]
+    lib.paged_decode_attn.restype = ctypes.c_int
+    lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.kvq_check_error.restype = ctypes.c_int
+    lib.kvq_status_string.argtypes = [ctypes.c_int]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    lib.kvq_version.argtypes = []
+    lib.kvq_version.restype = I32
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    h = getattr(stream, "cuda_stream", stream)
+    return h or None
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KvqError(status, where)
+
+
+@dataclass
+class KVPool:
+    """One layer's KV pool on the device (KVPool of "pymllm Runtime Design").
+
+    k, v: uint8/int16 tensors [num_blocks, 16, kv_heads, row] where row is
+    head_dim 16-bit elements (f16/bf16), head_dim bytes (int8) or head_dim/2
+    bytes (int4); k_sz, v_sz: int32 [num_blocks, kv_heads, 16] holding fp16
+    (scale, zero) pairs, or None for f16/bf16 pools.
+    """
+
+    k: object
+    v: object
+    k_sz: object
+    v_sz: object
+    num_blocks: int
+    kv_heads: int
+    kv_dtype: str
+    head_dim: int = HEAD_DIM
+
+    @staticmethod
+    def allocate(num_blocks: int, kv_heads: int, kv_dtype: str, device="cuda",
+                 head_dim: int = HEAD_DIM) -> "KVPool":
+        """Zero-filled pool tensors (allocation is the caller's side of the ABI)."""
+        import torch
+        row = {"f16": 2 * head_dim, "bf16": 2 * head_dim, "int8": head_dim,
+               "int4": head_dim // 2}[kv_dtype]
+        shape = (num_blocks, BLOCK_SIZE, kv_heads, row)
+        k = torch.zeros(shape, dtype=torch.uint8, device=device)
+        v = torch.zeros(shape, dtype=torch.uint8, device=device)
+        if kv_dtype in ("int8", "int4"):
+            szs = (num_blocks, kv_heads, BLOCK_SIZE)
+            k_sz = torch.zeros(szs, dtype=torch.int32, device=device)
+            v_sz = torch.zeros(szs, dtype=torch.int32, device=device)
+        else:
+            k_sz = v_sz = None
+        return KVPool(k, v, k_sz, v_sz, num_blocks, kv_heads, kv_dtype, head_dim)
+
+    def c_struct(self) -> _Pool:
+        return _Pool(_ptr(self.k), _ptr(self.v), _ptr(self.k_sz), _ptr(self.v_sz),
+                     self.num_blocks, BLOCK_SIZE, self.kv_heads, self.head_dim,
+                     DTYPE_CODES[self.kv_dtype])
+
+    def nbytes(self) -> int:
+        n = self.k.numel() + self.v.numel()
+        if self.k_sz is not None:
+            n += 4 * (self.k_sz.numel() + self.v_sz.numel())
+        return n
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return KVQ_F16
+    if t.dtype == torch.bfloat16:
+        return KVQ_BF16
+    raise TypeError(f"expected float16 or bfloat16 tensor, got {t.dtype}")
+
+
+def kv_store_quant(pool: KVPool, k_new, v_new, slot_mapping, dev_err=None, stream=None):
+    """Store new K/V rows [N, Hkv, D] at slot_mapping (int64 [N]); see kvq.h."""
+    lib = load()
+    ps = pool.c_struct()
+    st = lib.kv_store_quant(ctypes.byref(ps), _ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                            _ptr(slot_mapping), int(slot_mapping.numel()), _ptr(dev_err),
+                            _stream(stream))
+    _check(st, "kv_store_quant")
+
+
+def kvq_block_tables_from_req_to_token(req_to_token, req_pool_indices, seq_lens, block_tables,
+                                       dev_err=None, stream=None):
+    """Fill block_tables [B, max_blocks] (int32) from ReqToTokenPool rows; see kvq.h."""
+    lib = load()
+    st = lib.kvq_block_tables_from_req_to_token(
+        _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]),
+        _ptr(req_pool_indices), _ptr(seq_lens), int(seq_lens.numel()),
+        int(block_tables.shape[1]), _ptr(block_tables), _ptr(dev_err), _stream(stream))
+    _check(st, "kvq_block_tables_from_req_to_token")
+
+
+def paged_decode_attn_plan(batch, q_heads, kv_heads, max_seq_len, num_splits=0, num_sms=0,
+                           head_dim=HEAD_DIM) -> dict:
+    """Host-side launch plan (no device access when num_sms > 0)."""
+    lib = load()
+    p = _Plan()
+    st = lib.paged_decode_attn_plan(batch, q_heads, kv_heads, head_dim, max_seq_len, num_splits,
+                                    num_sms, ctypes.byref(p))
+    _check(st, "paged_decode_attn_plan")
+    return {f: getattr(p, f) for f, _ in _Plan._fields_}
+
+
+def paged_decode_attn_workspace_size(batch, q_heads, kv_heads, max_seq_len, num_splits=0,
+                                     head_dim=HEAD_DIM) -> int:
+    return int(load().paged_decode_attn_workspace_size(batch, q_heads, kv_heads, head_dim,
+                                                       max_seq_len, num_splits))
+
+
+def paged_decode_attn(pool: KVPool, q, out, block_tables, seq_lens, max_seq_len, sm_scale,
+                      num_splits=0, workspace=None, dev_err=None, stream=None):
+    """out[b, h] = softmax(sm_scale q[b, h] . K_b) V_b over the paged pool; see kvq.h."""
+    lib = load()
+    ps = pool.c_struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.paged_decode_attn(ctypes.byref(ps), _ptr(q), _dtype_code(q), _ptr(out),
+                               _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens),
+                               int(q.shape[0]), int(q.shape[1]), int(max_seq_len),
+                               float(sm_scale), int(num_splits), _ptr(workspace), ws_bytes,
+                               _ptr(dev_err), _stream(stream))
+    _check(st, "paged_decode_attn")
+
+
+def kvq_check_error(dev_err, stream=None) -> int:
+    """Synchronize, read and clear the device error word; returns its bits."""
+    lib = load()
+    bits = ctypes.c_uint32(0)
+    st = lib.kvq_check_error(_ptr(dev_err), ctypes.byref(bits), _stream(stream))
+    if st not in (0, 4):
+        _check(st, "kvq_check_error")
+    return int(bits.value)
+
+
+def kvq_status_string(status: int) -> str:
+    return load().kvq_status_string(status).decode()
+
+
+def kvq_version() -> int:
+    return int(load().kvq_version())
+
+
+class DecodeStep:
+    """One decode step of a layer through the C ABI: block tables, store, attention.
+
+    Holds the per-step device buffers (block tables, workspace, error word) so
+    the call itself allocates nothing.
+    """
+
+    def __init__(self, pool: KVPool, batch: int, q_heads: int, max_blocks_per_seq: int,
+                 max_seq_len: int, q_dtype, num_splits: int = 0, device="cuda"):
+        import torch
+        self.pool = pool
+        self.batch = batch
+        self.q_heads = q_heads
+        self.max_seq_len = max_seq_len
+        self.num_splits = num_splits
+        self.block_tables = torch.empty((batch, max_blocks_per_seq), dtype=torch.int32,
+                                        device=device)
+        ws = paged_decode_attn_workspace_size(batch, q_heads, pool.kv_heads, max_seq_len,
+                                              num_splits)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.out = torch.empty((batch, q_heads, pool.head_dim), dtype=q_dtype, device=device)
+
+    def __call__(self, req_to_token, req_pool_indices, seq_lens, q, k_new, v_new, slot_mapping,
+                 sm_scale, stream=None):
+        kvq_block_tables_from_req_to_token(req_to_token, req_pool_indices, seq_lens,
+                                           self.block_tables, self.dev_err, stream)
+        kv_store_quant(self.pool, k_new, v_new, slot_mapping, self.dev_err, stream)
+        paged_decode_attn(self.pool, q, self.out, self.block_tables, seq_lens, self.max_seq_len,
+                          sm_scale, self.num_splits, self.workspace, self.dev_err, stream)
+        return self.out

@@ -1,0 +1,249 @@
+// C ABI of libkvq: argument validation, launch planning and dispatch.
+// The declarations, with the passages of the source pages each entry point
+// follows, are in include/kvq.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+using kvq::kBlock;
+using kvq::kHeadDim;
+
+namespace {
+
+constexpr int kPlanCtasPerSm = 4;     // persistent decode CTAs per SM
+constexpr int kItemsPerCta = 8;       // work items the planner aims for per CTA
+constexpr int kAutoMinChunk = 16;     // blocks (256 tokens)
+constexpr int kAutoMaxChunk = 32;     // blocks (512 tokens)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool is_quant(int dt) { return dt == KVQ_INT8 || dt == KVQ_INT4; }
+bool is_float16(int dt) { return dt == KVQ_F16 || dt == KVQ_BF16; }
+
+kvq_status check_pool(const kvq_pool* p) {
+  if (p == nullptr || p->k == nullptr || p->v == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (p->num_blocks < 0 || p->kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (p->block_size != kBlock || p->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (!is_quant(p->kv_dtype) && !is_float16(p->kv_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(p->k) || !aligned16(p->v)) return KVQ_ERR_INVALID_ARG;
+  if (is_quant(p->kv_dtype)) {
+    if (p->k_sz == nullptr || p->v_sz == nullptr) return KVQ_ERR_INVALID_ARG;
+    if (!aligned4(p->k_sz) || !aligned4(p->v_sz)) return KVQ_ERR_INVALID_ARG;
+  }
+  return KVQ_OK;
+}
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvq_version(void) { return 100; }
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_OUT_OF_RANGE: return "device reported an out-of-range index or length";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+kvq_status kv_store_quant(const kvq_pool* pool, const void* k_new, const void* v_new,
+                          int32_t in_dtype, const int64_t* slot_mapping, int64_t num_tokens,
+                          int32_t* dev_err, void* stream) {
+  const kvq_status ps = check_pool(pool);
+  if (ps != KVQ_OK) return ps;
+  if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (!is_float16(in_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (is_float16(pool->kv_dtype) && in_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return KVQ_OK;
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  kvq::StoreArgs a;
+  a.k_pool = pool->k;
+  a.v_pool = pool->v;
+  a.k_sz = pool->k_sz;
+  a.v_sz = pool->v_sz;
+  a.num_blocks = pool->num_blocks;
+  a.kv_heads = pool->kv_heads;
+  a.kv_dtype = pool->kv_dtype;
+  a.in_dtype = in_dtype;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.dev_err = dev_err;
+  return kvq::launch_store(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK
+                                                                                  : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_block_tables_from_req_to_token(const int32_t* req_to_token,
+                                              int32_t num_req_slots, int32_t max_context_len,
+                                              const int32_t* req_pool_indices,
+                                              const int32_t* seq_lens, int32_t batch,
+                                              int32_t max_blocks_per_seq, int32_t* block_tables,
+                                              int32_t* dev_err, void* stream) {
+  if (batch < 0 || num_req_slots < 0 || max_context_len < 0 || max_blocks_per_seq <= 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (req_to_token == nullptr || req_pool_indices == nullptr || seq_lens == nullptr ||
+      block_tables == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  kvq::TablesArgs a{req_to_token, num_req_slots, max_context_len, req_pool_indices, seq_lens,
+                    batch, max_blocks_per_seq, block_tables, dev_err};
+  return kvq::launch_tables(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK
+                                                                                  : KVQ_ERR_CUDA;
+}
+
+kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len, int32_t num_splits,
+                                  int32_t num_sms, kvq_decode_plan* plan) {
+  if (plan == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (batch < 0 || q_heads <= 0 || kv_heads <= 0 || max_seq_len < 0 || num_splits < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (q_heads % kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (batch > kvq::kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  if (num_sms <= 0) num_sms = current_sm_count();
+  if (num_sms <= 0) return KVQ_ERR_CUDA;
+  const int group = q_heads / kv_heads;
+  const int head_groups = (group + 7) / 8;
+  const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
+  const int grid = num_sms * kPlanCtasPerSm;
+  int chunk;
+  if (num_splits > 0) {
+    const int s = std::min(num_splits, nblk);
+    chunk = (nblk + s - 1) / s;
+  } else {
+    // enough work items for every CTA, chunks of 256 to 512 tokens
+    const int64_t unsplit = static_cast<int64_t>(batch) * kv_heads * head_groups;
+    const int64_t want = static_cast<int64_t>(kItemsPerCta) * grid;
+    const int64_t s = unsplit > 0 ? std::max<int64_t>(1, (want + unsplit - 1) / unsplit) : 1;
+    chunk = static_cast<int>((nblk + s - 1) / s);
+    chunk = std::max(chunk, kAutoMinChunk);
+    chunk = std::min(chunk, kAutoMaxChunk);
+    chunk = std::min(chunk, nblk);
+  }
+  chunk = std::max(1, std::min(chunk, kvq::kMaxChunkBlocks));
+  const int splits = (nblk + chunk - 1) / chunk;
+  plan->chunk_blocks = chunk;
+  plan->max_splits = splits;
+  plan->head_groups = head_groups;
+  plan->grid_ctas = grid;
+  plan->num_sms = num_sms;
+  plan->reserved = 0;
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(batch) * q_heads * splits;
+    plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(float), 256) +
+                            align_up(rows * sizeof(float) * 2, 256);
+  } else {
+    plan->workspace_bytes = 0;
+  }
+  return KVQ_OK;
+}
+
+size_t paged_decode_attn_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                        int32_t head_dim, int32_t max_seq_len,
+                                        int32_t num_splits) {
+  kvq_decode_plan p;
+  if (paged_decode_attn_plan(batch, q_heads, kv_heads, head_dim, max_seq_len, num_splits, 0,
+                             &p) != KVQ_OK)
+    return 0;
+  return p.workspace_bytes;
+}
+
+kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+                             int32_t max_seq_len, float sm_scale, int32_t num_splits,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                             void* stream) {
+  const kvq_status ps = check_pool(pool);
+  if (ps != KVQ_OK) return ps;
+  if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (is_float16(pool->kv_dtype) && q_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
+  if (batch < 0 || q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  kvq_decode_plan plan;
+  const kvq_status st = paged_decode_attn_plan(batch, q_heads, pool->kv_heads, pool->head_dim,
+                                               max_seq_len, num_splits, 0, &plan);
+  if (st != KVQ_OK) return st;
+  if (batch == 0) return KVQ_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
+  if (plan.workspace_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return KVQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  }
+  kvq::DecodeArgs a;
+  a.k = static_cast<const uint8_t*>(pool->k);
+  a.v = static_cast<const uint8_t*>(pool->v);
+  a.k_sz = static_cast<const uint32_t*>(pool->k_sz);
+  a.v_sz = static_cast<const uint32_t*>(pool->v_sz);
+  a.num_blocks = pool->num_blocks;
+  a.kv_heads = pool->kv_heads;
+  a.q = q;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_heads = q_heads;
+  a.group = q_heads / pool->kv_heads;
+  a.head_groups = plan.head_groups;
+  a.chunk_blocks = plan.chunk_blocks;
+  a.max_splits = plan.max_splits;
+  a.len_cap = std::min(max_blocks_per_seq, plan.max_splits * plan.chunk_blocks) * kBlock;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  if (plan.max_splits > 1) {
+    const size_t rows = static_cast<size_t>(batch) * q_heads * plan.max_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                          align_up(rows * kHeadDim * sizeof(float), 256));
+  } else {
+    a.part_o = nullptr;
+    a.part_ml = nullptr;
+  }
+  a.dev_err = dev_err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, plan.grid_ctas, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (plan.max_splits > 1 && kvq::launch_combine(a, q_dtype, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_check_error(int32_t* dev_err, uint32_t* bits_out, void* stream) {
+  if (dev_err == nullptr) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, dev_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (v != 0 && cudaMemset(dev_err, 0, sizeof(v)) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (bits_out != nullptr) *bits_out = static_cast<uint32_t>(v);
+  return v == 0 ? KVQ_OK : KVQ_ERR_OUT_OF_RANGE;
+}
+
+}  // extern "C"

@@ -1,0 +1,594 @@
+// kvq_decode: single-token decode attention over the paged, quantized pool.
+//
+// LMDeploy article (devpress.csdn.net) §3.2 item 3: generation attention reads
+// a non-contiguous KV layout through indirect block pointers; §4.2: decoding
+// has its own hand-written kernel; §2.2: per-sequence block tables of 16-token
+// blocks; §2.4: INT8/INT4 KV with per-token, per-head scale and zero.
+//
+// Work decomposition
+//   A work item is (request b, kv head h, q-head group of up to 8, chunk s)
+//   where a chunk is `chunk_blocks` consecutive logical blocks. A persistent
+//   grid of CTAs walks the items round-robin; every CTA first scans the
+//   request lengths into per-request chunk counts in shared memory so that
+//   short requests cost no empty CTAs. All q heads of a kv head's group are
+//   handled by the same CTA, so every KV byte is read from HBM once.
+//   Inside a CTA, 4 warps take the chunk's blocks round-robin, each keeping
+//   its own online-softmax state, and merge through shared memory at the end.
+//   A request covered by one chunk writes its output directly; longer ones
+//   write (running max, sum, unnormalised output) partials that the combine
+//   kernel merges with a log-sum-exp.
+//
+// Per-block arithmetic of one warp (16 tokens of one kv head):
+//   S^T = K Q^T  with mma.m16n8k16: M = 16 tokens, N = 8 q heads (padded),
+//                K = 128 dims in 8 steps.
+//   O^T += V^T P'^T with M = 16 dims (8 steps over 128), N = 8 heads,
+//                K = 16 tokens.
+//   For INT8/INT4 pools the codes c go into the tensor cores exactly (as fp16
+//   or bf16 integers) and the per-token scale S and zero Z are applied
+//   outside: q.k = S (q.c) + Z sum(q); sum_t p_t v_t = sum_t (p_t S_t) c_t +
+//   sum_t p_t Z_t. The score fragment is transposed in registers
+//   (movmatrix) to become the B operand of the second product.
+//   Each lane's K and V loads are 8-32 contiguous bytes of a token row;
+//   the dims are assigned to mma k-columns so that the loads stay contiguous
+//   (the dot product does not depend on the order of the dims, and Q is
+//   permuted the same way once per item).
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = kDecodeThreads / 32;
+constexpr int kHeadsPerGroup = 8;  // mma N
+
+// ---- per-block fragments ------------------------------------------------------
+
+// Raw bytes one lane needs from one 16-token block (K rows g, g+8; V rows
+// 2t, 2t+1, 2t+8, 2t+9) plus the scale/zero words of tokens g and g+8.
+template <int KV>
+struct Frag;
+
+template <>
+struct Frag<kF16> {
+  uint4 k[2][4];   // 64 bytes of each K row: dims [32t, 32t+32)
+  uint4 v[4][2];   // 32 bytes of each V row: dims [16g, 16g+16)
+  uint32_t ksz[2], vsz[2];
+};
+template <>
+struct Frag<kBF16> : Frag<kF16> {};
+template <>
+struct Frag<kI8> {
+  uint4 k[2][2];   // 32 bytes: dims [32t, 32t+32)
+  uint4 v[4];      // 16 bytes: dims [16g, 16g+16)
+  uint32_t ksz[2], vsz[2];
+};
+template <>
+struct Frag<kI4> {
+  uint4 k[2];      // 16 bytes: dims [32t, 32t+32)
+  uint2 v[4];      // 8 bytes: dims [16g, 16g+16)
+  uint32_t ksz[2], vsz[2];
+};
+
+template <int KV>
+__device__ __forceinline__ void load_frag(Frag<KV>& f, const DecodeArgs& a, int64_t phys, int h,
+                                          int g, int t) {
+  constexpr int R = KvTraits<KV>::kRowBytes;
+  const int64_t row0 = phys * kBlock;  // first slot of the block
+  const int Hkv = a.kv_heads;
+  const uint8_t* kb = a.k + ((row0 * Hkv + h) * R);
+  const uint8_t* vb = a.v + ((row0 * Hkv + h) * R);
+  const int64_t tok_stride = static_cast<int64_t>(Hkv) * R;
+  const uint8_t* k0 = kb + g * tok_stride + t * (R / 4);
+  const uint8_t* k1 = kb + (g + 8) * tok_stride + t * (R / 4);
+  const int vr[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  if constexpr (KV == kF16 || KV == kBF16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f.k[0][i] = ldg_stream16(k0 + 16 * i);
+      f.k[1][i] = ldg_stream16(k1 + 16 * i);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint8_t* p = vb + vr[r] * tok_stride + g * (R / 8);
+      f.v[r][0] = ldg_stream16(p);
+      f.v[r][1] = ldg_stream16(p + 16);
+    }
+  } else if constexpr (KV == kI8) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      f.k[0][i] = ldg_stream16(k0 + 16 * i);
+      f.k[1][i] = ldg_stream16(k1 + 16 * i);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) f.v[r] = ldg_stream16(vb + vr[r] * tok_stride + g * (R / 8));
+  } else {
+    f.k[0] = ldg_stream16(k0);
+    f.k[1] = ldg_stream16(k1);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) f.v[r] = ldg_stream8(vb + vr[r] * tok_stride + g * (R / 8));
+  }
+  if constexpr (KvTraits<KV>::kQuant) {
+    const int64_t szb = (phys * Hkv + h) * kBlock;
+    f.ksz[0] = ldg_nc32(a.k_sz + szb + g);
+    f.ksz[1] = ldg_nc32(a.k_sz + szb + g + 8);
+    f.vsz[0] = ldg_nc32(a.v_sz + szb + g);
+    f.vsz[1] = ldg_nc32(a.v_sz + szb + g + 8);
+  }
+}
+
+__device__ __forceinline__ uint32_t w4(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// A operand of S^T = K Q^T for k-step kk: rows = tokens (g, g+8),
+// k-columns = this lane's dims (see the header comment).
+template <int KV, bool QBF>
+__device__ __forceinline__ void k_operand(const Frag<KV>& f, int kk, uint32_t (&a)[4]) {
+  if constexpr (KV == kF16 || KV == kBF16) {
+    a[0] = w4(f.k[0][kk >> 1], (2 * kk) & 3);
+    a[2] = w4(f.k[0][kk >> 1], (2 * kk + 1) & 3);
+    a[1] = w4(f.k[1][kk >> 1], (2 * kk) & 3);
+    a[3] = w4(f.k[1][kk >> 1], (2 * kk + 1) & 3);
+  } else if constexpr (KV == kI8) {
+    const uint32_t w0 = w4(f.k[0][kk >> 2], kk & 3);
+    const uint32_t w1 = w4(f.k[1][kk >> 2], kk & 3);
+    if constexpr (QBF) {
+      a[0] = bytes_to_bf16_pair(w0, 0, 1);
+      a[2] = bytes_to_bf16_pair(w0, 2, 3);
+      a[1] = bytes_to_bf16_pair(w1, 0, 1);
+      a[3] = bytes_to_bf16_pair(w1, 2, 3);
+    } else {
+      a[0] = bytes_to_f16_pair(w0, 0x4140u);
+      a[2] = bytes_to_f16_pair(w0, 0x4342u);
+      a[1] = bytes_to_f16_pair(w1, 0x4140u);
+      a[3] = bytes_to_f16_pair(w1, 0x4342u);
+    }
+  } else {
+    // kk = 2 j + u: pairs of dims (8j+2u, 8j+2u+4) and (8j+2u+1, 8j+2u+5)
+    const int j = kk >> 1, u = kk & 1;
+    const uint32_t w0 = w4(f.k[0], j), w1 = w4(f.k[1], j);
+    a[0] = nibbles_to_pair<QBF>(w0 >> (8 * u));
+    a[2] = nibbles_to_pair<QBF>(w0 >> (8 * u + 4));
+    a[1] = nibbles_to_pair<QBF>(w1 >> (8 * u));
+    a[3] = nibbles_to_pair<QBF>(w1 >> (8 * u + 4));
+  }
+}
+
+// A operand of O^T += V^T P'^T for dim step i: rows = dims (16g + 2i,
+// 16g + 2i + 1), k-columns = tokens (2t, 2t+1, 2t+8, 2t+9).
+template <int KV, bool QBF>
+__device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a)[4]) {
+  if constexpr (KV == kF16 || KV == kBF16) {
+    const uint32_t r0 = w4(f.v[0][i >> 2], i & 3), r1 = w4(f.v[1][i >> 2], i & 3);
+    const uint32_t r2 = w4(f.v[2][i >> 2], i & 3), r3 = w4(f.v[3][i >> 2], i & 3);
+    a[0] = prmt(r0, r1, 0x5410u);
+    a[1] = prmt(r0, r1, 0x7632u);
+    a[2] = prmt(r2, r3, 0x5410u);
+    a[3] = prmt(r2, r3, 0x7632u);
+  } else if constexpr (KV == kI8) {
+    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes k, k+1 of two rows, k = 2(i%2)
+    const uint32_t x01 = prmt(w4(f.v[0], i >> 1), w4(f.v[1], i >> 1), sel);
+    const uint32_t x23 = prmt(w4(f.v[2], i >> 1), w4(f.v[3], i >> 1), sel);
+    if constexpr (QBF) {
+      a[0] = bytes_to_bf16_pair(x01, 0, 1);
+      a[1] = bytes_to_bf16_pair(x01, 2, 3);
+      a[2] = bytes_to_bf16_pair(x23, 0, 1);
+      a[3] = bytes_to_bf16_pair(x23, 2, 3);
+    } else {
+      a[0] = bytes_to_f16_pair(x01, 0x4140u);
+      a[1] = bytes_to_f16_pair(x01, 0x4342u);
+      a[2] = bytes_to_f16_pair(x23, 0x4140u);
+      a[3] = bytes_to_f16_pair(x23, 0x4342u);
+    }
+  } else {
+    // i = 4 jj + 2 kk + m: bytes (2kk, 2kk+1) of word jj of the two rows,
+    // nibbles 2m and 2m+1 of each half
+    const int jj = i >> 2, kk = (i >> 1) & 1, m = i & 1;
+    const uint32_t sel = kk ? 0x7632u : 0x5410u;
+    const uint32_t r0 = jj ? f.v[0].y : f.v[0].x, r1 = jj ? f.v[1].y : f.v[1].x;
+    const uint32_t r2 = jj ? f.v[2].y : f.v[2].x, r3 = jj ? f.v[3].y : f.v[3].x;
+    const uint32_t x01 = prmt(r0, r1, sel), x23 = prmt(r2, r3, sel);
+    a[0] = nibbles_to_pair<QBF>(x01 >> (8 * m));
+    a[1] = nibbles_to_pair<QBF>(x01 >> (8 * m + 4));
+    a[2] = nibbles_to_pair<QBF>(x23 >> (8 * m));
+    a[3] = nibbles_to_pair<QBF>(x23 >> (8 * m + 4));
+  }
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+template <bool QBF>
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
+  if constexpr (QBF) {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+struct Smem {
+  float m[kWarps][kHeadsPerGroup];
+  float l[kWarps][kHeadsPerGroup];
+  float2 o[kWarps][kHeadsPerGroup][kHeadDim / 2];
+  int32_t warp_sum[kWarps];
+};
+
+// Clamped length of request b and its number of chunks (>= 1).
+__device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
+  return min(max(a.seq_lens[b], 0), a.len_cap);
+}
+
+template <int KV, bool QBF>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_kernel(DecodeArgs a) {
+  extern __shared__ int32_t cum[];  // [batch + 1] exclusive prefix of chunk counts
+  __shared__ Smem sm;
+  constexpr bool kQuant = KvTraits<KV>::kQuant;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int chunk_tokens = a.chunk_blocks * kBlock;
+
+  // ---- chunk counts of every request, prefix-summed --------------------------
+  {
+    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
+    const int b0 = min(tid * per, a.batch), b1 = min(b0 + per, a.batch);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L = clamped_len(a, b);
+      sum += max(1, (L + chunk_tokens - 1) / chunk_tokens);
+      if (blockIdx.x == 0 && a.seq_lens[b] > a.len_cap) report(a.dev_err, KVQ_DEV_ERR_LENGTH);
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) sm.warp_sum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += sm.warp_sum[w];
+    int run = base + incl - sum;
+    for (int b = b0; b < b1; ++b) {
+      cum[b] = run;
+      run += max(1, (clamped_len(a, b) + chunk_tokens - 1) / chunk_tokens);
+    }
+    if (tid == kDecodeThreads - 1) cum[a.batch] = base + incl;
+    __syncthreads();
+  }
+  const int total_chunks = cum[a.batch];
+  const int groups = a.kv_heads * a.head_groups;
+  const int64_t total_items = static_cast<int64_t>(total_chunks) * groups;
+
+  for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
+    const int hgi = static_cast<int>(item / total_chunks);
+    const int r = static_cast<int>(item % total_chunks);
+    // request: largest b with cum[b] <= r
+    int lo = 0, hi = a.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int s = r - cum[b];
+    const int h = hgi / a.head_groups;
+    const int hg = hgi - h * a.head_groups;
+    const int L = clamped_len(a, b);
+    const int n_chunks = max(1, (L + chunk_tokens - 1) / chunk_tokens);
+    const int nblk = (L + kBlock - 1) / kBlock;
+    const int blk_begin = s * a.chunk_blocks;
+    const int blk_end = min(blk_begin + a.chunk_blocks, nblk);
+    const int hq0 = h * a.group + hg * kHeadsPerGroup;
+    const int nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
+
+    // ---- Q fragments (B operand of S^T = K Q^T), permuted like the K dims --
+    uint32_t qb[8][2];
+    float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
+    {
+      uint32_t qw[16];
+      if (g < nh) {
+        const uint4* qp = reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(a.q) +
+            (static_cast<int64_t>(b) * a.q_heads + hq0 + g) * kHeadDim + 32 * t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = qp[i];
+          qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qw[i] = 0u;
+      }
+      if constexpr (KV == kI4) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int j = kk >> 1, u = kk & 1;
+          qb[kk][0] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x5410u);
+          qb[kk][1] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x7632u);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qb[kk][0] = qw[2 * kk];
+          qb[kk][1] = qw[2 * kk + 1];
+        }
+      }
+      if constexpr (kQuant) {
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) part += lo_to_float<QBF>(qw[i]) + hi_to_float<QBF>(qw[i]);
+        part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+        part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+        // lanes 4h hold sum(q) of head h
+        qs0 = __shfl_sync(0xFFFFFFFFu, part, (2 * t) * 4);
+        qs1 = __shfl_sync(0xFFFFFFFFu, part, (2 * t + 1) * 4);
+      }
+    }
+    const bool hv0 = 2 * t < nh, hv1 = 2 * t + 1 < nh;
+
+    // ---- this warp's blocks -------------------------------------------------
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks;
+    int j = blk_begin + warp;
+    int64_t phys = j < blk_end ? bt[j] : -1;
+    int64_t phys_next = j + kWarps < blk_end ? bt[j + kWarps] : -1;
+    Frag<KV> cur;
+    bool cur_ok = j < blk_end && phys >= 0 && phys < a.num_blocks;
+    if (j < blk_end && !cur_ok && lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+    if (cur_ok) load_frag<KV>(cur, a, phys, h, g, t);
+
+    for (; j < blk_end; j += kWarps) {
+      // prefetch block j + kWarps while block j is computed
+      const int jn = j + kWarps;
+      Frag<KV> nxt;
+      const bool nxt_ok = jn < blk_end && phys_next >= 0 && phys_next < a.num_blocks;
+      if (jn < blk_end && !nxt_ok && lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+      if (nxt_ok) load_frag<KV>(nxt, a, phys_next, h, g, t);
+      const int64_t phys_after = jn + kWarps < blk_end ? bt[jn + kWarps] : -1;
+
+      if (cur_ok) {
+        // S^T = K Q^T
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t ak[4];
+          k_operand<KV, QBF>(cur, kk, ak);
+          mma16816<QBF>(sc, ak, qb[kk]);
+        }
+        // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
+        const int tok0 = j * kBlock + g, tok1 = tok0 + 8;
+        float s00, s01, s10, s11;
+        if constexpr (kQuant) {
+          const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]);
+          const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]);
+          s00 = (S0 * sc[0] + Z0 * qs0) * a.sm_scale_log2;
+          s01 = (S0 * sc[1] + Z0 * qs1) * a.sm_scale_log2;
+          s10 = (S1 * sc[2] + Z1 * qs0) * a.sm_scale_log2;
+          s11 = (S1 * sc[3] + Z1 * qs1) * a.sm_scale_log2;
+        } else {
+          s00 = sc[0] * a.sm_scale_log2;
+          s01 = sc[1] * a.sm_scale_log2;
+          s10 = sc[2] * a.sm_scale_log2;
+          s11 = sc[3] * a.sm_scale_log2;
+        }
+        if (tok0 >= L) s00 = s01 = -INFINITY;
+        if (tok1 >= L) s10 = s11 = -INFINITY;
+        if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
+        if (!hv1) s01 = s11 = 0.f;
+        // block max over the 16 tokens (lanes with equal t)
+        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          bm0 = fmaxf(bm0, __shfl_xor_sync(0xFFFFFFFFu, bm0, off));
+          bm1 = fmaxf(bm1, __shfl_xor_sync(0xFFFFFFFFu, bm1, off));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+        const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
+        const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 = l0 * al0 + (p00 + p10);
+        l1 = l1 * al1 + (p01 + p11);
+        float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
+        if constexpr (kQuant) {
+          const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]);
+          const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]);
+          z0 = z0 * al0 + (p00 * Z0 + p10 * Z1);
+          z1 = z1 * al1 + (p01 * Z0 + p11 * Z1);
+          q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] *= al0; o[i][2] *= al0;
+          o[i][1] *= al1; o[i][3] *= al1;
+        }
+        // P'^T as the B operand: transpose the (token x head) fragments
+        uint32_t bp[2];
+        bp[0] = movmatrix_trans(pack2<QBF>(q00, q01));
+        bp[1] = movmatrix_trans(pack2<QBF>(q10, q11));
+        // O^T += V^T P'^T
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t av[4];
+          v_operand<KV, QBF>(cur, i, av);
+          mma16816<QBF>(o[i], av, bp);
+        }
+      }
+      cur = nxt;
+      cur_ok = nxt_ok;
+      phys_next = phys_after;
+    }
+
+    // ---- finish this warp: sums over the 8 token lanes -----------------------
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+      if constexpr (kQuant) {
+        z0 += __shfl_xor_sync(0xFFFFFFFFu, z0, off);
+        z1 += __shfl_xor_sync(0xFFFFFFFFu, z1, off);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sm.o[warp][2 * t][8 * g + i] = make_float2(o[i][0] + z0, o[i][2] + z0);
+      sm.o[warp][2 * t + 1][8 * g + i] = make_float2(o[i][1] + z1, o[i][3] + z1);
+    }
+    if (g == 0) {
+      sm.m[warp][2 * t] = m0;
+      sm.m[warp][2 * t + 1] = m1;
+      sm.l[warp][2 * t] = l0;
+      sm.l[warp][2 * t + 1] = l1;
+    }
+    __syncthreads();
+
+    // ---- merge the warps; write the output or the partial ---------------------
+    for (int idx = tid; idx < nh * kHeadDim; idx += kDecodeThreads) {
+      const int hh = idx / kHeadDim, d = idx % kHeadDim;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][hh]);
+      float acc = 0.f, lsum = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float e = exp2f(sm.m[w][hh] - M);
+          const float2 ov = sm.o[w][hh][d >> 1];
+          acc += e * ((d & 1) ? ov.y : ov.x);
+          lsum += e * sm.l[w][hh];
+        }
+      }
+      const int hq = hq0 + hh;
+      const int64_t bh = static_cast<int64_t>(b) * a.q_heads + hq;
+      if (n_chunks == 1) {
+        store_out<QBF>(a.out, bh * kHeadDim + d, lsum > 0.f ? acc / lsum : 0.f);
+      } else {
+        const int64_t ps = bh * a.max_splits + s;
+        a.part_o[ps * kHeadDim + d] = acc;
+        if (d == 0) a.part_ml[ps] = make_float2(M, lsum);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per (request, q head): merge the chunk partials of requests that
+// span more than one chunk (log-sum-exp in the exp2 domain).
+template <bool QBF>
+__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (bh >= static_cast<int64_t>(a.batch) * a.q_heads) return;
+  const int b = static_cast<int>(bh / a.q_heads);
+  const int chunk_tokens = a.chunk_blocks * kBlock;
+  const int L = clamped_len(a, b);
+  const int n = max(1, (L + chunk_tokens - 1) / chunk_tokens);
+  if (n == 1) return;  // written by the decode kernel
+  const float2* ml = a.part_ml + bh * a.max_splits;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + bh * a.max_splits * kHeadDim);
+  for (int s = 0; s < n; ++s) {
+    const float2 v = ml[s];
+    const float e = (v.x == -INFINITY) ? 0.f : exp2f(v.x - M);
+    lsum += e * v.y;
+    const float4 x = po[s * (kHeadDim / 4) + lane];
+    acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const int64_t base = bh * kHeadDim + 4 * lane;
+  store_out<QBF>(a.out, base + 0, acc.x * inv);
+  store_out<QBF>(a.out, base + 1, acc.y * inv);
+  store_out<QBF>(a.out, base + 2, acc.z * inv);
+  store_out<QBF>(a.out, base + 3, acc.w * inv);
+}
+
+template <int KV, bool QBF>
+cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
+  // the request-length scan may need more than the default 48 KB of dynamic
+  // shared memory; allow the largest batch once per device
+  static int opted_in_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (opted_in_device != dev) {
+    e = cudaFuncSetAttribute(decode_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(decode_smem_bytes(kMaxBatch)));
+    if (e != cudaSuccess) return e;
+    opted_in_device = dev;
+  }
+  const size_t smem = decode_smem_bytes(a.batch);
+  decode_kernel<KV, QBF><<<grid, kDecodeThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KV, bool QBF>
+int occupancy_t() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF>, kDecodeThreads,
+                                                    decode_smem_bytes(1024)) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int batch) { return static_cast<size_t>(batch + 1) * sizeof(int32_t); }
+
+cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid,
+                          cudaStream_t s) {
+  const bool qbf = q_dtype == kBF16;
+  switch (kv_dtype) {
+    case kF16:
+      return launch_t<kF16, false>(a, grid, s);
+    case kBF16:
+      return launch_t<kBF16, true>(a, grid, s);
+    case kI8:
+      return qbf ? launch_t<kI8, true>(a, grid, s) : launch_t<kI8, false>(a, grid, s);
+    case kI4:
+      return qbf ? launch_t<kI4, true>(a, grid, s) : launch_t<kI4, false>(a, grid, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_heads;
+  if (rows == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+  if (q_dtype == kBF16)
+    combine_kernel<true><<<grid, 128, 0, s>>>(a);
+  else
+    combine_kernel<false><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+int decode_ctas_per_sm(int kv_dtype, int q_dtype) {
+  const bool qbf = q_dtype == kBF16;
+  switch (kv_dtype) {
+    case kF16: return occupancy_t<kF16, false>();
+    case kBF16: return occupancy_t<kBF16, true>();
+    case kI8: return qbf ? occupancy_t<kI8, true>() : occupancy_t<kI8, false>();
+    case kI4: return qbf ? occupancy_t<kI4, true>() : occupancy_t<kI4, false>();
+    default: return 0;
+  }
+}
+
+}  // namespace kvq

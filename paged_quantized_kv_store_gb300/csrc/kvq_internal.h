@@ -1,0 +1,84 @@
+// Internal interface between the C-ABI layer (kvq_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kBlock = 16;     // tokens per block (LMDeploy article §2.2)
+constexpr int kHeadDim = 128;  // head_dim supported by the kernels
+
+struct StoreArgs {
+  void* k_pool;
+  void* v_pool;
+  void* k_sz;
+  void* v_sz;
+  int64_t num_blocks;
+  int kv_heads;
+  int kv_dtype;
+  int in_dtype;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int32_t* dev_err;
+};
+
+struct TablesArgs {
+  const int32_t* req_to_token;
+  int32_t num_req_slots;
+  int32_t max_context_len;
+  const int32_t* req_pool_indices;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t max_blocks_per_seq;
+  int32_t* block_tables;
+  int32_t* dev_err;
+};
+
+struct DecodeArgs {
+  const uint8_t* k;
+  const uint8_t* v;
+  const uint32_t* k_sz;  // (scale, zero) fp16 pairs
+  const uint32_t* v_sz;
+  int64_t num_blocks;
+  int kv_heads;
+  const void* q;         // [B, Hq, D]
+  void* out;             // [B, Hq, D]
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int batch;
+  int q_heads;
+  int group;             // q_heads / kv_heads
+  int head_groups;       // ceil(group / 8)
+  int chunk_blocks;      // blocks per work item
+  int max_splits;        // chunks of the longest allowed request
+  int len_cap;           // lengths are clamped to this (tokens)
+  float sm_scale_log2;   // sm_scale * log2(e): scores live in the exp2 domain
+  float* part_o;         // [B, Hq, max_splits, D]   (max_splits > 1)
+  float2* part_ml;       // [B, Hq, max_splits]      (running max, sum)
+  int32_t* dev_err;
+};
+
+cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
+// kv_dtype / q_dtype select the template instance
+cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
+                          cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s);
+
+// CTAs of the decode kernel resident per SM (occupancy), per dtype pair
+int decode_ctas_per_sm(int kv_dtype, int q_dtype);
+// Bytes of dynamic shared memory the decode kernel needs for a batch
+size_t decode_smem_bytes(int batch);
+
+constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared memory
+constexpr int kMaxChunkBlocks = 1024;  // blocks per work item
+constexpr int kDecodeThreads = 128;
+
+}  // namespace kvq

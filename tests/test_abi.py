@@ -1,0 +1,136 @@
+"""The C ABI library: it loads, exports what kvq.h declares, validates on the host.
+
+No compute call is made here (these tests run without a GPU): only argument
+checks that return before any launch, and the host-only launch planner.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_quantized_kv_store_gb300 as kvq
+from paged_quantized_kv_store_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kvq.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[a-z_][\w ]*?\**\s*\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(kvq.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = os.popen(f"nm -D --defined-only {_build.LIB_PATH}").read()
+    for n in names:
+        assert re.search(rf"\bT {n}$", out, flags=re.M), n
+
+
+def test_version_and_status_strings(lib):
+    assert kvq.kvq_version() >= 100
+    for s in range(6):
+        assert kvq.kvq_status_string(s)
+
+
+def _pool(**kw):
+    d = dict(k=16, v=32, k_sz=48, v_sz=64, num_blocks=4, block_size=16, kv_heads=2,
+             head_dim=128, kv_dtype=kvq.KVQ_INT8)
+    d.update(kw)
+    return kvq._Pool(d["k"], d["v"], d["k_sz"], d["v_sz"], d["num_blocks"], d["block_size"],
+                     d["kv_heads"], d["head_dim"], d["kv_dtype"])
+
+
+def test_store_validation(lib):
+    f = lib.kv_store_quant
+    ok_ptr = 256
+    assert f(None, ok_ptr, ok_ptr, 0, ok_ptr, 1, None, None) == 1
+    assert f(ctypes.byref(_pool(head_dim=64)), ok_ptr, ok_ptr, 0, ok_ptr, 1, None, None) == 2
+    assert f(ctypes.byref(_pool(block_size=32)), ok_ptr, ok_ptr, 0, ok_ptr, 1, None, None) == 2
+    assert f(ctypes.byref(_pool(k_sz=None)), ok_ptr, ok_ptr, 0, ok_ptr, 1, None, None) == 1
+    assert f(ctypes.byref(_pool(k=17)), ok_ptr, ok_ptr, 0, ok_ptr, 1, None, None) == 1  # misaligned
+    assert f(ctypes.byref(_pool()), ok_ptr, ok_ptr, 4, ok_ptr, 1, None, None) == 2  # int4 input
+    assert f(ctypes.byref(_pool(kv_dtype=kvq.KVQ_F16)), ok_ptr, ok_ptr, kvq.KVQ_BF16, ok_ptr, 1,
+             None, None) == 2  # copy pools need matching dtypes
+    assert f(ctypes.byref(_pool()), None, ok_ptr, 0, ok_ptr, 1, None, None) == 1
+    assert f(ctypes.byref(_pool()), ok_ptr, ok_ptr, 0, ok_ptr, -1, None, None) == 1
+    assert f(ctypes.byref(_pool()), None, None, 0, None, 0, None, None) == 0  # nothing to do
+
+
+def test_decode_validation(lib):
+    f = lib.paged_decode_attn
+    p = 256
+    args = dict(q=p, q_dtype=0, out=p, bt=p, mb=4, sl=p, batch=2, hq=4, msl=64, scale=0.1,
+                splits=0, ws=None, wsb=0, err=None, s=None)
+
+    def call(pool, **kw):
+        a = dict(args)
+        a.update(kw)
+        return f(ctypes.byref(pool) if pool is not None else None, a["q"], a["q_dtype"],
+                 a["out"], a["bt"], a["mb"], a["sl"], a["batch"], a["hq"], a["msl"],
+                 a["scale"], a["splits"], a["ws"], a["wsb"], a["err"], a["s"])
+
+    assert call(None) == 1
+    assert call(_pool(), q_dtype=4) == 2
+    assert call(_pool(kv_dtype=kvq.KVQ_BF16), q_dtype=0) == 2
+    assert call(_pool(), hq=3) == 1          # q heads not a multiple of kv heads
+    assert call(_pool(), mb=0) == 1
+    assert call(_pool(), scale=float("nan")) == 1
+    assert call(_pool(head_dim=256)) == 2
+
+
+def test_tables_validation(lib):
+    f = lib.kvq_block_tables_from_req_to_token
+    assert f(256, 4, 64, 256, 256, -1, 4, 256, None, None) == 1
+    assert f(256, 4, 64, 256, 256, 2, 0, 256, None, None) == 1
+    assert f(None, 4, 64, 256, 256, 2, 4, 256, None, None) == 1
+    assert f(None, 4, 64, None, None, 0, 4, None, None, None) == 0
+
+
+def test_planner(lib):
+    plan = kvq.paged_decode_attn_plan
+    # one work item per request when they are few and long enough to split
+    p = plan(128, 32, 32, 4096, num_sms=152)
+    assert p["chunk_blocks"] * p["max_splits"] >= 256
+    assert 16 <= p["chunk_blocks"] <= 32
+    assert p["grid_ctas"] == 152 * 4
+    assert p["workspace_bytes"] >= 128 * 32 * p["max_splits"] * 130 * 4
+    # short contexts: a single chunk and no workspace
+    p = plan(4, 16, 8, 100, num_sms=152)
+    assert p["max_splits"] == 1 and p["workspace_bytes"] == 0
+    # explicit split counts
+    for s in (1, 2, 3, 7):
+        p = plan(6, 16, 8, 4000, num_splits=s, num_sms=152)
+        nblk = (4000 + 15) // 16
+        assert p["max_splits"] == -(-nblk // p["chunk_blocks"])
+        assert p["max_splits"] <= s
+    # head groups of 8
+    assert plan(2, 64, 2, 64, num_sms=10)["head_groups"] == 4
+    with pytest.raises(kvq.KvqError):
+        plan(2, 6, 4, 64, num_sms=10)
+    with pytest.raises(kvq.KvqError):
+        plan(2, 8, 4, 64, num_sms=10, head_dim=64)
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The product package neither imports nor links the oracle or the generator."""
+    pkg = os.path.join(ROOT, "paged_quantized_kv_store_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                for banned in ("import oracle", "from oracle", "kvq_oracle", "synthetic",
+                               "kvqgen"):
+                    assert banned not in text, (fn, banned)
