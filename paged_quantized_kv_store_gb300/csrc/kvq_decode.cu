@@ -23,11 +23,16 @@
 //                K = 128 dims in 8 steps.
 //   O^T += V^T P'^T with M = 16 dims (8 steps over 128), N = 8 heads,
 //                K = 16 tokens.
-//   For INT8/INT4 pools the codes c go into the tensor cores exactly (as fp16
-//   or bf16 integers) and the per-token scale S and zero Z are applied
-//   outside: q.k = S (q.c) + Z sum(q); sum_t p_t v_t = sum_t (p_t S_t) c_t +
-//   sum_t p_t Z_t. The score fragment is transposed in registers
-//   (movmatrix) to become the B operand of the second product.
+//   For INT8/INT4 pools the codes go into the tensor cores exactly, centred
+//   on mid = 128 or 8 (as fp16 or bf16 integers), and the per-token scale S
+//   and zero Z are applied outside: with Z' = Z + mid S,
+//     q.k = S (q.(c - mid)) + Z' sum(q)
+//     sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t Z'_t.
+//   Centring keeps the two terms from cancelling, so the 16-bit rounding of
+//   p_t S_t stays small next to the result. The P.V product is fp16 for
+//   quantized pools whatever Q's type (P' <= S fits fp16). The score
+//   fragment is transposed in registers (movmatrix) to become the B operand
+//   of the second product.
 //   Each lane's K and V loads are 8-32 contiguous bytes of a token row;
 //   the dims are assigned to mma k-columns so that the loads stay contiguous
 //   (the dot product does not depend on the order of the dims, and Q is
@@ -157,8 +162,9 @@ __device__ __forceinline__ void k_operand(const Frag<KV>& f, int kk, uint32_t (&
 }
 
 // A operand of O^T += V^T P'^T for dim step i: rows = dims (16g + 2i,
-// 16g + 2i + 1), k-columns = tokens (2t, 2t+1, 2t+8, 2t+9).
-template <int KV, bool QBF>
+// 16g + 2i + 1), k-columns = tokens (2t, 2t+1, 2t+8, 2t+9). The product runs
+// in bf16 only for bf16 pools; quantized codes always go in as fp16.
+template <int KV>
 __device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a)[4]) {
   if constexpr (KV == kF16 || KV == kBF16) {
     const uint32_t r0 = w4(f.v[0][i >> 2], i & 3), r1 = w4(f.v[1][i >> 2], i & 3);
@@ -171,17 +177,10 @@ __device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a
     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes k, k+1 of two rows, k = 2(i%2)
     const uint32_t x01 = prmt(w4(f.v[0], i >> 1), w4(f.v[1], i >> 1), sel);
     const uint32_t x23 = prmt(w4(f.v[2], i >> 1), w4(f.v[3], i >> 1), sel);
-    if constexpr (QBF) {
-      a[0] = bytes_to_bf16_pair(x01, 0, 1);
-      a[1] = bytes_to_bf16_pair(x01, 2, 3);
-      a[2] = bytes_to_bf16_pair(x23, 0, 1);
-      a[3] = bytes_to_bf16_pair(x23, 2, 3);
-    } else {
-      a[0] = bytes_to_f16_pair(x01, 0x4140u);
-      a[1] = bytes_to_f16_pair(x01, 0x4342u);
-      a[2] = bytes_to_f16_pair(x23, 0x4140u);
-      a[3] = bytes_to_f16_pair(x23, 0x4342u);
-    }
+    a[0] = bytes_to_f16_pair(x01, 0x4140u);
+    a[1] = bytes_to_f16_pair(x01, 0x4342u);
+    a[2] = bytes_to_f16_pair(x23, 0x4140u);
+    a[3] = bytes_to_f16_pair(x23, 0x4342u);
   } else {
     // i = 4 jj + 2 kk + m: bytes (2kk, 2kk+1) of word jj of the two rows,
     // nibbles 2m and 2m+1 of each half
@@ -190,10 +189,10 @@ __device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a
     const uint32_t r0 = jj ? f.v[0].y : f.v[0].x, r1 = jj ? f.v[1].y : f.v[1].x;
     const uint32_t r2 = jj ? f.v[2].y : f.v[2].x, r3 = jj ? f.v[3].y : f.v[3].x;
     const uint32_t x01 = prmt(r0, r1, sel), x23 = prmt(r2, r3, sel);
-    a[0] = nibbles_to_pair<QBF>(x01 >> (8 * m));
-    a[1] = nibbles_to_pair<QBF>(x01 >> (8 * m + 4));
-    a[2] = nibbles_to_pair<QBF>(x23 >> (8 * m));
-    a[3] = nibbles_to_pair<QBF>(x23 >> (8 * m + 4));
+    a[0] = nibbles_to_pair<false>(x01 >> (8 * m));
+    a[1] = nibbles_to_pair<false>(x01 >> (8 * m + 4));
+    a[2] = nibbles_to_pair<false>(x23 >> (8 * m));
+    a[3] = nibbles_to_pair<false>(x23 >> (8 * m + 4));
   }
 }
 
@@ -231,6 +230,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
   extern __shared__ int32_t cum[];  // [batch + 1] exclusive prefix of chunk counts
   __shared__ Smem sm;
   constexpr bool kQuant = KvTraits<KV>::kQuant;
+  constexpr bool kPvBf = KV == kBF16;  // P.V product type: bf16 only for bf16 pools
+  constexpr float kMid = KV == kI8 ? 128.f : 8.f;  // code centre (quantized pools)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -371,8 +372,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
         const int tok0 = j * kBlock + g, tok1 = tok0 + 8;
         float s00, s01, s10, s11;
         if constexpr (kQuant) {
-          const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]);
-          const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]);
+          // q.k = S (q.(c - mid)) + (Z + mid S) sum(q)
+          const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) + kMid * S0;
+          const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) + kMid * S1;
           s00 = (S0 * sc[0] + Z0 * qs0) * a.sm_scale_log2;
           s01 = (S0 * sc[1] + Z0 * qs1) * a.sm_scale_log2;
           s10 = (S1 * sc[2] + Z1 * qs0) * a.sm_scale_log2;
@@ -404,8 +406,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
         l1 = l1 * al1 + (p01 + p11);
         float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
         if constexpr (kQuant) {
-          const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]);
-          const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]);
+          // sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t (Z_t + mid S_t)
+          const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
+          const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
           z0 = z0 * al0 + (p00 * Z0 + p10 * Z1);
           z1 = z1 * al1 + (p01 * Z0 + p11 * Z1);
           q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
@@ -416,15 +419,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
           o[i][1] *= al1; o[i][3] *= al1;
         }
         // P'^T as the B operand: transpose the (token x head) fragments
-        uint32_t bp[2];
-        bp[0] = movmatrix_trans(pack2<QBF>(q00, q01));
-        bp[1] = movmatrix_trans(pack2<QBF>(q10, q11));
+        uint32_t bp[2], bp_lo[2];
+        const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
+        bp[0] = movmatrix_trans(h0);
+        bp[1] = movmatrix_trans(h1);
+        if constexpr (kPvBf) {
+          // bf16 keeps 8 bits of P: add the rounding residual in a second
+          // product so P carries ~16 bits (P = hi + lo)
+          bp_lo[0] = movmatrix_trans(pack2<true>(q00 - lo_to_float<true>(h0),
+                                                 q01 - hi_to_float<true>(h0)));
+          bp_lo[1] = movmatrix_trans(pack2<true>(q10 - lo_to_float<true>(h1),
+                                                 q11 - hi_to_float<true>(h1)));
+        }
         // O^T += V^T P'^T
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t av[4];
-          v_operand<KV, QBF>(cur, i, av);
-          mma16816<QBF>(o[i], av, bp);
+          v_operand<KV>(cur, i, av);
+          mma16816<kPvBf>(o[i], av, bp);
+          if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
         }
       }
       cur = nxt;

@@ -87,28 +87,34 @@ __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Codes enter the tensor cores centred: c - 8 (INT4) or c - 128 (INT8), so
+// that the dequantized value is S (c - mid) + (Z + mid S) and no large terms
+// cancel when the per-token zero is added back outside the product. Every
+// centred code is an exact fp16 / bf16 integer.
+
 // Two 4-bit codes (bits [4s, 4s+4) of each 16-bit half of w) as a pair of
-// exact 16-bit floats. Setting the exponent field over the code gives
-// 1024 + c (fp16, 0x6400) or 128 + c (bf16, 0x4300); one packed subtract
-// removes the offset, exactly.
+// exact 16-bit floats c - 8. Setting the exponent field over the code gives
+// 1024 + c (fp16, 0x6400) or 128 + c (bf16, 0x4300); one packed subtract of
+// 1032 (0x6408) or 136 (0x4308) leaves c - 8, exactly.
 template <bool BF>
 __device__ __forceinline__ uint32_t nibbles_to_pair(uint32_t w_shifted) {
   constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
-  return sub2<BF>(and_or(w_shifted, 0x000F000Fu, kMagic), kMagic);
+  constexpr uint32_t kMagicMid = BF ? 0x43084308u : 0x64086408u;
+  return sub2<BF>(and_or(w_shifted, 0x000F000Fu, kMagic), kMagicMid);
 }
 
 // Two bytes of w (selected by sel, producing [b_lo, 0x64, b_hi, 0x64]) as an
-// exact fp16 pair: 1024 + c, minus 1024.
+// exact fp16 pair c - 128: 1024 + c, minus 1152 (0x6480).
 __device__ __forceinline__ uint32_t bytes_to_f16_pair(uint32_t w, uint32_t sel) {
-  return sub2<false>(prmt(w, 0x64646464u, sel), 0x64006400u);
+  return sub2<false>(prmt(w, 0x64646464u, sel), 0x64806480u);
 }
 
-// Two bytes of w (byte indices i0 low, i1 high) as an exact bf16 pair: bf16
-// has 8 significant bits, so every code 0..255 is exact; the bytes go through
-// fp32 (2^23 + c, minus 2^23) and a paired round-to-nearest conversion.
+// Two bytes of w (byte indices i0 low, i1 high) as an exact bf16 pair c - 128:
+// the bytes go through fp32 (2^23 + c, minus 2^23 + 128) and a paired
+// round-to-nearest conversion, exact since |c - 128| <= 128.
 __device__ __forceinline__ uint32_t bytes_to_bf16_pair(uint32_t w, int i0, int i1) {
-  const float f0 = __uint_as_float(0x4B000000u | ((w >> (8 * i0)) & 0xFFu)) - 8388608.0f;
-  const float f1 = __uint_as_float(0x4B000000u | ((w >> (8 * i1)) & 0xFFu)) - 8388608.0f;
+  const float f0 = __uint_as_float(0x4B000000u | ((w >> (8 * i0)) & 0xFFu)) - 8388736.0f;
+  const float f1 = __uint_as_float(0x4B000000u | ((w >> (8 * i1)) & 0xFFu)) - 8388736.0f;
   __nv_bfloat162 p = __floats2bfloat162_rn(f0, f1);
   return *reinterpret_cast<uint32_t*>(&p);
 }

@@ -162,7 +162,7 @@ def test_uniform_k_gives_mean_of_v(gpu):
     opool = oracle.Pool(wl.num_blocks, 1, D, "int8")
     oracle.kv_store(opool, k, v, "f16", slots)
     rows = opool.v.reshape(-1, 1, D)[slots].astype(np.float64)[:, 0]
-    sz = opool.v_sz[pos // 16, 0, pos % 16]
+    sz = opool.v_sz[slots // 16, 0, slots % 16]
     vhat = rows * oracle.f16_to_f32(sz[:, 0])[:, None] + oracle.f16_to_f32(sz[:, 1])[:, None]
     for h in range(4):
         assert_close(out_to_f64(out)[0, h], vhat.mean(axis=0))
