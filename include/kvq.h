@@ -206,6 +206,39 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              void* stream);
 
 /*
+ * paged_decode_attn_noalloc -- the same computation as paged_decode_attn,
+ * for callers that cannot allocate device memory (an operator inside an
+ * engine that only passes it its tensors, a program that must reserve all
+ * device memory when it loads, a loop where an allocation's latency or
+ * implied synchronization is not acceptable). The pages have no counterpart:
+ * this is a deployment convenience of this library.
+ *
+ * The split-K scratch comes from one array of KVQ_NOALLOC_SCRATCH_BYTES that
+ * the library keeps in device memory (every GPU that loads the library holds
+ * it until the process exits); nothing is allocated by the call. The caller
+ * still passes inputs and outputs, with the meaning and layout of
+ * paged_decode_attn.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Sizes whose paged_decode_attn_workspace_size exceeds
+ *    KVQ_NOALLOC_SCRATCH_BYTES are rejected with KVQ_ERR_WORKSPACE before
+ *    anything is launched.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero (every entry read is first written
+ *    by the same call). Calls whose work overlaps on the GPU (other streams,
+ *    other host threads) race on the array: serialize them.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_t q_dtype,
+                                     void* out, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     int32_t batch, int32_t q_heads, int32_t max_seq_len,
+                                     float sm_scale, int32_t num_splits, int32_t* dev_err,
+                                     void* stream);
+
+/*
  * kvq_check_error -- synchronize `stream`, read the device error word and
  * clear it. Returns KVQ_OK if it was 0, KVQ_ERR_OUT_OF_RANGE otherwise (the
  * bits are stored to *bits_out when bits_out is not NULL), KVQ_ERR_CUDA if the

@@ -60,7 +60,7 @@ class _Plan(ctypes.Structure):
 
 EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decode_attn_plan",
             "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
-            "kvq_status_string", "kvq_version"]
+            "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc"]
 
 
 def load(build_if_missing: bool = False):
@@ -88,6 +88,9 @@ def load(build_if_missing: bool = False):
     lib.paged_decode_attn.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, I32, P, I32, I32, I32,
                                       F, I32, P, SZ, P, P]
     lib.paged_decode_attn.restype = ctypes.c_int
+    lib.paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, I32, P, I32,
+                                              I32, I32, F, I32, P, P]
+    lib.paged_decode_attn_noalloc.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.kvq_check_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -223,6 +226,21 @@ def paged_decode_attn(pool: KVPool, q, out, block_tables, seq_lens, max_seq_len,
                                float(sm_scale), int(num_splits), _ptr(workspace), ws_bytes,
                                _ptr(dev_err), _stream(stream))
     _check(st, "paged_decode_attn")
+
+
+def paged_decode_attn_noalloc(pool: KVPool, q, out, block_tables, seq_lens, max_seq_len,
+                              sm_scale, num_splits=0, dev_err=None, stream=None):
+    """paged_decode_attn without a caller workspace, for callers that cannot
+    allocate device memory: the scratch is a fixed array inside libkvq
+    (shared by all calls; overlapping calls race). See kvq.h."""
+    lib = load()
+    ps = pool.c_struct()
+    st = lib.paged_decode_attn_noalloc(ctypes.byref(ps), _ptr(q), _dtype_code(q), _ptr(out),
+                                       _ptr(block_tables), int(block_tables.shape[1]),
+                                       _ptr(seq_lens), int(q.shape[0]), int(q.shape[1]),
+                                       int(max_seq_len), float(sm_scale), int(num_splits),
+                                       _ptr(dev_err), _stream(stream))
+    _check(st, "paged_decode_attn_noalloc")
 
 
 def kvq_check_error(dev_err, stream=None) -> int:

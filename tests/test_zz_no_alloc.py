@@ -1,0 +1,68 @@
+"""paged_decode_attn_noalloc: decode attention without a caller workspace.
+
+Some callers cannot allocate device memory (an operator inside an engine that
+only receives its tensors, a program that reserves all device memory at load
+time, a loop where an allocation is not acceptable). For them libkvq keeps the
+split-K scratch in a fixed array of its own. These tests call that entry point
+through the C ABI and check that two calls in a row, with different sizes,
+give the same outputs as paged_decode_attn with a caller-allocated workspace,
+within the tolerance of the other parity tests. This file sorts last so that
+a run stopping at its first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+from gpu_harness import assert_close, decode, fill_pool, i32, out_to_f64, run_step, to_dev  # noqa: E402
+
+SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def _noalloc(kvq, wl, pool, bt, num_splits=0):
+    q = to_dev(wl.q(), wl.q_dtype)
+    out = torch.full_like(q, float("nan"))
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.paged_decode_attn_noalloc(pool, q, out, bt, i32(wl.seq_lens), wl.max_seq_len,
+                                  wl.sm_scale, num_splits, dev_err)
+    assert kvq.kvq_check_error(dev_err) == 0
+    return out
+
+
+def test_two_calls_match_the_workspace_entry_point(gpu):
+    # two different shapes back to back: the second call sees the first
+    # call's leftovers in the shared scratch
+    cases = [
+        (synthetic.cfg4(batch=12), 0),
+        (synthetic.custom("noalloc_int8", "int8", [700, 33, 1500, 5, 260], 16, 4, seed=90), 5),
+    ]
+    for wl, splits in cases:
+        pool = fill_pool(wl)
+        ref, bt, dev_err = run_step(wl, pool, num_splits=splits)
+        assert gpu.kvq_check_error(dev_err) == 0
+        assert gpu.paged_decode_attn_workspace_size(
+            wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, splits) > 0  # scratch is used
+        got = _noalloc(gpu, wl, pool, bt, splits)
+        assert_close(out_to_f64(got), out_to_f64(ref))
+        # a repeated call gives the same bits
+        again = _noalloc(gpu, wl, pool, bt, splits)
+        assert torch.equal(got.view(torch.int16), again.view(torch.int16))
+
+
+def test_sizes_beyond_the_scratch_are_rejected(gpu):
+    wl = synthetic.custom("noalloc_big", "int8", [16], 64, 64, seed=91)
+    pool = gpu.KVPool.allocate(wl.num_blocks, wl.kv_heads, "int8")
+    batch, q_heads, max_len = 4096, 64, 8192
+    need = gpu.paged_decode_attn_workspace_size(batch, q_heads, 64, max_len, 0)
+    assert need > SCRATCH_BYTES
+    q = torch.zeros((batch, q_heads, 128), dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    bt = torch.zeros((batch, max_len // 16), dtype=torch.int32, device="cuda")
+    sl = torch.ones(batch, dtype=torch.int32, device="cuda")
+    with pytest.raises(gpu.KvqError) as e:
+        gpu.paged_decode_attn_noalloc(pool, q, out, bt, sl, max_len, 0.1)
+    assert e.value.status == 5
+    assert torch.count_nonzero(out) == 0  # nothing was launched
