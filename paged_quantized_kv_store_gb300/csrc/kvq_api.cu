@@ -21,7 +21,6 @@ constexpr int kAutoMinChunk = 16;     // blocks (256 tokens)
 constexpr int kAutoMaxChunk = 32;     // blocks (512 tokens)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool is_quant(int dt) { return dt == KVQ_INT8 || dt == KVQ_INT4; }
 bool is_float16(int dt) { return dt == KVQ_F16 || dt == KVQ_BF16; }
@@ -34,7 +33,7 @@ kvq_status check_pool(const kvq_pool* p) {
   if (!aligned16(p->k) || !aligned16(p->v)) return KVQ_ERR_INVALID_ARG;
   if (is_quant(p->kv_dtype)) {
     if (p->k_sz == nullptr || p->v_sz == nullptr) return KVQ_ERR_INVALID_ARG;
-    if (!aligned4(p->k_sz) || !aligned4(p->v_sz)) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(p->k_sz) || !aligned16(p->v_sz)) return KVQ_ERR_INVALID_ARG;
   }
   return KVQ_OK;
 }
@@ -227,7 +226,11 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   }
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, plan.grid_ctas, s) != cudaSuccess)
+  // persistent grid: as many CTAs as fit on the device at once
+  const int per_sm = kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
+  if (per_sm <= 0) return KVQ_ERR_CUDA;
+  const int grid = plan.num_sms * per_sm;
+  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   if (plan.max_splits > 1 && kvq::launch_combine(a, q_dtype, s) != cudaSuccess)
     return KVQ_ERR_CUDA;

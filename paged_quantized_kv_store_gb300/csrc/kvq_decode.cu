@@ -76,50 +76,121 @@ struct Frag<kI4> {
   uint32_t ksz[2], vsz[2];
 };
 
+// ---- shared-memory staging -------------------------------------------------------
+
+// One pipeline stage holds one 16-token block of one kv head: the K tile and
+// the V tile (16 rows of kRow bytes each; the 16-byte chunks of row r are
+// XOR-swizzled with r so that the fragment reads below fall on distinct
+// banks) and, for quantized pools, the 16 (scale, zero) pairs of K and of V.
 template <int KV>
-__device__ __forceinline__ void load_frag(Frag<KV>& f, const DecodeArgs& a, int64_t phys, int h,
-                                          int g, int t) {
-  constexpr int R = KvTraits<KV>::kRowBytes;
-  const int64_t row0 = phys * kBlock;  // first slot of the block
-  const int Hkv = a.kv_heads;
-  const uint8_t* kb = a.k + ((row0 * Hkv + h) * R);
-  const uint8_t* vb = a.v + ((row0 * Hkv + h) * R);
-  const int64_t tok_stride = static_cast<int64_t>(Hkv) * R;
-  const uint8_t* k0 = kb + g * tok_stride + t * (R / 4);
-  const uint8_t* k1 = kb + (g + 8) * tok_stride + t * (R / 4);
+struct Stage {
+  static constexpr int kRow = KvTraits<KV>::kRowBytes;
+  static constexpr int kChunks = kRow / 16;                // 16-byte chunks per row
+  static constexpr int kSwz = (kChunks < 8 ? kChunks : 8) - 1;
+  static constexpr int kTile = kBlock * kRow;
+  static constexpr int kBytes = 2 * kTile + (KvTraits<KV>::kQuant ? 128 : 0);
+  // blocks in flight per warp: about 16 KB of KV per warp
+  static constexpr int kDepth = KV == kI4 ? 6 : (KV == kI8 ? 4 : 2);
+};
+
+__device__ __forceinline__ int swz(int r, int c, int mask) { return c ^ (r & mask); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+
+// The warp copies block `phys` of kv head h into the stage at shared address
+// st: every lane moves 16-byte chunks of both tiles, lanes 0-7 the scale/zero
+// pairs. Asynchronous (cp.async); the caller commits the group.
+template <int KV>
+__device__ __forceinline__ void issue_block(uint32_t st, const DecodeArgs& a, int64_t phys,
+                                            int h, int lane) {
+  using S = Stage<KV>;
+  const int64_t tok_stride = static_cast<int64_t>(a.kv_heads) * S::kRow;
+  const int64_t base = (phys * kBlock * a.kv_heads + h) * S::kRow;
+  const uint8_t* kb = a.k + base;
+  const uint8_t* vb = a.v + base;
+#pragma unroll
+  for (int i = 0; i < kBlock * S::kChunks / 32; ++i) {
+    const int n = lane + 32 * i;
+    const int r = n / S::kChunks, c = n % S::kChunks;
+    const uint32_t off = r * S::kRow + swz(r, c, S::kSwz) * 16;
+    cp_async16(st + off, kb + r * tok_stride + c * 16);
+    cp_async16(st + S::kTile + off, vb + r * tok_stride + c * 16);
+  }
+  if constexpr (KvTraits<KV>::kQuant) {
+    if (lane < 8) {
+      const uint32_t* src =
+          (lane < 4 ? a.k_sz : a.v_sz) + (phys * a.kv_heads + h) * kBlock + 4 * (lane & 3);
+      cp_async16(st + 2 * S::kTile + 16 * lane, src);
+    }
+  }
+}
+
+// This lane's fragment bytes of the staged block: K rows g, g+8 and V rows
+// 2t, 2t+1, 2t+8, 2t+9 (see the operand builders below), and the scale/zero
+// words of tokens g and g+8.
+template <int KV>
+__device__ __forceinline__ void read_frag(Frag<KV>& f, uint32_t st, int g, int t) {
+  using S = Stage<KV>;
   const int vr[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  auto ka = [&](int r, int c) { return st + r * S::kRow + swz(r, c, S::kSwz) * 16; };
+  auto va = [&](int r, int c) { return st + S::kTile + r * S::kRow + swz(r, c, S::kSwz) * 16; };
   if constexpr (KV == kF16 || KV == kBF16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      f.k[0][i] = ldg_stream16(k0 + 16 * i);
-      f.k[1][i] = ldg_stream16(k1 + 16 * i);
+      f.k[0][i] = lds128(ka(g, 4 * t + i));
+      f.k[1][i] = lds128(ka(g + 8, 4 * t + i));
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const uint8_t* p = vb + vr[r] * tok_stride + g * (R / 8);
-      f.v[r][0] = ldg_stream16(p);
-      f.v[r][1] = ldg_stream16(p + 16);
+      f.v[r][0] = lds128(va(vr[r], 2 * g));
+      f.v[r][1] = lds128(va(vr[r], 2 * g + 1));
     }
   } else if constexpr (KV == kI8) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      f.k[0][i] = ldg_stream16(k0 + 16 * i);
-      f.k[1][i] = ldg_stream16(k1 + 16 * i);
+      f.k[0][i] = lds128(ka(g, 2 * t + i));
+      f.k[1][i] = lds128(ka(g + 8, 2 * t + i));
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = ldg_stream16(vb + vr[r] * tok_stride + g * (R / 8));
+    for (int r = 0; r < 4; ++r) f.v[r] = lds128(va(vr[r], g));
   } else {
-    f.k[0] = ldg_stream16(k0);
-    f.k[1] = ldg_stream16(k1);
+    f.k[0] = lds128(ka(g, t));
+    f.k[1] = lds128(ka(g + 8, t));
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = ldg_stream8(vb + vr[r] * tok_stride + g * (R / 8));
+    for (int r = 0; r < 4; ++r) f.v[r] = lds64(va(vr[r], g >> 1) + 8 * (g & 1));
   }
   if constexpr (KvTraits<KV>::kQuant) {
-    const int64_t szb = (phys * Hkv + h) * kBlock;
-    f.ksz[0] = ldg_nc32(a.k_sz + szb + g);
-    f.ksz[1] = ldg_nc32(a.k_sz + szb + g + 8);
-    f.vsz[0] = ldg_nc32(a.v_sz + szb + g);
-    f.vsz[1] = ldg_nc32(a.v_sz + szb + g + 8);
+    const uint32_t sz = st + 2 * S::kTile;
+    f.ksz[0] = lds32(sz + 4 * g);
+    f.ksz[1] = lds32(sz + 4 * (g + 8));
+    f.vsz[0] = lds32(sz + 64 + 4 * g);
+    f.vsz[1] = lds32(sz + 64 + 4 * (g + 8));
   }
 }
 
@@ -212,14 +283,31 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
   }
 }
 
-struct Smem {
+// Merge area of the CTA (aliased onto the pipeline stages once they drain).
+struct Merge {
   float m[kWarps][kHeadsPerGroup];
   float l[kWarps][kHeadsPerGroup];
   float2 o[kWarps][kHeadsPerGroup][kHeadDim / 2];
-  int32_t warp_sum[kWarps];
 };
 
-// Clamped length of request b and its number of chunks (>= 1).
+constexpr int kBtCacheBytes = kMaxChunkBlocks * 4;
+
+__host__ __device__ constexpr size_t align128(size_t x) { return (x + 127) / 128 * 128; }
+
+// Dynamic shared memory: [request chunk prefix sums][block ids of the item]
+// [pipeline stages of every warp, the merge area aliased at their start].
+template <int KV>
+__host__ __device__ constexpr size_t stage_region_bytes() {
+  return static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes > sizeof(Merge)
+             ? static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes
+             : sizeof(Merge);
+}
+template <int KV>
+__host__ __device__ constexpr size_t smem_bytes_for(int batch) {
+  return align128((batch + 1) * sizeof(int32_t)) + kBtCacheBytes + stage_region_bytes<KV>();
+}
+
+// Clamped length of request b.
 __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
   return min(max(a.seq_lens[b], 0), a.len_cap);
 }
@@ -227,15 +315,24 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
 template <int KV, bool QBF>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(DecodeArgs a) {
-  extern __shared__ int32_t cum[];  // [batch + 1] exclusive prefix of chunk counts
-  __shared__ Smem sm;
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ int32_t warp_sum[kWarps];
+  using S = Stage<KV>;
   constexpr bool kQuant = KvTraits<KV>::kQuant;
   constexpr bool kPvBf = KV == kBF16;  // P.V product type: bf16 only for bf16 pools
   constexpr float kMid = KV == kI8 ? 128.f : 8.f;  // code centre (quantized pools)
+  constexpr int D = S::kDepth;
+
+  int32_t* cum = reinterpret_cast<int32_t*>(dsmem);  // [batch + 1] prefix of chunk counts
+  int32_t* s_bt = reinterpret_cast<int32_t*>(dsmem + align128((a.batch + 1) * sizeof(int32_t)));
+  unsigned char* stages = dsmem + align128((a.batch + 1) * sizeof(int32_t)) + kBtCacheBytes;
+  Merge& mg = *reinterpret_cast<Merge*>(stages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int chunk_tokens = a.chunk_blocks * kBlock;
+  const uint32_t my_stages = static_cast<uint32_t>(__cvta_generic_to_shared(stages)) +
+                             static_cast<uint32_t>(warp * D * S::kBytes);
 
   // ---- chunk counts of every request, prefix-summed --------------------------
   {
@@ -253,10 +350,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
       const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
       if (lane >= off) incl += y;
     }
-    if (lane == 31) sm.warp_sum[warp] = incl;
+    if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
     int base = 0;
-    for (int w = 0; w < warp; ++w) base += sm.warp_sum[w];
+    for (int w = 0; w < warp; ++w) base += warp_sum[w];
     int run = base + incl - sum;
     for (int b = b0; b < b1; ++b) {
       cum[b] = run;
@@ -289,6 +386,27 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int blk_end = min(blk_begin + a.chunk_blocks, nblk);
     const int hq0 = h * a.group + hg * kHeadsPerGroup;
     const int nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
+
+    // block ids of this item, once for the CTA
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks;
+    for (int i = tid; i < blk_end - blk_begin; i += kDecodeThreads) s_bt[i] = bt[blk_begin + i];
+    __syncthreads();
+
+    // this warp's blocks: blk_begin + warp + kWarps * k, k < n_w
+    const int n_w = blk_end - blk_begin > warp ? (blk_end - blk_begin - warp + kWarps - 1) / kWarps
+                                               : 0;
+    auto issue = [&](int k) {
+      if (k < n_w) {
+        const int32_t phys = s_bt[warp + kWarps * k];
+        if (phys >= 0 && phys < a.num_blocks)
+          issue_block<KV>(my_stages + (k % D) * S::kBytes, a, phys, h, lane);
+        else if (lane == 0)
+          report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue(k);
 
     // ---- Q fragments (B operand of S^T = K Q^T), permuted like the K dims --
     uint32_t qb[8][2];
@@ -335,31 +453,20 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     const bool hv0 = 2 * t < nh, hv1 = 2 * t + 1 < nh;
 
-    // ---- this warp's blocks -------------------------------------------------
     float o[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
 
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks;
-    int j = blk_begin + warp;
-    int64_t phys = j < blk_end ? bt[j] : -1;
-    int64_t phys_next = j + kWarps < blk_end ? bt[j + kWarps] : -1;
-    Frag<KV> cur;
-    bool cur_ok = j < blk_end && phys >= 0 && phys < a.num_blocks;
-    if (j < blk_end && !cur_ok && lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
-    if (cur_ok) load_frag<KV>(cur, a, phys, h, g, t);
-
-    for (; j < blk_end; j += kWarps) {
-      // prefetch block j + kWarps while block j is computed
-      const int jn = j + kWarps;
-      Frag<KV> nxt;
-      const bool nxt_ok = jn < blk_end && phys_next >= 0 && phys_next < a.num_blocks;
-      if (jn < blk_end && !nxt_ok && lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
-      if (nxt_ok) load_frag<KV>(nxt, a, phys_next, h, g, t);
-      const int64_t phys_after = jn + kWarps < blk_end ? bt[jn + kWarps] : -1;
-
-      if (cur_ok) {
+    for (int k = 0; k < n_w; ++k) {
+      issue(k + D - 1);      // refills the stage block k - 1 used
+      cp_async_wait<D - 1>();  // this lane's copies of block k have landed
+      __syncwarp();            // ... and every other lane's
+      const int j = blk_begin + warp + kWarps * k;
+      const int32_t phys = s_bt[warp + kWarps * k];
+      if (phys >= 0 && phys < a.num_blocks) {
+        Frag<KV> cur;
+        read_frag<KV>(cur, my_stages + (k % D) * S::kBytes, g, t);
         // S^T = K Q^T
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -440,10 +547,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
           if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
         }
       }
-      cur = nxt;
-      cur_ok = nxt_ok;
-      phys_next = phys_after;
+      __syncwarp();  // all lanes are done with this stage before it is refilled
     }
+    cp_async_wait<0>();
 
     // ---- finish this warp: sums over the 8 token lanes -----------------------
 #pragma unroll
@@ -455,16 +561,17 @@ __global__ void __launch_bounds__(kDecodeThreads)
         z1 += __shfl_xor_sync(0xFFFFFFFFu, z1, off);
       }
     }
+    __syncthreads();  // every warp's stages are drained: the merge area may overwrite them
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      sm.o[warp][2 * t][8 * g + i] = make_float2(o[i][0] + z0, o[i][2] + z0);
-      sm.o[warp][2 * t + 1][8 * g + i] = make_float2(o[i][1] + z1, o[i][3] + z1);
+      mg.o[warp][2 * t][8 * g + i] = make_float2(o[i][0] + z0, o[i][2] + z0);
+      mg.o[warp][2 * t + 1][8 * g + i] = make_float2(o[i][1] + z1, o[i][3] + z1);
     }
     if (g == 0) {
-      sm.m[warp][2 * t] = m0;
-      sm.m[warp][2 * t + 1] = m1;
-      sm.l[warp][2 * t] = l0;
-      sm.l[warp][2 * t + 1] = l1;
+      mg.m[warp][2 * t] = m0;
+      mg.m[warp][2 * t + 1] = m1;
+      mg.l[warp][2 * t] = l0;
+      mg.l[warp][2 * t + 1] = l1;
     }
     __syncthreads();
 
@@ -473,15 +580,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
       const int hh = idx / kHeadDim, d = idx % kHeadDim;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][hh]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mg.m[w][hh]);
       float acc = 0.f, lsum = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const float e = exp2f(sm.m[w][hh] - M);
-          const float2 ov = sm.o[w][hh][d >> 1];
+          const float e = exp2f(mg.m[w][hh] - M);
+          const float2 ov = mg.o[w][hh][d >> 1];
           acc += e * ((d & 1) ? ov.y : ov.x);
-          lsum += e * sm.l[w][hh];
+          lsum += e * mg.l[w][hh];
         }
       }
       const int hq = hq0 + hh;
@@ -494,7 +601,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         if (d == 0) a.part_ml[ps] = make_float2(M, lsum);
       }
     }
-    __syncthreads();
+    __syncthreads();  // the merge area and s_bt are reused by the next item
   }
 }
 
@@ -535,35 +642,43 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 
 template <int KV, bool QBF>
 cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
-  // the request-length scan may need more than the default 48 KB of dynamic
-  // shared memory; allow the largest batch once per device
+  // allow the largest dynamic shared memory the kernel can ask for, once
+  // per device
   static int opted_in_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (opted_in_device != dev) {
     e = cudaFuncSetAttribute(decode_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes(kMaxBatch)));
+                             static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
   }
-  const size_t smem = decode_smem_bytes(a.batch);
-  decode_kernel<KV, QBF><<<grid, kDecodeThreads, smem, s>>>(a);
+  decode_kernel<KV, QBF><<<grid, kDecodeThreads, smem_bytes_for<KV>(a.batch), s>>>(a);
   return cudaGetLastError();
 }
 
 template <int KV, bool QBF>
-int occupancy_t() {
+int occupancy_t(int batch) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  if (dev == cached_dev && batch == cached_batch) return cached_n;
+  if (cudaFuncSetAttribute(decode_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
+    return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF>, kDecodeThreads,
-                                                    decode_smem_bytes(1024)) != cudaSuccess)
+                                                    smem_bytes_for<KV>(batch)) != cudaSuccess)
     return 0;
+  cached_dev = dev;
+  cached_batch = batch;
+  cached_n = n;
   return n;
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int batch) { return static_cast<size_t>(batch + 1) * sizeof(int32_t); }
 
 cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid,
                           cudaStream_t s) {
@@ -593,13 +708,13 @@ cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int decode_ctas_per_sm(int kv_dtype, int q_dtype) {
+int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch) {
   const bool qbf = q_dtype == kBF16;
   switch (kv_dtype) {
-    case kF16: return occupancy_t<kF16, false>();
-    case kBF16: return occupancy_t<kBF16, true>();
-    case kI8: return qbf ? occupancy_t<kI8, true>() : occupancy_t<kI8, false>();
-    case kI4: return qbf ? occupancy_t<kI4, true>() : occupancy_t<kI4, false>();
+    case kF16: return occupancy_t<kF16, false>(batch);
+    case kBF16: return occupancy_t<kBF16, true>(batch);
+    case kI8: return qbf ? occupancy_t<kI8, true>(batch) : occupancy_t<kI8, false>(batch);
+    case kI4: return qbf ? occupancy_t<kI4, true>(batch) : occupancy_t<kI4, false>(batch);
     default: return 0;
   }
 }

@@ -72,10 +72,8 @@ cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int gr
                           cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s);
 
-// CTAs of the decode kernel resident per SM (occupancy), per dtype pair
-int decode_ctas_per_sm(int kv_dtype, int q_dtype);
-// Bytes of dynamic shared memory the decode kernel needs for a batch
-size_t decode_smem_bytes(int batch);
+// CTAs of the decode kernel resident per SM (occupancy) for a dtype pair and batch
+int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
 
 constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared memory
 constexpr int kMaxChunkBlocks = 1024;  // blocks per work item
