@@ -144,23 +144,25 @@ kvq_status kvq_block_tables_from_req_to_token(const int32_t* req_to_token,
 
 /*
  * Launch plan of paged_decode_attn (host-only arithmetic; no device access
- * when num_sms > 0). The context of each request is cut into chunks of
- * chunk_blocks blocks; each (request, kv head, chunk) is one work item of a
- * persistent grid of grid_ctas CTAs. Requests longer than one chunk write
- * partial results (running max, sum, unnormalised output) to the workspace
- * and a combine kernel merges them (log-sum-exp).
- *  num_splits      : 0 = choose automatically; else the wanted number of
- *                    chunks for the longest request (clamped to [1, blocks]).
- *  num_sms         : SMs to plan for; 0 = ask the current device.
+ * when num_sms > 0). The decode work is one stream of (kv head, q-head group,
+ * request, block) items; a persistent grid of warps cuts it into equal
+ * contiguous ranges, at least min_blocks_per_warp blocks each. A warp writes
+ * the output of every request it covers completely and, for the first and
+ * last request of its range, a partial result (running max, sum,
+ * unnormalised output) that a combine kernel merges with a log-sum-exp.
+ *  num_splits : 0 = automatic; else requests are cut into at most
+ *               num_splits + 1 pieces (min_blocks_per_warp =
+ *               ceil(max blocks / num_splits)).
+ *  num_sms    : SMs to plan for; 0 = ask the current device.
  */
 typedef struct kvq_decode_plan {
-  int32_t chunk_blocks;     /* blocks (of 16 tokens) per work item */
-  int32_t max_splits;       /* chunks of the longest request */
-  int32_t head_groups;      /* q heads of one kv head are taken 8 at a time */
-  int32_t grid_ctas;        /* persistent CTAs launched */
+  int32_t min_blocks_per_warp; /* lower bound of each warp's share, in blocks */
+  int32_t warps;               /* warps the workspace has partial slots for */
+  int32_t head_groups;         /* ceil((q_heads / kv_heads) / 8) */
+  int32_t heads_per_group;     /* min(q_heads / kv_heads, 8) */
   int32_t num_sms;
-  int32_t reserved;
-  size_t workspace_bytes;   /* 0 when max_splits == 1 */
+  int32_t max_ctas_per_sm;     /* persistent CTAs per SM the workspace allows */
+  size_t workspace_bytes;      /* header (lengths prefix) + 2 partial slots per warp */
 } kvq_decode_plan;
 
 kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_heads,
@@ -229,7 +231,7 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
  *    by the same call). Calls whose work overlaps on the GPU (other streams,
  *    other host threads) race on the array: serialize them.
  */
-#define KVQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_t q_dtype,
                                      void* out, const int32_t* block_tables,

@@ -52,9 +52,9 @@ class _Pool(ctypes.Structure):
 
 
 class _Plan(ctypes.Structure):
-    _fields_ = [("chunk_blocks", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("head_groups", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    _fields_ = [("min_blocks_per_warp", ctypes.c_int32), ("warps", ctypes.c_int32),
+                ("head_groups", ctypes.c_int32), ("heads_per_group", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("max_ctas_per_sm", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t)]
 
 

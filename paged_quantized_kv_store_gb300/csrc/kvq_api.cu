@@ -15,10 +15,7 @@ using kvq::kHeadDim;
 
 namespace {
 
-constexpr int kPlanCtasPerSm = 4;     // persistent decode CTAs per SM
-constexpr int kItemsPerCta = 8;       // work items the planner aims for per CTA
-constexpr int kAutoMinChunk = 16;     // blocks (256 tokens)
-constexpr int kAutoMaxChunk = 32;     // blocks (512 tokens)
+constexpr int kAutoMinBlocksPerWarp = 4;  // a warp's range is never shorter than this
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -124,38 +121,18 @@ kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_hea
   if (num_sms <= 0) num_sms = current_sm_count();
   if (num_sms <= 0) return KVQ_ERR_CUDA;
   const int group = q_heads / kv_heads;
-  const int head_groups = (group + 7) / 8;
   const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
-  const int grid = num_sms * kPlanCtasPerSm;
-  int chunk;
-  if (num_splits > 0) {
-    const int s = std::min(num_splits, nblk);
-    chunk = (nblk + s - 1) / s;
-  } else {
-    // enough work items for every CTA, chunks of 256 to 512 tokens
-    const int64_t unsplit = static_cast<int64_t>(batch) * kv_heads * head_groups;
-    const int64_t want = static_cast<int64_t>(kItemsPerCta) * grid;
-    const int64_t s = unsplit > 0 ? std::max<int64_t>(1, (want + unsplit - 1) / unsplit) : 1;
-    chunk = static_cast<int>((nblk + s - 1) / s);
-    chunk = std::max(chunk, kAutoMinChunk);
-    chunk = std::min(chunk, kAutoMaxChunk);
-    chunk = std::min(chunk, nblk);
-  }
-  chunk = std::max(1, std::min(chunk, kvq::kMaxChunkBlocks));
-  const int splits = (nblk + chunk - 1) / chunk;
-  plan->chunk_blocks = chunk;
-  plan->max_splits = splits;
-  plan->head_groups = head_groups;
-  plan->grid_ctas = grid;
+  plan->min_blocks_per_warp =
+      num_splits > 0 ? (nblk + num_splits - 1) / num_splits : kAutoMinBlocksPerWarp;
+  plan->warps = num_sms * kvq::kMaxCtasPerSm * (kvq::kDecodeThreads / 32);
+  plan->head_groups = (group + 7) / 8;
+  plan->heads_per_group = std::min(group, 8);
   plan->num_sms = num_sms;
-  plan->reserved = 0;
-  if (splits > 1) {
-    const size_t rows = static_cast<size_t>(batch) * q_heads * splits;
-    plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(float), 256) +
-                            align_up(rows * sizeof(float) * 2, 256);
-  } else {
-    plan->workspace_bytes = 0;
-  }
+  plan->max_ctas_per_sm = kvq::kMaxCtasPerSm;
+  plan->workspace_bytes =
+      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256) +
+      static_cast<size_t>(plan->warps) * 2 * plan->heads_per_group * kvq::kPartStride *
+          sizeof(float);
   return KVQ_OK;
 }
 
@@ -191,10 +168,9 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
-  if (plan.workspace_bytes > 0) {
-    if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return KVQ_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
-  }
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
   kvq::DecodeArgs a;
   a.k = static_cast<const uint8_t*>(pool->k);
   a.v = static_cast<const uint8_t*>(pool->v);
@@ -211,29 +187,26 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   a.q_heads = q_heads;
   a.group = q_heads / pool->kv_heads;
   a.head_groups = plan.head_groups;
-  a.chunk_blocks = plan.chunk_blocks;
-  a.max_splits = plan.max_splits;
-  a.len_cap = std::min(max_blocks_per_seq, plan.max_splits * plan.chunk_blocks) * kBlock;
+  a.hpg = plan.heads_per_group;
+  a.min_blocks_per_warp = plan.min_blocks_per_warp;
+  const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
+  a.len_cap = std::min(max_blocks_per_seq, nblk) * kBlock;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  if (plan.max_splits > 1) {
-    const size_t rows = static_cast<size_t>(batch) * q_heads * plan.max_splits;
-    a.part_o = static_cast<float*>(workspace);
-    a.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                          align_up(rows * kHeadDim * sizeof(float), 256));
-  } else {
-    a.part_o = nullptr;
-    a.part_ml = nullptr;
-  }
+  a.hdr = static_cast<int32_t*>(workspace);
+  a.part = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) +
+      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256));
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // persistent grid: as many CTAs as fit on the device at once
-  const int per_sm = kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
+  // persistent grid: as many CTAs as fit on the device at once (the
+  // workspace has partial slots for kMaxCtasPerSm per SM)
+  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
+                              kvq::kMaxCtasPerSm);
   if (per_sm <= 0) return KVQ_ERR_CUDA;
   const int grid = plan.num_sms * per_sm;
   if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  if (plan.max_splits > 1 && kvq::launch_combine(a, q_dtype, s) != cudaSuccess)
-    return KVQ_ERR_CUDA;
+  if (kvq::launch_combine(a, q_dtype, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 

@@ -6,17 +6,19 @@
 // blocks; §2.4: INT8/INT4 KV with per-token, per-head scale and zero.
 //
 // Work decomposition
-//   A work item is (request b, kv head h, q-head group of up to 8, chunk s)
-//   where a chunk is `chunk_blocks` consecutive logical blocks. A persistent
-//   grid of CTAs walks the items round-robin; every CTA first scans the
-//   request lengths into per-request chunk counts in shared memory so that
-//   short requests cost no empty CTAs. All q heads of a kv head's group are
-//   handled by the same CTA, so every KV byte is read from HBM once.
-//   Inside a CTA, 4 warps take the chunk's blocks round-robin, each keeping
-//   its own online-softmax state, and merge through shared memory at the end.
-//   A request covered by one chunk writes its output directly; longer ones
-//   write (running max, sum, unnormalised output) partials that the combine
-//   kernel merges with a log-sum-exp.
+//   All the work is one stream of blocks ordered by (q-head group, request,
+//   block), where a q-head group is a kv head with up to 8 of its q heads.
+//   A persistent grid (as many CTAs as fit on the device) gives every warp
+//   one contiguous range of the stream of equal length, so the split between
+//   warps is exact whatever the mix of request lengths. Each CTA first scans
+//   the request lengths into per-request block offsets in shared memory.
+//   A warp streams its range through its own ring of shared-memory stages
+//   (cp.async, several blocks in flight), crossing request boundaries without
+//   a pause: it writes the output of every request it covers entirely and,
+//   for the request holding the first and the one holding the last block of
+//   its range, a partial record (running max, sum, unnormalised output) that
+//   the combine kernel merges with a log-sum-exp. All q heads of a kv head's
+//   group are handled by the same warp, so every KV byte is read once.
 //
 // Per-block arithmetic of one warp (16 tokens of one kv head):
 //   S^T = K Q^T  with mma.m16n8k16: M = 16 tokens, N = 8 q heads (padded),
@@ -283,33 +285,52 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
   }
 }
 
-// Merge area of the CTA (aliased onto the pipeline stages once they drain).
-struct Merge {
-  float m[kWarps][kHeadsPerGroup];
-  float l[kWarps][kHeadsPerGroup];
-  float2 o[kWarps][kHeadsPerGroup][kHeadDim / 2];
-};
-
-constexpr int kBtCacheBytes = kMaxChunkBlocks * 4;
-
 __host__ __device__ constexpr size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 
-// Dynamic shared memory: [request chunk prefix sums][block ids of the item]
-// [pipeline stages of every warp, the merge area aliased at their start].
-template <int KV>
-__host__ __device__ constexpr size_t stage_region_bytes() {
-  return static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes > sizeof(Merge)
-             ? static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes
-             : sizeof(Merge);
-}
+// Dynamic shared memory: [prefix sums of the blocks per request][pipeline
+// stages of every warp].
 template <int KV>
 __host__ __device__ constexpr size_t smem_bytes_for(int batch) {
-  return align128((batch + 1) * sizeof(int32_t)) + kBtCacheBytes + stage_region_bytes<KV>();
+  return align128((batch + 1) * sizeof(int32_t)) +
+         static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes;
 }
 
 // Clamped length of request b.
 __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
   return min(max(a.seq_lens[b], 0), a.len_cap);
+}
+
+// Position in the block stream: q-head group hgi (kv head * head_groups +
+// group), request b, block j of nblk.
+struct Cursor {
+  int hgi, b, j, nblk;
+};
+
+__device__ __forceinline__ void locate(Cursor& c, int64_t x, const int32_t* cum, int batch,
+                                       int tb) {
+  c.hgi = static_cast<int>(x / tb);
+  const int r = static_cast<int>(x - static_cast<int64_t>(c.hgi) * tb);
+  int lo = 0, hi = batch - 1;  // largest b with cum[b] <= r: the non-empty request holding r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  c.b = lo;
+  c.j = r - cum[lo];
+  c.nblk = cum[lo + 1] - cum[lo];
+}
+
+// Next block of the stream (the caller knows there is one).
+__device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch) {
+  if (++c.j < c.nblk) return;
+  c.j = 0;
+  do {
+    if (++c.b == batch) {
+      c.b = 0;
+      ++c.hgi;
+    }
+    c.nblk = cum[c.b + 1] - cum[c.b];
+  } while (c.nblk == 0);
 }
 
 template <int KV, bool QBF>
@@ -322,32 +343,27 @@ __global__ void __launch_bounds__(kDecodeThreads)
   constexpr bool kPvBf = KV == kBF16;  // P.V product type: bf16 only for bf16 pools
   constexpr float kMid = KV == kI8 ? 128.f : 8.f;  // code centre (quantized pools)
   constexpr int D = S::kDepth;
+  constexpr unsigned kFull = 0xFFFFFFFFu;
 
-  int32_t* cum = reinterpret_cast<int32_t*>(dsmem);  // [batch + 1] prefix of chunk counts
-  int32_t* s_bt = reinterpret_cast<int32_t*>(dsmem + align128((a.batch + 1) * sizeof(int32_t)));
-  unsigned char* stages = dsmem + align128((a.batch + 1) * sizeof(int32_t)) + kBtCacheBytes;
-  Merge& mg = *reinterpret_cast<Merge*>(stages);
+  int32_t* cum = reinterpret_cast<int32_t*>(dsmem);  // [batch + 1]: blocks before request b
+  unsigned char* stages = dsmem + align128((a.batch + 1) * sizeof(int32_t));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int chunk_tokens = a.chunk_blocks * kBlock;
-  const uint32_t my_stages = static_cast<uint32_t>(__cvta_generic_to_shared(stages)) +
-                             static_cast<uint32_t>(warp * D * S::kBytes);
 
-  // ---- chunk counts of every request, prefix-summed --------------------------
+  // ---- blocks per request, prefix-summed (every CTA) --------------------------
   {
     const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
     const int b0 = min(tid * per, a.batch), b1 = min(b0 + per, a.batch);
     int sum = 0;
     for (int b = b0; b < b1; ++b) {
-      const int L = clamped_len(a, b);
-      sum += max(1, (L + chunk_tokens - 1) / chunk_tokens);
+      sum += (clamped_len(a, b) + kBlock - 1) / kBlock;
       if (blockIdx.x == 0 && a.seq_lens[b] > a.len_cap) report(a.dev_err, KVQ_DEV_ERR_LENGTH);
     }
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      const int y = __shfl_up_sync(kFull, incl, off);
       if (lane >= off) incl += y;
     }
     if (lane == 31) warp_sum[warp] = incl;
@@ -357,66 +373,148 @@ __global__ void __launch_bounds__(kDecodeThreads)
     int run = base + incl - sum;
     for (int b = b0; b < b1; ++b) {
       cum[b] = run;
-      run += max(1, (clamped_len(a, b) + chunk_tokens - 1) / chunk_tokens);
+      run += (clamped_len(a, b) + kBlock - 1) / kBlock;
     }
     if (tid == kDecodeThreads - 1) cum[a.batch] = base + incl;
     __syncthreads();
   }
-  const int total_chunks = cum[a.batch];
+  const int tb = cum[a.batch];  // blocks of one q-head group over all requests
   const int groups = a.kv_heads * a.head_groups;
-  const int64_t total_items = static_cast<int64_t>(total_chunks) * groups;
-
-  for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
-    const int hgi = static_cast<int>(item / total_chunks);
-    const int r = static_cast<int>(item % total_chunks);
-    // request: largest b with cum[b] <= r
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (cum[mid] <= r) lo = mid; else hi = mid - 1;
+  const int64_t total = static_cast<int64_t>(tb) * groups;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t even_share = (total + nwarps - 1) / nwarps;
+  const int P = static_cast<int>(even_share > a.min_blocks_per_warp ? even_share
+                                                                    : a.min_blocks_per_warp);
+  if (blockIdx.x == 0) {
+    // what the combine kernel needs, and the all-zero rows of empty requests
+    if (tid == 0) {
+      a.hdr[0] = tb;
+      a.hdr[1] = P;
     }
-    const int b = lo;
-    const int s = r - cum[b];
-    const int h = hgi / a.head_groups;
-    const int hg = hgi - h * a.head_groups;
-    const int L = clamped_len(a, b);
-    const int n_chunks = max(1, (L + chunk_tokens - 1) / chunk_tokens);
-    const int nblk = (L + kBlock - 1) / kBlock;
-    const int blk_begin = s * a.chunk_blocks;
-    const int blk_end = min(blk_begin + a.chunk_blocks, nblk);
-    const int hq0 = h * a.group + hg * kHeadsPerGroup;
-    const int nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
+    for (int b = tid; b <= a.batch; b += kDecodeThreads) a.hdr[2 + b] = cum[b];
+    for (int b = 0; b < a.batch; ++b) {
+      if (cum[b + 1] != cum[b]) continue;
+      for (int e = tid; e < a.q_heads * kHeadDim; e += kDecodeThreads)
+        store_out<QBF>(a.out, static_cast<int64_t>(b) * a.q_heads * kHeadDim + e, 0.f);
+    }
+  }
 
-    // block ids of this item, once for the CTA
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks;
-    for (int i = tid; i < blk_end - blk_begin; i += kDecodeThreads) s_bt[i] = bt[blk_begin + i];
-    __syncthreads();
+  // ---- this warp's range [x0, x0 + n) of the stream -----------------------------
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t x0 = gw * P;
+  if (x0 >= total) return;  // no block barrier follows: warps are independent from here
+  const int n = static_cast<int>(total - x0 < P ? total - x0 : P);
+  const uint32_t my_stages = static_cast<uint32_t>(__cvta_generic_to_shared(stages)) +
+                             static_cast<uint32_t>(warp * D * S::kBytes);
 
-    // this warp's blocks: blk_begin + warp + kWarps * k, k < n_w
-    const int n_w = blk_end - blk_begin > warp ? (blk_end - blk_begin - warp + kWarps - 1) / kWarps
-                                               : 0;
-    auto issue = [&](int k) {
-      if (k < n_w) {
-        const int32_t phys = s_bt[warp + kWarps * k];
-        if (phys >= 0 && phys < a.num_blocks)
-          issue_block<KV>(my_stages + (k % D) * S::kBytes, a, phys, h, lane);
-        else if (lane == 0)
-          report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+  // issue side: cursor, a 32-entry window of the block table, validity bits
+  Cursor ic;
+  locate(ic, x0, cum, a.batch, tb);
+  Cursor cc = ic;  // compute side
+  int win_b = -1, win_j0 = 0;
+  int32_t win = -1;
+  uint32_t ok_mask = 0;
+  auto issue = [&](int k) {
+    if (k < n) {
+      if (ic.b != win_b || ic.j >= win_j0 + 32) {
+        win_b = ic.b;
+        win_j0 = ic.j;
+        const int jj = win_j0 + lane;
+        win = jj < ic.nblk ? a.block_tables[static_cast<int64_t>(ic.b) * a.max_blocks + jj] : -1;
       }
-      cp_async_commit();
-    };
+      const int32_t phys = __shfl_sync(kFull, win, ic.j - win_j0);
+      const bool ok = phys >= 0 && phys < a.num_blocks;
+      const uint32_t bit = 1u << (k % D);
+      if (ok) {
+        issue_block<KV>(my_stages + (k % D) * S::kBytes, a, phys, ic.hgi / a.head_groups, lane);
+        ok_mask |= bit;
+      } else {
+        ok_mask &= ~bit;
+        if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+      }
+      if (k + 1 < n) advance(ic, cum, a.batch);
+    }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int k = 0; k < D - 1; ++k) issue(k);
+  for (int k = 0; k < D - 1; ++k) issue(k);
 
-    // ---- Q fragments (B operand of S^T = K Q^T), permuted like the K dims --
-    uint32_t qb[8][2];
-    float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
-    {
+  // ---- per-request state ---------------------------------------------------------
+  int seg_b = -1, seg_hgi = -1, hq0 = 0, nh = 0, L = 0, seg_nblk = 0;
+  int64_t seg_start = 0;
+  uint32_t qb[8][2];
+  float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
+  bool hv0 = false, hv1 = false;
+  float o[8][4];
+  float m0, m1, l0, l1, z0, z1;
+
+  // writes the finished state of request seg_b: the output if this warp
+  // covered all of its blocks, else a partial record
+  auto flush = [&]() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+      if constexpr (kQuant) {
+        z0 += __shfl_xor_sync(kFull, z0, off);
+        z1 += __shfl_xor_sync(kFull, z1, off);
+      }
+    }
+    const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
+    const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int hh = 2 * t + u;
+      if (hh >= nh) continue;
+      const float z = u ? z1 : z0, l = u ? l1 : l0, m = u ? m1 : m0;
+      if (contained) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = pack2<QBF>((o[i][u] + z) * inv, (o[i][2 + u] + z) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                              (row0 + hh) * kHeadDim + 16 * g);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+        const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
+        float* rec = a.part + ((gw * 2 + slot) * a.hpg + hh) * kPartStride;
+        float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2)
+          ov[i / 2] = make_float4(o[i][u] + z, o[i][2 + u] + z, o[i + 1][u] + z, o[i + 1][2 + u] + z);
+        if (g == 0) {
+          rec[kHeadDim] = m;
+          rec[kHeadDim + 1] = l;
+        }
+      }
+    }
+  };
+
+  for (int k = 0; k < n; ++k) {
+    issue(k + D - 1);        // refills the stage block k - 1 used
+    cp_async_wait<D - 1>();  // this lane's copies of block k have landed
+    __syncwarp();            // ... and every other lane's
+
+    if (cc.b != seg_b || cc.hgi != seg_hgi) {
+      if (seg_b >= 0) flush();
+      // start request cc.b for q-head group cc.hgi
+      seg_b = cc.b;
+      seg_hgi = cc.hgi;
+      seg_nblk = cc.nblk;
+      seg_start = static_cast<int64_t>(cc.hgi) * tb + cum[cc.b];
+      const int h = cc.hgi / a.head_groups;
+      const int hg = cc.hgi - h * a.head_groups;
+      hq0 = h * a.group + hg * kHeadsPerGroup;
+      nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
+      L = clamped_len(a, cc.b);
+      // Q fragments (B operand of S^T = K Q^T), permuted like the K dims
       uint32_t qw[16];
       if (g < nh) {
         const uint4* qp = reinterpret_cast<const uint4*>(
             static_cast<const uint16_t*>(a.q) +
-            (static_cast<int64_t>(b) * a.q_heads + hq0 + g) * kHeadDim + 32 * t);
+            (static_cast<int64_t>(cc.b) * a.q_heads + hq0 + g) * kHeadDim + 32 * t);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint4 v = qp[i];
@@ -444,193 +542,148 @@ __global__ void __launch_bounds__(kDecodeThreads)
         float part = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) part += lo_to_float<QBF>(qw[i]) + hi_to_float<QBF>(qw[i]);
-        part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
-        part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
-        // lanes 4h hold sum(q) of head h
-        qs0 = __shfl_sync(0xFFFFFFFFu, part, (2 * t) * 4);
-        qs1 = __shfl_sync(0xFFFFFFFFu, part, (2 * t + 1) * 4);
+        part += __shfl_xor_sync(kFull, part, 1);
+        part += __shfl_xor_sync(kFull, part, 2);
+        qs0 = __shfl_sync(kFull, part, (2 * t) * 4);  // lanes 4h hold sum(q) of head h
+        qs1 = __shfl_sync(kFull, part, (2 * t + 1) * 4);
       }
+      hv0 = 2 * t < nh;
+      hv1 = 2 * t + 1 < nh;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = z0 = z1 = 0.f;
     }
-    const bool hv0 = 2 * t < nh, hv1 = 2 * t + 1 < nh;
 
-    float o[8][4];
+    if ((ok_mask >> (k % D)) & 1u) {
+      Frag<KV> cur;
+      read_frag<KV>(cur, my_stages + (k % D) * S::kBytes, g, t);
+      // S^T = K Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
-
-    for (int k = 0; k < n_w; ++k) {
-      issue(k + D - 1);      // refills the stage block k - 1 used
-      cp_async_wait<D - 1>();  // this lane's copies of block k have landed
-      __syncwarp();            // ... and every other lane's
-      const int j = blk_begin + warp + kWarps * k;
-      const int32_t phys = s_bt[warp + kWarps * k];
-      if (phys >= 0 && phys < a.num_blocks) {
-        Frag<KV> cur;
-        read_frag<KV>(cur, my_stages + (k % D) * S::kBytes, g, t);
-        // S^T = K Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          uint32_t ak[4];
-          k_operand<KV, QBF>(cur, kk, ak);
-          mma16816<QBF>(sc, ak, qb[kk]);
-        }
-        // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
-        const int tok0 = j * kBlock + g, tok1 = tok0 + 8;
-        float s00, s01, s10, s11;
-        if constexpr (kQuant) {
-          // q.k = S (q.(c - mid)) + (Z + mid S) sum(q)
-          const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) + kMid * S0;
-          const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) + kMid * S1;
-          s00 = (S0 * sc[0] + Z0 * qs0) * a.sm_scale_log2;
-          s01 = (S0 * sc[1] + Z0 * qs1) * a.sm_scale_log2;
-          s10 = (S1 * sc[2] + Z1 * qs0) * a.sm_scale_log2;
-          s11 = (S1 * sc[3] + Z1 * qs1) * a.sm_scale_log2;
-        } else {
-          s00 = sc[0] * a.sm_scale_log2;
-          s01 = sc[1] * a.sm_scale_log2;
-          s10 = sc[2] * a.sm_scale_log2;
-          s11 = sc[3] * a.sm_scale_log2;
-        }
-        if (tok0 >= L) s00 = s01 = -INFINITY;
-        if (tok1 >= L) s10 = s11 = -INFINITY;
-        if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
-        if (!hv1) s01 = s11 = 0.f;
-        // block max over the 16 tokens (lanes with equal t)
-        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          bm0 = fmaxf(bm0, __shfl_xor_sync(0xFFFFFFFFu, bm0, off));
-          bm1 = fmaxf(bm1, __shfl_xor_sync(0xFFFFFFFFu, bm1, off));
-        }
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-        const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
-        const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        l0 = l0 * al0 + (p00 + p10);
-        l1 = l1 * al1 + (p01 + p11);
-        float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
-        if constexpr (kQuant) {
-          // sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t (Z_t + mid S_t)
-          const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
-          const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
-          z0 = z0 * al0 + (p00 * Z0 + p10 * Z1);
-          z1 = z1 * al1 + (p01 * Z0 + p11 * Z1);
-          q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i][0] *= al0; o[i][2] *= al0;
-          o[i][1] *= al1; o[i][3] *= al1;
-        }
-        // P'^T as the B operand: transpose the (token x head) fragments
-        uint32_t bp[2], bp_lo[2];
-        const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
-        bp[0] = movmatrix_trans(h0);
-        bp[1] = movmatrix_trans(h1);
-        if constexpr (kPvBf) {
-          // bf16 keeps 8 bits of P: add the rounding residual in a second
-          // product so P carries ~16 bits (P = hi + lo)
-          bp_lo[0] = movmatrix_trans(pack2<true>(q00 - lo_to_float<true>(h0),
-                                                 q01 - hi_to_float<true>(h0)));
-          bp_lo[1] = movmatrix_trans(pack2<true>(q10 - lo_to_float<true>(h1),
-                                                 q11 - hi_to_float<true>(h1)));
-        }
-        // O^T += V^T P'^T
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t av[4];
-          v_operand<KV>(cur, i, av);
-          mma16816<kPvBf>(o[i], av, bp);
-          if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t ak[4];
+        k_operand<KV, QBF>(cur, kk, ak);
+        mma16816<QBF>(sc, ak, qb[kk]);
       }
-      __syncwarp();  // all lanes are done with this stage before it is refilled
-    }
-    cp_async_wait<0>();
-
-    // ---- finish this warp: sums over the 8 token lanes -----------------------
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
-      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+      // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
+      const int tok0 = cc.j * kBlock + g, tok1 = tok0 + 8;
+      float s00, s01, s10, s11;
       if constexpr (kQuant) {
-        z0 += __shfl_xor_sync(0xFFFFFFFFu, z0, off);
-        z1 += __shfl_xor_sync(0xFFFFFFFFu, z1, off);
-      }
-    }
-    __syncthreads();  // every warp's stages are drained: the merge area may overwrite them
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mg.o[warp][2 * t][8 * g + i] = make_float2(o[i][0] + z0, o[i][2] + z0);
-      mg.o[warp][2 * t + 1][8 * g + i] = make_float2(o[i][1] + z1, o[i][3] + z1);
-    }
-    if (g == 0) {
-      mg.m[warp][2 * t] = m0;
-      mg.m[warp][2 * t + 1] = m1;
-      mg.l[warp][2 * t] = l0;
-      mg.l[warp][2 * t + 1] = l1;
-    }
-    __syncthreads();
-
-    // ---- merge the warps; write the output or the partial ---------------------
-    for (int idx = tid; idx < nh * kHeadDim; idx += kDecodeThreads) {
-      const int hh = idx / kHeadDim, d = idx % kHeadDim;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mg.m[w][hh]);
-      float acc = 0.f, lsum = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float e = exp2f(mg.m[w][hh] - M);
-          const float2 ov = mg.o[w][hh][d >> 1];
-          acc += e * ((d & 1) ? ov.y : ov.x);
-          lsum += e * mg.l[w][hh];
-        }
-      }
-      const int hq = hq0 + hh;
-      const int64_t bh = static_cast<int64_t>(b) * a.q_heads + hq;
-      if (n_chunks == 1) {
-        store_out<QBF>(a.out, bh * kHeadDim + d, lsum > 0.f ? acc / lsum : 0.f);
+        // q.k = S (q.(c - mid)) + (Z + mid S) sum(q)
+        const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) + kMid * S0;
+        const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) + kMid * S1;
+        s00 = (S0 * sc[0] + Z0 * qs0) * a.sm_scale_log2;
+        s01 = (S0 * sc[1] + Z0 * qs1) * a.sm_scale_log2;
+        s10 = (S1 * sc[2] + Z1 * qs0) * a.sm_scale_log2;
+        s11 = (S1 * sc[3] + Z1 * qs1) * a.sm_scale_log2;
       } else {
-        const int64_t ps = bh * a.max_splits + s;
-        a.part_o[ps * kHeadDim + d] = acc;
-        if (d == 0) a.part_ml[ps] = make_float2(M, lsum);
+        s00 = sc[0] * a.sm_scale_log2;
+        s01 = sc[1] * a.sm_scale_log2;
+        s10 = sc[2] * a.sm_scale_log2;
+        s11 = sc[3] * a.sm_scale_log2;
+      }
+      if (tok0 >= L) s00 = s01 = -INFINITY;
+      if (tok1 >= L) s10 = s11 = -INFINITY;
+      if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
+      if (!hv1) s01 = s11 = 0.f;
+      // block max over the 16 tokens (lanes with equal t)
+      float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+      }
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
+      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 = l0 * al0 + (p00 + p10);
+      l1 = l1 * al1 + (p01 + p11);
+      float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
+      if constexpr (kQuant) {
+        // sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t (Z_t + mid S_t)
+        const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
+        const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
+        z0 = z0 * al0 + (p00 * Z0 + p10 * Z1);
+        z1 = z1 * al1 + (p01 * Z0 + p11 * Z1);
+        q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] *= al0; o[i][2] *= al0;
+        o[i][1] *= al1; o[i][3] *= al1;
+      }
+      // P'^T as the B operand: transpose the (token x head) fragments
+      uint32_t bp[2], bp_lo[2];
+      const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
+      bp[0] = movmatrix_trans(h0);
+      bp[1] = movmatrix_trans(h1);
+      if constexpr (kPvBf) {
+        // bf16 keeps 8 bits of P: add the rounding residual in a second
+        // product so P carries ~16 bits (P = hi + lo)
+        bp_lo[0] = movmatrix_trans(pack2<true>(q00 - lo_to_float<true>(h0),
+                                               q01 - hi_to_float<true>(h0)));
+        bp_lo[1] = movmatrix_trans(pack2<true>(q10 - lo_to_float<true>(h1),
+                                               q11 - hi_to_float<true>(h1)));
+      }
+      // O^T += V^T P'^T
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t av[4];
+        v_operand<KV>(cur, i, av);
+        mma16816<kPvBf>(o[i], av, bp);
+        if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
       }
     }
-    __syncthreads();  // the merge area and s_bt are reused by the next item
+    __syncwarp();  // all lanes are done with this stage before it is refilled
+    if (k + 1 < n) advance(cc, cum, a.batch);
   }
+  cp_async_wait<0>();
+  flush();
 }
 
-// One warp per (request, q head): merge the chunk partials of requests that
-// span more than one chunk (log-sum-exp in the exp2 domain).
+// One warp per (request, q head): merge the partial records of a request
+// whose blocks were split between warps (log-sum-exp in the exp2 domain).
+// Requests covered by one warp were written by the decode kernel.
 template <bool QBF>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (bh >= static_cast<int64_t>(a.batch) * a.q_heads) return;
   const int b = static_cast<int>(bh / a.q_heads);
-  const int chunk_tokens = a.chunk_blocks * kBlock;
-  const int L = clamped_len(a, b);
-  const int n = max(1, (L + chunk_tokens - 1) / chunk_tokens);
-  if (n == 1) return;  // written by the decode kernel
-  const float2* ml = a.part_ml + bh * a.max_splits;
+  const int hq = static_cast<int>(bh - static_cast<int64_t>(b) * a.q_heads);
+  const int tb = a.hdr[0], P = a.hdr[1];
+  const int32_t* cum = a.hdr + 2;
+  const int nblk = cum[b + 1] - cum[b];
+  if (nblk == 0) return;
+  const int h = hq / a.group, within = hq - h * a.group;
+  const int hgi = h * a.head_groups + within / kHeadsPerGroup;
+  const int hh = within % kHeadsPerGroup;
+  const int64_t seg_start = static_cast<int64_t>(hgi) * tb + cum[b];
+  const int64_t w_first = seg_start / P, w_last = (seg_start + nblk - 1) / P;
+  if (w_first == w_last) return;
+  auto rec_of = [&](int64_t w) {
+    const int slot = (w == w_first && seg_start != w * P) ? 1 : 0;
+    return a.part + ((w * 2 + slot) * a.hpg + hh) * kPartStride;
+  };
   float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[s].x);
+  for (int64_t w = w_first + lane; w <= w_last; w += 32) M = fmaxf(M, rec_of(w)[kHeadDim]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
-  const float4* po = reinterpret_cast<const float4*>(a.part_o + bh * a.max_splits * kHeadDim);
-  for (int s = 0; s < n; ++s) {
-    const float2 v = ml[s];
-    const float e = (v.x == -INFINITY) ? 0.f : exp2f(v.x - M);
-    lsum += e * v.y;
-    const float4 x = po[s * (kHeadDim / 4) + lane];
-    acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+  if (M != -INFINITY) {
+    for (int64_t w = w_first; w <= w_last; ++w) {
+      const float* rec = rec_of(w);
+      const float mw = rec[kHeadDim];
+      const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+      lsum += e * rec[kHeadDim + 1];
+      const float4 x = reinterpret_cast<const float4*>(rec)[lane];
+      acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+    }
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const int64_t base = bh * kHeadDim + 4 * lane;

@@ -56,12 +56,13 @@ struct DecodeArgs {
   int q_heads;
   int group;             // q_heads / kv_heads
   int head_groups;       // ceil(group / 8)
-  int chunk_blocks;      // blocks per work item
-  int max_splits;        // chunks of the longest allowed request
+  int hpg;               // heads per group slot: min(group, 8)
+  int min_blocks_per_warp;
   int len_cap;           // lengths are clamped to this (tokens)
   float sm_scale_log2;   // sm_scale * log2(e): scores live in the exp2 domain
-  float* part_o;         // [B, Hq, max_splits, D]   (max_splits > 1)
-  float2* part_ml;       // [B, Hq, max_splits]      (running max, sum)
+  float* part;           // [warps][2][hpg][kPartStride]: o[128], max, sum
+  int32_t* hdr;          // [0] blocks per head group, [1] blocks per warp,
+                         // [2 .. 2 + batch] prefix sums of the blocks per request
   int32_t* dev_err;
 };
 
@@ -76,7 +77,8 @@ cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s);
 int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
 
 constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared memory
-constexpr int kMaxChunkBlocks = 1024;  // blocks per work item
 constexpr int kDecodeThreads = 128;
+constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many CTAs per SM
+constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)
 
 }  // namespace kvq

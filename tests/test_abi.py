@@ -101,23 +101,26 @@ def test_tables_validation(lib):
 
 def test_planner(lib):
     plan = kvq.paged_decode_attn_plan
-    # one work item per request when they are few and long enough to split
     p = plan(128, 32, 32, 4096, num_sms=152)
-    assert p["chunk_blocks"] * p["max_splits"] >= 256
-    assert 16 <= p["chunk_blocks"] <= 32
-    assert p["grid_ctas"] == 152 * 4
-    assert p["workspace_bytes"] >= 128 * 32 * p["max_splits"] * 130 * 4
-    # short contexts: a single chunk and no workspace
-    p = plan(4, 16, 8, 100, num_sms=152)
-    assert p["max_splits"] == 1 and p["workspace_bytes"] == 0
-    # explicit split counts
+    assert p["warps"] == 152 * 4 * 4 and p["max_ctas_per_sm"] == 4
+    assert p["min_blocks_per_warp"] == 4
+    assert p["head_groups"] == 1 and p["heads_per_group"] == 1
+    # two partial records (132 floats) per warp and head, plus the length header
+    assert p["workspace_bytes"] >= p["warps"] * 2 * 132 * 4 + 4 * 131
+    p4 = plan(64, 32, 8, 8192, num_sms=152)
+    assert p4["heads_per_group"] == 4
+    assert p4["workspace_bytes"] >= p4["warps"] * 2 * 4 * 132 * 4
+    # the workspace does not grow with the context
+    assert plan(64, 32, 8, 100, num_sms=152)["workspace_bytes"] == p4["workspace_bytes"]
+    # explicit split counts bound the pieces of a request
     for s in (1, 2, 3, 7):
         p = plan(6, 16, 8, 4000, num_splits=s, num_sms=152)
-        nblk = (4000 + 15) // 16
-        assert p["max_splits"] == -(-nblk // p["chunk_blocks"])
-        assert p["max_splits"] <= s
-    # head groups of 8
-    assert plan(2, 64, 2, 64, num_sms=10)["head_groups"] == 4
+        assert p["min_blocks_per_warp"] == -(-250 // s)
+    # q heads of a kv head are taken 8 at a time
+    p = plan(2, 64, 2, 64, num_sms=10)
+    assert p["head_groups"] == 4 and p["heads_per_group"] == 8
+    p = plan(2, 12, 4, 64, num_sms=10)
+    assert p["head_groups"] == 1 and p["heads_per_group"] == 3
     with pytest.raises(kvq.KvqError):
         plan(2, 6, 4, 64, num_sms=10)
     with pytest.raises(kvq.KvqError):
