@@ -22,23 +22,29 @@
 //
 // Per-block arithmetic of one warp (16 tokens of one kv head):
 //   S^T = K Q^T  with mma.m16n8k16: M = 16 tokens, N = 8 q heads (padded),
-//                K = 128 dims in 8 steps.
+//                K = 128 dims in 8 steps (two independent accumulators).
 //   O^T += V^T P'^T with M = 16 dims (8 steps over 128), N = 8 heads,
 //                K = 16 tokens.
-//   For INT8/INT4 pools the codes go into the tensor cores exactly, centred
-//   on mid = 128 or 8 (as fp16 or bf16 integers), and the per-token scale S
-//   and zero Z are applied outside: with Z' = Z + mid S,
-//     q.k = S (q.(c - mid)) + Z' sum(q)
-//     sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t Z'_t.
-//   Centring keeps the two terms from cancelling, so the 16-bit rounding of
-//   p_t S_t stays small next to the result. The P.V product is fp16 for
-//   quantized pools whatever Q's type (P' <= S fits fp16). The score
-//   fragment is transposed in registers (movmatrix) to become the B operand
-//   of the second product.
-//   Each lane's K and V loads are 8-32 contiguous bytes of a token row;
-//   the dims are assigned to mma k-columns so that the loads stay contiguous
-//   (the dot product does not depend on the order of the dims, and Q is
-//   permuted the same way once per item).
+//   Quantized codes go into the tensor cores as exact 16-bit floats a + c,
+//   made by writing the code into the mantissa of a constant (INT4: a shift
+//   and a lop3 per two codes, a = 16; INT8: a prmt and a packed subtract,
+//   centred: a = -128); the offset is removed outside the products together
+//   with the per-token zero: c S + Z = (a + c) S + Z - a S.
+//     q.k = S (q.(a + c)) + (Z - a S) sum(q)
+//     sum_t p_t v_t = sum_t P'_t (a + c_t) + sum_t p_t (Z_t + mid S_t)
+//                     - (a + mid) sum_t P'_t,   P'_t = fp16(p_t S_t)
+//   where the last sum runs over the rounded P' fed to the product, so their
+//   rounding error only multiplies c - mid (mid = 2^(b-1)); for centred INT8
+//   codes (a = -mid) that term vanishes. The INT4 offset of 16 keeps the P.V
+//   accumulator within a few times its centred size, so its fp32
+//   accumulation error stays negligible over long contexts. The P.V product is fp16 for quantized
+//   pools whatever Q's type (P' = p S <= S fits fp16); bf16 pools carry P as a
+//   bf16 hi + lo pair. The score fragment is transposed in registers
+//   (movmatrix) to become the B operand of the second product.
+//   Each lane's K and V reads are 8-64 contiguous bytes of a token row; the
+//   dims are assigned to mma k-columns so that these stay contiguous (the dot
+//   product does not depend on the order of the dims, and Q is permuted the
+//   same way once per request).
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -49,6 +55,7 @@ namespace {
 
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kHeadsPerGroup = 8;  // mma N
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // ---- per-block fragments ------------------------------------------------------
 
@@ -78,6 +85,17 @@ struct Frag<kI4> {
   uint32_t ksz[2], vsz[2];
 };
 
+// Offset a of the code encoding a + c on the K side (Q's type) and V side,
+// and the middle code (2^(b-1)).
+template <int KV, bool QBF>
+struct CodeOffset {
+  static constexpr float kK = KV == kI8 ? -128.f : (QBF ? 128.f : 16.f);
+  static constexpr float kV = KV == kI8 ? -128.f : 16.f;
+  static constexpr float kMid = KV == kI8 ? 128.f : 8.f;
+  // the rounded-P' correction is needed only when the V codes are not centred
+  static constexpr bool kPCorr = KV == kI4;
+};
+
 // ---- shared-memory staging -------------------------------------------------------
 
 // One pipeline stage holds one 16-token block of one kv head: the K tile and
@@ -91,11 +109,14 @@ struct Stage {
   static constexpr int kSwz = (kChunks < 8 ? kChunks : 8) - 1;
   static constexpr int kTile = kBlock * kRow;
   static constexpr int kBytes = 2 * kTile + (KvTraits<KV>::kQuant ? 128 : 0);
+  static constexpr int kCopies = kBlock * kChunks / 32;    // chunks per lane per tile
+  static constexpr int kKReads = kChunks / 4;              // 16-byte K reads per row
+  static constexpr int kVReads = kChunks >= 8 ? kChunks / 8 : 1;  // V reads per row
   // blocks in flight per warp: about 16 KB of KV per warp
   static constexpr int kDepth = KV == kI4 ? 6 : (KV == kI8 ? 4 : 2);
 };
 
-__device__ __forceinline__ int swz(int r, int c, int mask) { return c ^ (r & mask); }
+__host__ __device__ constexpr int swz(int r, int c, int mask) { return c ^ (r & mask); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -125,24 +146,66 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return r;
 }
 
-// The warp copies block `phys` of kv head h into the stage at shared address
-// st: every lane moves 16-byte chunks of both tiles, lanes 0-7 the scale/zero
-// pairs. Asynchronous (cp.async); the caller commits the group.
+// 2^x by the hardware approximation (relative error about 2^-22; tiny
+// results flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Per-lane constants of the copies into a stage and of the fragment reads
+// from it; only the stage base and the block's global address change.
 template <int KV>
-__device__ __forceinline__ void issue_block(uint32_t st, const DecodeArgs& a, int64_t phys,
-                                            int h, int lane) {
+struct LaneMap {
   using S = Stage<KV>;
-  const int64_t tok_stride = static_cast<int64_t>(a.kv_heads) * S::kRow;
+  uint32_t src[S::kCopies];            // byte offset within the tile's global rows
+  uint32_t dst[S::kCopies];            // byte offset within the stage (V adds kTile)
+  uint32_t kr[2][S::kKReads];          // K fragment reads
+  uint32_t vr[4][S::kVReads];          // V fragment reads
+  __device__ __forceinline__ void init(int lane, int g, int t, uint32_t tok_stride) {
+#pragma unroll
+    for (int i = 0; i < S::kCopies; ++i) {
+      const int n = lane + 32 * i;
+      const int r = n / S::kChunks, c = n % S::kChunks;
+      src[i] = r * tok_stride + c * 16;
+      dst[i] = r * S::kRow + swz(r, c, S::kSwz) * 16;
+    }
+#pragma unroll
+    for (int i = 0; i < S::kKReads; ++i) {
+      const int c = S::kKReads * t + i;
+      kr[0][i] = g * S::kRow + swz(g, c, S::kSwz) * 16;
+      kr[1][i] = (g + 8) * S::kRow + swz(g + 8, c, S::kSwz) * 16;
+    }
+    const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t row = S::kTile + rows[r] * S::kRow;
+      if constexpr (KV == kI4) {
+        vr[r][0] = row + swz(rows[r], g >> 1, S::kSwz) * 16 + 8 * (g & 1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < S::kVReads; ++i)
+          vr[r][i] = row + swz(rows[r], S::kVReads * g + i, S::kSwz) * 16;
+      }
+    }
+  }
+};
+
+// The warp copies block `phys` of kv head h into the stage at shared address
+// st (asynchronous; the caller commits the group).
+template <int KV>
+__device__ __forceinline__ void issue_block(uint32_t st, const DecodeArgs& a,
+                                            const LaneMap<KV>& lm, int64_t phys, int h,
+                                            int lane) {
+  using S = Stage<KV>;
   const int64_t base = (phys * kBlock * a.kv_heads + h) * S::kRow;
   const uint8_t* kb = a.k + base;
   const uint8_t* vb = a.v + base;
 #pragma unroll
-  for (int i = 0; i < kBlock * S::kChunks / 32; ++i) {
-    const int n = lane + 32 * i;
-    const int r = n / S::kChunks, c = n % S::kChunks;
-    const uint32_t off = r * S::kRow + swz(r, c, S::kSwz) * 16;
-    cp_async16(st + off, kb + r * tok_stride + c * 16);
-    cp_async16(st + S::kTile + off, vb + r * tok_stride + c * 16);
+  for (int i = 0; i < S::kCopies; ++i) {
+    cp_async16(st + lm.dst[i], kb + lm.src[i]);
+    cp_async16(st + S::kTile + lm.dst[i], vb + lm.src[i]);
   }
   if constexpr (KvTraits<KV>::kQuant) {
     if (lane < 8) {
@@ -153,46 +216,43 @@ __device__ __forceinline__ void issue_block(uint32_t st, const DecodeArgs& a, in
   }
 }
 
-// This lane's fragment bytes of the staged block: K rows g, g+8 and V rows
-// 2t, 2t+1, 2t+8, 2t+9 (see the operand builders below), and the scale/zero
-// words of tokens g and g+8.
+// This lane's fragment bytes of the staged block and the scale/zero words of
+// tokens g and g+8.
 template <int KV>
-__device__ __forceinline__ void read_frag(Frag<KV>& f, uint32_t st, int g, int t) {
+__device__ __forceinline__ void read_frag(Frag<KV>& f, uint32_t st, const LaneMap<KV>& lm,
+                                          int g) {
   using S = Stage<KV>;
-  const int vr[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-  auto ka = [&](int r, int c) { return st + r * S::kRow + swz(r, c, S::kSwz) * 16; };
-  auto va = [&](int r, int c) { return st + S::kTile + r * S::kRow + swz(r, c, S::kSwz) * 16; };
   if constexpr (KV == kF16 || KV == kBF16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      f.k[0][i] = lds128(ka(g, 4 * t + i));
-      f.k[1][i] = lds128(ka(g + 8, 4 * t + i));
+      f.k[0][i] = lds128(st + lm.kr[0][i]);
+      f.k[1][i] = lds128(st + lm.kr[1][i]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      f.v[r][0] = lds128(va(vr[r], 2 * g));
-      f.v[r][1] = lds128(va(vr[r], 2 * g + 1));
+      f.v[r][0] = lds128(st + lm.vr[r][0]);
+      f.v[r][1] = lds128(st + lm.vr[r][1]);
     }
   } else if constexpr (KV == kI8) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      f.k[0][i] = lds128(ka(g, 2 * t + i));
-      f.k[1][i] = lds128(ka(g + 8, 2 * t + i));
+      f.k[0][i] = lds128(st + lm.kr[0][i]);
+      f.k[1][i] = lds128(st + lm.kr[1][i]);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = lds128(va(vr[r], g));
+    for (int r = 0; r < 4; ++r) f.v[r] = lds128(st + lm.vr[r][0]);
   } else {
-    f.k[0] = lds128(ka(g, t));
-    f.k[1] = lds128(ka(g + 8, t));
+    f.k[0] = lds128(st + lm.kr[0][0]);
+    f.k[1] = lds128(st + lm.kr[1][0]);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = lds64(va(vr[r], g >> 1) + 8 * (g & 1));
+    for (int r = 0; r < 4; ++r) f.v[r] = lds64(st + lm.vr[r][0]);
   }
   if constexpr (KvTraits<KV>::kQuant) {
-    const uint32_t sz = st + 2 * S::kTile;
-    f.ksz[0] = lds32(sz + 4 * g);
-    f.ksz[1] = lds32(sz + 4 * (g + 8));
-    f.vsz[0] = lds32(sz + 64 + 4 * g);
-    f.vsz[1] = lds32(sz + 64 + 4 * (g + 8));
+    const uint32_t sz = st + 2 * S::kTile + 4 * g;
+    f.ksz[0] = lds32(sz);
+    f.ksz[1] = lds32(sz + 32);
+    f.vsz[0] = lds32(sz + 64);
+    f.vsz[1] = lds32(sz + 96);
   }
 }
 
@@ -218,19 +278,19 @@ __device__ __forceinline__ void k_operand(const Frag<KV>& f, int kk, uint32_t (&
       a[1] = bytes_to_bf16_pair(w1, 0, 1);
       a[3] = bytes_to_bf16_pair(w1, 2, 3);
     } else {
-      a[0] = bytes_to_f16_pair(w0, 0x4140u);
-      a[2] = bytes_to_f16_pair(w0, 0x4342u);
-      a[1] = bytes_to_f16_pair(w1, 0x4140u);
-      a[3] = bytes_to_f16_pair(w1, 0x4342u);
+      a[0] = bytes_to_f16(w0, 0x4140u);
+      a[2] = bytes_to_f16(w0, 0x4342u);
+      a[1] = bytes_to_f16(w1, 0x4140u);
+      a[3] = bytes_to_f16(w1, 0x4342u);
     }
   } else {
     // kk = 2 j + u: pairs of dims (8j+2u, 8j+2u+4) and (8j+2u+1, 8j+2u+5)
     const int j = kk >> 1, u = kk & 1;
     const uint32_t w0 = w4(f.k[0], j), w1 = w4(f.k[1], j);
-    a[0] = nibbles_to_pair<QBF>(w0 >> (8 * u));
-    a[2] = nibbles_to_pair<QBF>(w0 >> (8 * u + 4));
-    a[1] = nibbles_to_pair<QBF>(w1 >> (8 * u));
-    a[3] = nibbles_to_pair<QBF>(w1 >> (8 * u + 4));
+    a[0] = nibbles_to_pair<QBF>(w0, 2 * u);
+    a[2] = nibbles_to_pair<QBF>(w0, 2 * u + 1);
+    a[1] = nibbles_to_pair<QBF>(w1, 2 * u);
+    a[3] = nibbles_to_pair<QBF>(w1, 2 * u + 1);
   }
 }
 
@@ -250,10 +310,10 @@ __device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a
     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes k, k+1 of two rows, k = 2(i%2)
     const uint32_t x01 = prmt(w4(f.v[0], i >> 1), w4(f.v[1], i >> 1), sel);
     const uint32_t x23 = prmt(w4(f.v[2], i >> 1), w4(f.v[3], i >> 1), sel);
-    a[0] = bytes_to_f16_pair(x01, 0x4140u);
-    a[1] = bytes_to_f16_pair(x01, 0x4342u);
-    a[2] = bytes_to_f16_pair(x23, 0x4140u);
-    a[3] = bytes_to_f16_pair(x23, 0x4342u);
+    a[0] = bytes_to_f16(x01, 0x4140u);
+    a[1] = bytes_to_f16(x01, 0x4342u);
+    a[2] = bytes_to_f16(x23, 0x4140u);
+    a[3] = bytes_to_f16(x23, 0x4342u);
   } else {
     // i = 4 jj + 2 kk + m: bytes (2kk, 2kk+1) of word jj of the two rows,
     // nibbles 2m and 2m+1 of each half
@@ -262,10 +322,10 @@ __device__ __forceinline__ void v_operand(const Frag<KV>& f, int i, uint32_t (&a
     const uint32_t r0 = jj ? f.v[0].y : f.v[0].x, r1 = jj ? f.v[1].y : f.v[1].x;
     const uint32_t r2 = jj ? f.v[2].y : f.v[2].x, r3 = jj ? f.v[3].y : f.v[3].x;
     const uint32_t x01 = prmt(r0, r1, sel), x23 = prmt(r2, r3, sel);
-    a[0] = nibbles_to_pair<false>(x01 >> (8 * m));
-    a[1] = nibbles_to_pair<false>(x01 >> (8 * m + 4));
-    a[2] = nibbles_to_pair<false>(x23 >> (8 * m));
-    a[3] = nibbles_to_pair<false>(x23 >> (8 * m + 4));
+    a[0] = nibbles_to_pair<false>(x01, 2 * m);
+    a[1] = nibbles_to_pair<false>(x01, 2 * m + 1);
+    a[2] = nibbles_to_pair<false>(x23, 2 * m);
+    a[3] = nibbles_to_pair<false>(x23, 2 * m + 1);
   }
 }
 
@@ -341,9 +401,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
   using S = Stage<KV>;
   constexpr bool kQuant = KvTraits<KV>::kQuant;
   constexpr bool kPvBf = KV == kBF16;  // P.V product type: bf16 only for bf16 pools
-  constexpr float kMid = KV == kI8 ? 128.f : 8.f;  // code centre (quantized pools)
+  constexpr float kAk = CodeOffset<KV, QBF>::kK;
+  constexpr float kAv = CodeOffset<KV, QBF>::kV;
+  constexpr float kMid = CodeOffset<KV, QBF>::kMid;
+  constexpr bool kPCorr = CodeOffset<KV, QBF>::kPCorr;
   constexpr int D = S::kDepth;
-  constexpr unsigned kFull = 0xFFFFFFFFu;
 
   int32_t* cum = reinterpret_cast<int32_t*>(dsmem);  // [batch + 1]: blocks before request b
   unsigned char* stages = dsmem + align128((a.batch + 1) * sizeof(int32_t));
@@ -406,6 +468,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int n = static_cast<int>(total - x0 < P ? total - x0 : P);
   const uint32_t my_stages = static_cast<uint32_t>(__cvta_generic_to_shared(stages)) +
                              static_cast<uint32_t>(warp * D * S::kBytes);
+  LaneMap<KV> lm;
+  lm.init(lane, g, t, static_cast<uint32_t>(a.kv_heads * S::kRow));
 
   // issue side: cursor, a 32-entry window of the block table, validity bits
   Cursor ic;
@@ -414,8 +478,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
   int win_b = -1, win_j0 = 0;
   int32_t win = -1;
   uint32_t ok_mask = 0;
-  auto issue = [&](int k) {
-    if (k < n) {
+  int k_issue = 0;   // next block of the range to issue
+  int st_issue = 0;  // its stage
+  auto issue_next = [&]() {
+    if (k_issue < n) {
       if (ic.b != win_b || ic.j >= win_j0 + 32) {
         win_b = ic.b;
         win_j0 = ic.j;
@@ -424,20 +490,23 @@ __global__ void __launch_bounds__(kDecodeThreads)
       }
       const int32_t phys = __shfl_sync(kFull, win, ic.j - win_j0);
       const bool ok = phys >= 0 && phys < a.num_blocks;
-      const uint32_t bit = 1u << (k % D);
+      const uint32_t bit = 1u << st_issue;
       if (ok) {
-        issue_block<KV>(my_stages + (k % D) * S::kBytes, a, phys, ic.hgi / a.head_groups, lane);
+        issue_block<KV>(my_stages + st_issue * S::kBytes, a, lm, phys, ic.hgi / a.head_groups,
+                        lane);
         ok_mask |= bit;
       } else {
         ok_mask &= ~bit;
         if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
       }
-      if (k + 1 < n) advance(ic, cum, a.batch);
+      if (k_issue + 1 < n) advance(ic, cum, a.batch);
     }
     cp_async_commit();
+    ++k_issue;
+    st_issue = st_issue == D - 1 ? 0 : st_issue + 1;
   };
 #pragma unroll
-  for (int k = 0; k < D - 1; ++k) issue(k);
+  for (int k = 0; k < D - 1; ++k) issue_next();
 
   // ---- per-request state ---------------------------------------------------------
   int seg_b = -1, seg_hgi = -1, hq0 = 0, nh = 0, L = 0, seg_nblk = 0;
@@ -446,7 +515,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
   float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
   bool hv0 = false, hv1 = false;
   float o[8][4];
-  float m0, m1, l0, l1, z0, z1;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+  float r0 = 0.f, r1 = 0.f;  // sums of the 16-bit P' values fed to the P.V product
 
   // writes the finished state of request seg_b: the output if this warp
   // covered all of its blocks, else a partial record
@@ -458,7 +528,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
       if constexpr (kQuant) {
         z0 += __shfl_xor_sync(kFull, z0, off);
         z1 += __shfl_xor_sync(kFull, z1, off);
+        if constexpr (kPCorr) {
+          r0 += __shfl_xor_sync(kFull, r0, off);
+          r1 += __shfl_xor_sync(kFull, r1, off);
+        }
       }
+    }
+    if constexpr (kPCorr) {
+      // o = sum P'(a + c) + sum p (Z + mid S) - (a + mid) sum P'
+      z0 -= (kAv + kMid) * r0;
+      z1 -= (kAv + kMid) * r1;
     }
     const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
     const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
@@ -483,7 +562,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
         float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
 #pragma unroll
         for (int i = 0; i < 8; i += 2)
-          ov[i / 2] = make_float4(o[i][u] + z, o[i][2 + u] + z, o[i + 1][u] + z, o[i + 1][2 + u] + z);
+          ov[i / 2] =
+              make_float4(o[i][u] + z, o[i][2 + u] + z, o[i + 1][u] + z, o[i + 1][2 + u] + z);
         if (g == 0) {
           rec[kHeadDim] = m;
           rec[kHeadDim + 1] = l;
@@ -492,8 +572,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
   };
 
+  int st = 0;  // stage of block k
   for (int k = 0; k < n; ++k) {
-    issue(k + D - 1);        // refills the stage block k - 1 used
+    issue_next();            // refills the stage block k - 1 used
     cp_async_wait<D - 1>();  // this lane's copies of block k have landed
     __syncwarp();            // ... and every other lane's
 
@@ -552,36 +633,40 @@ __global__ void __launch_bounds__(kDecodeThreads)
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       m0 = m1 = -INFINITY;
-      l0 = l1 = z0 = z1 = 0.f;
+      l0 = l1 = z0 = z1 = r0 = r1 = 0.f;
     }
 
-    if ((ok_mask >> (k % D)) & 1u) {
+    if ((ok_mask >> st) & 1u) {
       Frag<KV> cur;
-      read_frag<KV>(cur, my_stages + (k % D) * S::kBytes, g, t);
-      // S^T = K Q^T
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      read_frag<KV>(cur, my_stages + st * S::kBytes, lm, g);
+      // S^T = K Q^T, even and odd k-steps in two accumulators
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < 8; kk += 2) {
         uint32_t ak[4];
         k_operand<KV, QBF>(cur, kk, ak);
-        mma16816<QBF>(sc, ak, qb[kk]);
+        mma16816<QBF>(sa, ak, qb[kk]);
+        k_operand<KV, QBF>(cur, kk + 1, ak);
+        mma16816<QBF>(sb, ak, qb[kk + 1]);
       }
+      const float sc0 = sa[0] + sb[0], sc1 = sa[1] + sb[1];
+      const float sc2 = sa[2] + sb[2], sc3 = sa[3] + sb[3];
       // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
       const int tok0 = cc.j * kBlock + g, tok1 = tok0 + 8;
       float s00, s01, s10, s11;
       if constexpr (kQuant) {
-        // q.k = S (q.(c - mid)) + (Z + mid S) sum(q)
-        const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) + kMid * S0;
-        const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) + kMid * S1;
-        s00 = (S0 * sc[0] + Z0 * qs0) * a.sm_scale_log2;
-        s01 = (S0 * sc[1] + Z0 * qs1) * a.sm_scale_log2;
-        s10 = (S1 * sc[2] + Z1 * qs0) * a.sm_scale_log2;
-        s11 = (S1 * sc[3] + Z1 * qs1) * a.sm_scale_log2;
+        // q.k = S (q.(a + c)) + (Z - a S) sum(q)
+        const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) - kAk * S0;
+        const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) - kAk * S1;
+        s00 = (S0 * sc0 + Z0 * qs0) * a.sm_scale_log2;
+        s01 = (S0 * sc1 + Z0 * qs1) * a.sm_scale_log2;
+        s10 = (S1 * sc2 + Z1 * qs0) * a.sm_scale_log2;
+        s11 = (S1 * sc3 + Z1 * qs1) * a.sm_scale_log2;
       } else {
-        s00 = sc[0] * a.sm_scale_log2;
-        s01 = sc[1] * a.sm_scale_log2;
-        s10 = sc[2] * a.sm_scale_log2;
-        s11 = sc[3] * a.sm_scale_log2;
+        s00 = sc0 * a.sm_scale_log2;
+        s01 = sc1 * a.sm_scale_log2;
+        s10 = sc2 * a.sm_scale_log2;
+        s11 = sc3 * a.sm_scale_log2;
       }
       if (tok0 >= L) s00 = s01 = -INFINITY;
       if (tok1 >= L) s10 = s11 = -INFINITY;
@@ -595,30 +680,46 @@ __global__ void __launch_bounds__(kDecodeThreads)
         bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
       }
       const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
-      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+      const float p00 = ex2(s00 - mn0), p10 = ex2(s10 - mn0);
+      const float p01 = ex2(s01 - mn1), p11 = ex2(s11 - mn1);
+      // rescale the running state only when some head's maximum moved
+      if (__any_sync(kFull, mn0 != m0 || mn1 != m1)) {
+        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+        l0 *= al0;
+        l1 *= al1;
+        z0 *= al0;
+        z1 *= al1;
+        r0 *= al0;
+        r1 *= al1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] *= al0; o[i][2] *= al0;
+          o[i][1] *= al1; o[i][3] *= al1;
+        }
+      }
       m0 = mn0;
       m1 = mn1;
-      l0 = l0 * al0 + (p00 + p10);
-      l1 = l1 * al1 + (p01 + p11);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
       float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
       if constexpr (kQuant) {
-        // sum_t p_t v_t = sum_t (p_t S_t)(c_t - mid) + sum_t p_t (Z_t + mid S_t)
+        // sum_t p_t v_t = sum_t P'_t (a + c_t) + sum_t p_t (Z_t + mid S_t)
+        //                 - (a + mid) sum_t P'_t,  with P'_t = p_t S_t in fp16:
+        // subtracting the rounded P' actually used leaves their rounding
+        // error multiplied by c - mid only, as if the codes were centred
         const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
         const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
-        z0 = z0 * al0 + (p00 * Z0 + p10 * Z1);
-        z1 = z1 * al1 + (p01 * Z0 + p11 * Z1);
+        z0 += p00 * Z0 + p10 * Z1;
+        z1 += p01 * Z0 + p11 * Z1;
         q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i][0] *= al0; o[i][2] *= al0;
-        o[i][1] *= al1; o[i][3] *= al1;
       }
       // P'^T as the B operand: transpose the (token x head) fragments
       uint32_t bp[2], bp_lo[2];
       const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
+      if constexpr (kPCorr) {
+        r0 += lo_to_float<false>(h0) + lo_to_float<false>(h1);
+        r1 += hi_to_float<false>(h0) + hi_to_float<false>(h1);
+      }
       bp[0] = movmatrix_trans(h0);
       bp[1] = movmatrix_trans(h1);
       if constexpr (kPvBf) {
@@ -639,6 +740,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       }
     }
     __syncwarp();  // all lanes are done with this stage before it is refilled
+    st = st == D - 1 ? 0 : st + 1;
     if (k + 1 < n) advance(cc, cum, a.batch);
   }
   cp_async_wait<0>();
@@ -669,21 +771,34 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
     const int slot = (w == w_first && seg_start != w * P) ? 1 : 0;
     return a.part + ((w * 2 + slot) * a.hpg + hh) * kPartStride;
   };
+  const int64_t npieces = w_last - w_first + 1;
+  // lanes read the pieces' maxima in parallel
   float M = -INFINITY;
-  for (int64_t w = w_first + lane; w <= w_last; w += 32) M = fmaxf(M, rec_of(w)[kHeadDim]);
+  for (int64_t i = lane; i < npieces; i += 32) M = fmaxf(M, rec_of(w_first + i)[kHeadDim]);
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
   if (M != -INFINITY) {
-    for (int64_t w = w_first; w <= w_last; ++w) {
-      const float* rec = rec_of(w);
-      const float mw = rec[kHeadDim];
-      const float e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-      lsum += e * rec[kHeadDim + 1];
-      const float4 x = reinterpret_cast<const float4*>(rec)[lane];
-      acc.x += e * x.x; acc.y += e * x.y; acc.z += e * x.z; acc.w += e * x.w;
+    for (int64_t base = 0; base < npieces; base += 32) {
+      float e = 0.f, lw = 0.f;
+      if (base + lane < npieces) {
+        const float* rec = rec_of(w_first + base + lane);
+        const float mw = rec[kHeadDim];
+        e = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        lw = rec[kHeadDim + 1];
+      }
+      lsum += e * lw;
+      const int cnt = static_cast<int>(npieces - base < 32 ? npieces - base : 32);
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        const float ei = __shfl_sync(kFull, e, i);
+        const float4 x = reinterpret_cast<const float4*>(rec_of(w_first + base + i))[lane];
+        acc.x += ei * x.x; acc.y += ei * x.y; acc.z += ei * x.z; acc.w += ei * x.w;
+      }
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const int64_t base = bh * kHeadDim + 4 * lane;
@@ -731,7 +846,6 @@ int occupancy_t(int batch) {
 }
 
 }  // namespace
-
 
 cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid,
                           cudaStream_t s) {

@@ -76,42 +76,42 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   return r;
 }
 
+// Codes enter the tensor cores as exact 16-bit floats a + c, made by writing
+// the code into the mantissa of a constant whose exponent makes one mantissa
+// step worth 1; the caller removes a outside the products (with the zero).
+//   INT4 as fp16: 16 + c   (0x4C00 with the code in mantissa bits 6..9)
+//   INT4 as bf16: 128 + c  (0x4300 with the code in mantissa bits 0..3)
+//   INT8 as fp16: c - 128  (0x6400 with the code in mantissa bits 0..7 is
+//                           1024 + c; one packed subtract centres it)
+//   INT8 as bf16: c - 128  (through fp32)
+// INT8 codes are centred exactly: with a large offset the P.V accumulator
+// would carry a constant that grows over a long context, and its fp32
+// accumulation error with it.
+
+// Nibble s (0..3) of each 16-bit half of w as a pair a + c. s is a constant
+// after unrolling, so the shift folds into one instruction or none.
 template <bool BF>
-__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
-  uint32_t r;
+__device__ __forceinline__ uint32_t nibbles_to_pair(uint32_t w, int s) {
   if constexpr (BF) {
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return and_or(w >> (4 * s), 0x000F000Fu, 0x43004300u);
   } else {
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    const uint32_t x = s == 0 ? (w << 6) : s == 1 ? (w << 2) : s == 2 ? (w >> 2) : (w >> 6);
+    return and_or(x, 0x03C003C0u, 0x4C004C00u);
   }
+}
+
+// Two bytes of w (selected by sel, producing [b_lo, 0x64, b_hi, 0x64], the
+// fp16 pair 1024 + c) as the exact fp16 pair c - 128: one packed subtract of
+// 1152 (0x6480).
+__device__ __forceinline__ uint32_t bytes_to_f16(uint32_t w, uint32_t sel) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(prmt(w, 0x64646464u, sel)), "r"(0x64806480u));
   return r;
 }
 
-// Codes enter the tensor cores centred: c - 8 (INT4) or c - 128 (INT8), so
-// that the dequantized value is S (c - mid) + (Z + mid S) and no large terms
-// cancel when the per-token zero is added back outside the product. Every
-// centred code is an exact fp16 / bf16 integer.
-
-// Two 4-bit codes (bits [4s, 4s+4) of each 16-bit half of w) as a pair of
-// exact 16-bit floats c - 8. Setting the exponent field over the code gives
-// 1024 + c (fp16, 0x6400) or 128 + c (bf16, 0x4300); one packed subtract of
-// 1032 (0x6408) or 136 (0x4308) leaves c - 8, exactly.
-template <bool BF>
-__device__ __forceinline__ uint32_t nibbles_to_pair(uint32_t w_shifted) {
-  constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
-  constexpr uint32_t kMagicMid = BF ? 0x43084308u : 0x64086408u;
-  return sub2<BF>(and_or(w_shifted, 0x000F000Fu, kMagic), kMagicMid);
-}
-
-// Two bytes of w (selected by sel, producing [b_lo, 0x64, b_hi, 0x64]) as an
-// exact fp16 pair c - 128: 1024 + c, minus 1152 (0x6480).
-__device__ __forceinline__ uint32_t bytes_to_f16_pair(uint32_t w, uint32_t sel) {
-  return sub2<false>(prmt(w, 0x64646464u, sel), 0x64806480u);
-}
-
-// Two bytes of w (byte indices i0 low, i1 high) as an exact bf16 pair c - 128:
-// the bytes go through fp32 (2^23 + c, minus 2^23 + 128) and a paired
-// round-to-nearest conversion, exact since |c - 128| <= 128.
+// Two bytes of w (byte indices i0 low, i1 high) as the exact bf16 pair
+// c - 128: the bytes go through fp32 (2^23 + c, minus 2^23 + 128) and a
+// paired round-to-nearest conversion, exact since |c - 128| <= 128.
 __device__ __forceinline__ uint32_t bytes_to_bf16_pair(uint32_t w, int i0, int i1) {
   const float f0 = __uint_as_float(0x4B000000u | ((w >> (8 * i0)) & 0xFFu)) - 8388736.0f;
   const float f1 = __uint_as_float(0x4B000000u | ((w >> (8 * i1)) & 0xFFu)) - 8388736.0f;

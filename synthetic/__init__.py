@@ -450,8 +450,11 @@ def by_name(name: str, **kw) -> Workload:
 
 def custom(name: str, kv_dtype: str, lens, q_heads: int, kv_heads: int, seed: int = 7,
            in_dtype: str = "f16", q_dtype: Optional[str] = None, value_scale: float = 1.0,
-           extra_blocks: int = 5) -> Workload:
-    """Small ad-hoc workload: random distinct blocks for each request."""
+           extra_blocks: int = 5, outliers: bool = False) -> Workload:
+    """Small ad-hoc workload: random distinct blocks for each request.
+
+    outliers: scale 1 % of the K and of the V channels by 8, as in cfg3.
+    """
     lens = np.asarray(lens, dtype=np.int32)
     nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
     total = int(nblk.sum()) + extra_blocks
@@ -461,5 +464,9 @@ def custom(name: str, kv_dtype: str, lens, q_heads: int, kv_heads: int, seed: in
         q_dtype = kv_dtype if kv_dtype in ("f16", "bf16") else in_dtype
     if kv_dtype in ("f16", "bf16"):
         in_dtype = kv_dtype
+    kw = {}
+    if outliers:
+        nc = kv_heads * HEAD_DIM
+        kw = dict(k_chan_scale=_outliers(seed, S_OUT_K, nc), v_chan_scale=_outliers(seed, S_OUT_V, nc))
     return _finish(name, kv_dtype, in_dtype, q_dtype, q_heads, kv_heads, seed, lens, total, bt,
-                   value_scale=value_scale)
+                   value_scale=value_scale, **kw)

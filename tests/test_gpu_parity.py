@@ -82,6 +82,21 @@ def test_dtypes_and_groups(gpu, kv_dtype, in_dtype, heads):
     assert_close(out_to_f64(out), oout)
 
 
+@pytest.mark.parametrize("kv_dtype,q_dtype", [("int8", "f16"), ("int4", "f16"),
+                                               ("int4", "bf16")])
+def test_long_context_with_outlier_channels(gpu, kv_dtype, q_dtype):
+    """Long contexts and x8 outlier channels stress the accumulation of the
+    code offsets and the 16-bit rounding of p * scale."""
+    wl = synthetic.custom("long_outliers", kv_dtype, [4096, 3001, 17, 2048], 8, 2, seed=55,
+                          q_dtype=q_dtype, outliers=True)
+    pool = fill_pool(wl)
+    out, _, dev_err = run_step(wl, pool)
+    assert gpu.kvq_check_error(dev_err) == 0
+    opool, oout = oracle.run_workload(wl)
+    _compare_pools(pool, opool)
+    assert_close(out_to_f64(out), oout)
+
+
 @pytest.mark.parametrize("kv_dtype", ["int8", "int4"])
 def test_bf16_queries_over_quantized_pool(gpu, kv_dtype):
     wl = synthetic.custom("bfq", kv_dtype, [40, 300, 77], 8, 2, seed=51, in_dtype="f16",
