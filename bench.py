@@ -51,6 +51,7 @@ def parse_args():
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
     p.add_argument("--json-out", default="")
     return p.parse_args()
 
@@ -194,6 +195,26 @@ def traffic_from_profile(workload: str):
     return float(m_b.group(1)), sha
 
 
+def copy_bandwidth_gbs(dev, n_bytes: int = 1 << 31, reps: int = 10) -> float:
+    """This GPU's device-to-device copy bandwidth right now (read + write bytes),
+    best of `reps` copies of a 2 GiB buffer (larger than L2)."""
+    import torch
+    a = torch.empty(n_bytes // 2, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    return 2 * n_bytes / (best / 1e3) / 1e9
+
+
 # ---- our arm ---------------------------------------------------------------------
 
 def run_ours(args, rank: int, world: int, dist):
@@ -236,26 +257,45 @@ def run_ours(args, rank: int, world: int, dist):
                                       args.num_splits)
     stream = torch.cuda.current_stream(dev)
 
-    def one_step(inp, ev0=None, ev1=None):
+    def pre_step(inp):
         kvq.kvq_block_tables_from_req_to_token(r2t, inp["req_pool_indices"], inp["seq_lens"],
                                                step.block_tables, step.dev_err)
         kvq.kv_store_quant(pool, inp["k_new"], inp["v_new"], inp["slot_mapping"], step.dev_err)
-        if ev0 is not None:
-            ev0.record(stream)
+
+    def dec_step(inp):
         kvq.paged_decode_attn(pool, inp["q"], step.out, step.block_tables, inp["seq_lens"],
                               wl.max_seq_len, wl.sm_scale, args.num_splits, step.workspace,
                               step.dev_err)
-        if ev1 is not None:
-            ev1.record(stream)
 
     launches_per_step = 4  # tables, store, decode, combine
 
-    for _ in range(args.warmup):
-        one_step(d_in)
+    for _ in range(max(args.warmup, 1)):
+        pre_step(d_in)
+        dec_step(d_in)
     torch.cuda.synchronize()
     bits = kvq.kvq_check_error(step.dev_err)
     if bits:
         raise RuntimeError(f"device error word {bits:#x} after warm-up")
+    use_graph = not args.no_graph
+    if use_graph:
+        # the step as two CUDA graphs (a decode step is replayed as a graph in
+        # serving runtimes); the decode call is timed between the two replays
+        g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_pre):
+            pre_step(d_in)
+        with torch.cuda.graph(g_dec):
+            dec_step(d_in)
+        run_pre, run_dec = g_pre.replay, g_dec.replay
+        for _ in range(args.warmup):
+            run_pre()
+            run_dec()
+        torch.cuda.synchronize()
+    else:
+        def run_pre():
+            pre_step(d_in)
+
+        def run_dec():
+            dec_step(d_in)
 
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     sampler = ClockSampler(uuid)
@@ -270,7 +310,10 @@ def run_ours(args, rank: int, world: int, dist):
     sampler.start()
     t0.record(stream)
     for i in range(K):
-        one_step(d_in, ev_d0[i], ev_d1[i])
+        run_pre()
+        ev_d0[i].record(stream)
+        run_dec()
+        ev_d1[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -297,12 +340,20 @@ def run_ours(args, rank: int, world: int, dist):
         h2d = sum(t.numel() * t.element_size() for t in pinned.values())
         d2h = out_host.numel() * out_host.element_size()
 
-        def e2e_step():
+        def e2e_body():
             for key, t in pinned.items():
                 e_raw[key].copy_(t, non_blocking=True)
-            one_step(e_in)
+            pre_step(e_in)
+            dec_step(e_in)
             out_host.copy_(step.out, non_blocking=True)
 
+        if use_graph:
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e):
+                e2e_body()
+            e2e_step = g_e2e.replay
+        else:
+            e2e_step = e2e_body
         for _ in range(max(3, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
@@ -331,6 +382,7 @@ def run_ours(args, rank: int, world: int, dist):
         raise RuntimeError(f"device error word {bits:#x} after the timed steps")
 
     # ---- roofline of the dominant call (decode + combine) ---------------------------
+    box_copy = copy_bandwidth_gbs(dev)
     alg = decode_algorithmic_bytes(wl)
     uniq = unique_decode_bytes(wl)
     mean_decode_ms = float(np.mean(decode_ms))
@@ -349,6 +401,8 @@ def run_ours(args, rank: int, world: int, dist):
         "decode_ms_max": round(float(np.max(decode_ms)), 5),
         "unique_frac": round(uniq / (mean_decode_ms / 1e3) / 1e9 / peak, 4),
         "kernel_source_sha": sha,
+        "copy_gbs_this_gpu": round(box_copy, 1),
+        "frac_of_this_gpu_copy": round(achieved / box_copy, 4),
     }
 
     result = {
@@ -358,6 +412,7 @@ def run_ours(args, rank: int, world: int, dist):
         "dtype": {"int8": "u8", "int4": "u4", "f16": "f16", "bf16": "bf16"}[wl.kv_dtype],
         "data": "synthetic (seeded counter-based generator; no dataset)",
         "config": {**workload_desc(wl), "l2": "no flush: the pool is larger than L2",
+                   "cuda_graph": use_graph,
                    "plan": plan, "parallelism": f"replicas x{world} (no data-path collective)"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches_per_step * K,

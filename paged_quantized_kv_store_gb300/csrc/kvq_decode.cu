@@ -89,7 +89,7 @@ struct Frag<kI4> {
 // and the middle code (2^(b-1)).
 template <int KV, bool QBF>
 struct CodeOffset {
-  static constexpr float kK = KV == kI8 ? -128.f : (QBF ? 128.f : 16.f);
+  static constexpr float kK = KV == kI8 ? (QBF ? -128.f : 1024.f) : (QBF ? 128.f : 16.f);
   static constexpr float kV = KV == kI8 ? -128.f : 16.f;
   static constexpr float kMid = KV == kI8 ? 128.f : 8.f;
   // the rounded-P' correction is needed only when the V codes are not centred
@@ -278,10 +278,10 @@ __device__ __forceinline__ void k_operand(const Frag<KV>& f, int kk, uint32_t (&
       a[1] = bytes_to_bf16_pair(w1, 0, 1);
       a[3] = bytes_to_bf16_pair(w1, 2, 3);
     } else {
-      a[0] = bytes_to_f16(w0, 0x4140u);
-      a[2] = bytes_to_f16(w0, 0x4342u);
-      a[1] = bytes_to_f16(w1, 0x4140u);
-      a[3] = bytes_to_f16(w1, 0x4342u);
+      a[0] = bytes_to_f16_offset(w0, 0x4140u);
+      a[2] = bytes_to_f16_offset(w0, 0x4342u);
+      a[1] = bytes_to_f16_offset(w1, 0x4140u);
+      a[3] = bytes_to_f16_offset(w1, 0x4342u);
     }
   } else {
     // kk = 2 j + u: pairs of dims (8j+2u, 8j+2u+4) and (8j+2u+1, 8j+2u+5)
@@ -672,18 +672,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
       if (tok1 >= L) s10 = s11 = -INFINITY;
       if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
       if (!hv1) s01 = s11 = 0.f;
-      // block max over the 16 tokens (lanes with equal t)
+      // the running maximum moves only when some lane holds a larger score:
+      // then reduce the block maximum over the 16 tokens (lanes with equal t)
+      // and rescale the running state
       float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+      float mn0 = m0, mn1 = m1;
+      if (__any_sync(kFull, bm0 > m0 || bm1 > m1)) {
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-      }
-      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      const float p00 = ex2(s00 - mn0), p10 = ex2(s10 - mn0);
-      const float p01 = ex2(s01 - mn1), p11 = ex2(s11 - mn1);
-      // rescale the running state only when some head's maximum moved
-      if (__any_sync(kFull, mn0 != m0 || mn1 != m1)) {
+        for (int off = 4; off < 32; off <<= 1) {
+          bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+          bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+        }
+        mn0 = fmaxf(m0, bm0);
+        mn1 = fmaxf(m1, bm1);
         const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
         l0 *= al0;
         l1 *= al1;
@@ -699,6 +700,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
       }
       m0 = mn0;
       m1 = mn1;
+      const float p00 = ex2(s00 - mn0), p10 = ex2(s10 - mn0);
+      const float p01 = ex2(s01 - mn1), p11 = ex2(s11 - mn1);
       l0 += p00 + p10;
       l1 += p01 + p11;
       float q00 = p00, q01 = p01, q10 = p10, q11 = p11;

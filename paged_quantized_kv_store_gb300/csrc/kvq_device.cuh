@@ -81,12 +81,13 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // step worth 1; the caller removes a outside the products (with the zero).
 //   INT4 as fp16: 16 + c   (0x4C00 with the code in mantissa bits 6..9)
 //   INT4 as bf16: 128 + c  (0x4300 with the code in mantissa bits 0..3)
-//   INT8 as fp16: c - 128  (0x6400 with the code in mantissa bits 0..7 is
-//                           1024 + c; one packed subtract centres it)
+//   INT8 as fp16: 1024 + c (0x6400 with the code in mantissa bits 0..7), and
+//                 c - 128 after one packed subtract
 //   INT8 as bf16: c - 128  (through fp32)
-// INT8 codes are centred exactly: with a large offset the P.V accumulator
-// would carry a constant that grows over a long context, and its fp32
-// accumulation error with it.
+// The P.V product takes INT8 codes centred exactly: with a large offset its
+// accumulator would carry a constant that grows over a long context, and its
+// fp32 accumulation error with it. The Q.K product starts afresh for every
+// block, so the offset costs nothing there.
 
 // Nibble s (0..3) of each 16-bit half of w as a pair a + c. s is a constant
 // after unrolling, so the shift folds into one instruction or none.
@@ -98,6 +99,12 @@ __device__ __forceinline__ uint32_t nibbles_to_pair(uint32_t w, int s) {
     const uint32_t x = s == 0 ? (w << 6) : s == 1 ? (w << 2) : s == 2 ? (w >> 2) : (w >> 6);
     return and_or(x, 0x03C003C0u, 0x4C004C00u);
   }
+}
+
+// Two bytes of w (selected by sel, producing [b_lo, 0x64, b_hi, 0x64]) as the
+// fp16 pair 1024 + c.
+__device__ __forceinline__ uint32_t bytes_to_f16_offset(uint32_t w, uint32_t sel) {
+  return prmt(w, 0x64646464u, sel);
 }
 
 // Two bytes of w (selected by sel, producing [b_lo, 0x64, b_hi, 0x64], the
