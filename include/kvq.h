@@ -69,6 +69,7 @@ typedef enum kvq_dtype {
 #define KVQ_DEV_ERR_NOT_BLOCKED 8u /* block tables: row not block-contiguous */
 #define KVQ_DEV_ERR_SLOT 16u       /* store: slot >= num_blocks * 16 (token skipped) */
 #define KVQ_DEV_ERR_BLOCK_ID 32u   /* decode: block id outside [0, num_blocks) (block skipped) */
+#define KVQ_DEV_ERR_TIMEOUT 64u    /* decode: a tile copy did not complete within 2 s (warp stopped) */
 
 /*
  * One layer's KV pool (KVPool of "pymllm Runtime Design"; shape from LMDeploy

@@ -30,6 +30,7 @@ HEAD_DIM = 128
 
 DEV_ERR_BITS = {
     "req_slot": 1, "length": 2, "kv_index": 4, "not_blocked": 8, "slot": 16, "block_id": 32,
+    "timeout": 64,
 }
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",

@@ -1,11 +1,14 @@
 // C ABI of libkvq: argument validation, launch planning and dispatch.
 // The declarations, with the passages of the source pages each entry point
 // follows, are in include/kvq.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "kvq.h"
 #include "kvq_internal.h"
@@ -43,6 +46,49 @@ int current_sm_count() {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
+// link-time dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// TMA view of a quantized K or V pool: [num_blocks][16][kv_heads][row bytes],
+// one box = the 16 rows of one (block, head) tile, swizzled to match the
+// decode kernel's reads (128-byte pattern for 128-byte rows, 64-byte pattern
+// for 64-byte rows). No L2 promotion: a wider fetch would pull in the
+// neighbouring head's row.
+bool encode_pool_map(CUtensorMap* map, void* base, int64_t num_blocks, int kv_heads,
+                     int row_bytes) {
+  std::memset(map, 0, sizeof(*map));
+  if (num_blocks <= 0) return true;  // no valid block id: no copy is ever issued
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes),
+                              static_cast<cuuint64_t>(kv_heads), 16,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(kv_heads) * row_bytes,
+                                 static_cast<cuuint64_t>(16) * kv_heads * row_bytes};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(row_bytes), 1, 16, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -172,6 +218,14 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
   kvq::DecodeArgs a;
+  if (pool->kv_dtype == KVQ_INT8) {  // the INT8 kernel stages its tiles by TMA
+    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
+        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
+      return KVQ_ERR_CUDA;
+  } else {
+    std::memset(&a.k_map, 0, sizeof(a.k_map));
+    std::memset(&a.v_map, 0, sizeof(a.v_map));
+  }
   a.k = static_cast<const uint8_t*>(pool->k);
   a.v = static_cast<const uint8_t*>(pool->v);
   a.k_sz = static_cast<const uint32_t*>(pool->k_sz);

@@ -98,25 +98,44 @@ struct CodeOffset {
 
 // ---- shared-memory staging -------------------------------------------------------
 
-// One pipeline stage holds one 16-token block of one kv head: the K tile and
-// the V tile (16 rows of kRow bytes each; the 16-byte chunks of row r are
-// XOR-swizzled with r so that the fragment reads below fall on distinct
-// banks) and, for quantized pools, the 16 (scale, zero) pairs of K and of V.
+// Every warp owns kDepth stages; stage st holds one 16-token block of one kv
+// head: the K tile and the V tile (16 rows of kRow bytes) and, for quantized
+// pools, the 16 (scale, zero) pairs of K and of V. The 16-byte chunks of a
+// tile row are XOR-swizzled so that the fragment reads below fall on distinct
+// banks. INT8 tiles arrive by TMA (one 4-D tensor copy per tile with the
+// hardware's 128-byte swizzle, completion on a per-stage mbarrier); the other
+// kinds by per-lane 16-byte cp.async with the same pattern (64-byte pattern
+// for 64-byte rows) applied by hand.
+//   per warp: [K tiles][V tiles][scale/zero][mbarriers], 1024-byte aligned
 template <int KV>
 struct Stage {
   static constexpr int kRow = KvTraits<KV>::kRowBytes;
   static constexpr int kChunks = kRow / 16;                // 16-byte chunks per row
-  static constexpr int kSwz = (kChunks < 8 ? kChunks : 8) - 1;
   static constexpr int kTile = kBlock * kRow;
-  static constexpr int kBytes = 2 * kTile + (KvTraits<KV>::kQuant ? 128 : 0);
-  static constexpr int kCopies = kBlock * kChunks / 32;    // chunks per lane per tile
+  // TMA for INT8 tiles (2 KB boxes); INT4 tiles (1 KB) stream faster through
+  // per-lane cp.async (measured on the same GPU: 57 vs 64 us for the INT4
+  // GQA-4 workload)
+  static constexpr bool kTma = KV == kI8;
+  static constexpr int kCopies = kBlock * kChunks / 32;    // cp.async chunks per lane per tile
   static constexpr int kKReads = kChunks / 4;              // 16-byte K reads per row
   static constexpr int kVReads = kChunks >= 8 ? kChunks / 8 : 1;  // V reads per row
-  // blocks in flight per warp: about 16 KB of KV per warp
-  static constexpr int kDepth = KV == kI4 ? 6 : (KV == kI8 ? 4 : 2);
+  // blocks in flight per warp (about 8-16 KB of KV per warp)
+  static constexpr int kDepth = KV == kI4 ? 4 : (KV == kI8 ? 4 : 2);
+  static constexpr int kVOff = kDepth * kTile;
+  static constexpr int kSzOff = 2 * kDepth * kTile;
+  static constexpr int kBarOff = kSzOff + kDepth * 128;
+  static constexpr int kWarpBytes = (kBarOff + kDepth * 8 + 1023) / 1024 * 1024;
+  static constexpr int kTxBytes = kTma ? 2 * kTile + 128 : 0;  // bytes one TMA stage receives
+  // chunk c of row r sits at chunk c ^ swz_bits(r): the 128-byte pattern
+  // (r mod 8) for 128- and 256-byte rows, the 64-byte pattern ((r / 2) mod 4)
+  // for 64-byte rows
+  __host__ __device__ static constexpr int swz_bits(int r) {
+    return kRow == 64 ? ((r >> 1) & 3) : (r & 7);
+  }
+  __host__ __device__ static constexpr int at(int r, int c) {
+    return r * kRow + (c ^ swz_bits(r)) * 16;
+  }
 };
-
-__host__ __device__ constexpr int swz(int r, int c, int mask) { return c ^ (r & mask); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -146,6 +165,56 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return r;
 }
 
+// ---- mbarrier / TMA -------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arm(uint32_t bar, uint32_t tx_bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx_bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of parity `parity` of the barrier; gives up after 2 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_tile_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 2^x by the hardware approximation (relative error about 2^-22; tiny
 // results flush to zero).
 __device__ __forceinline__ float ex2(float x) {
@@ -154,101 +223,120 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Per-lane constants of the copies into a stage and of the fragment reads
-// from it; only the stage base and the block's global address change.
+// Per-lane constants of the fragment reads from a stage (and of the cp.async
+// copies into it); only the stage base and the block's address change.
 template <int KV>
 struct LaneMap {
   using S = Stage<KV>;
-  uint32_t src[S::kCopies];            // byte offset within the tile's global rows
-  uint32_t dst[S::kCopies];            // byte offset within the stage (V adds kTile)
-  uint32_t kr[2][S::kKReads];          // K fragment reads
-  uint32_t vr[4][S::kVReads];          // V fragment reads
+  uint32_t src[S::kTma ? 1 : S::kCopies];  // byte offset within the tile's global rows
+  uint32_t dst[S::kTma ? 1 : S::kCopies];  // byte offset within the tile
+  uint32_t kr[2][S::kKReads];              // K fragment reads (offset in the K tile)
+  uint32_t vr[4][S::kVReads];              // V fragment reads (offset in the V tile)
   __device__ __forceinline__ void init(int lane, int g, int t, uint32_t tok_stride) {
+    if constexpr (!S::kTma) {
 #pragma unroll
-    for (int i = 0; i < S::kCopies; ++i) {
-      const int n = lane + 32 * i;
-      const int r = n / S::kChunks, c = n % S::kChunks;
-      src[i] = r * tok_stride + c * 16;
-      dst[i] = r * S::kRow + swz(r, c, S::kSwz) * 16;
+      for (int i = 0; i < S::kCopies; ++i) {
+        const int n = lane + 32 * i;
+        const int r = n / S::kChunks, c = n % S::kChunks;
+        src[i] = r * tok_stride + c * 16;
+        dst[i] = S::at(r, c);
+      }
     }
 #pragma unroll
     for (int i = 0; i < S::kKReads; ++i) {
       const int c = S::kKReads * t + i;
-      kr[0][i] = g * S::kRow + swz(g, c, S::kSwz) * 16;
-      kr[1][i] = (g + 8) * S::kRow + swz(g + 8, c, S::kSwz) * 16;
+      kr[0][i] = S::at(g, c);
+      kr[1][i] = S::at(g + 8, c);
     }
     const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const uint32_t row = S::kTile + rows[r] * S::kRow;
       if constexpr (KV == kI4) {
-        vr[r][0] = row + swz(rows[r], g >> 1, S::kSwz) * 16 + 8 * (g & 1);
+        vr[r][0] = S::at(rows[r], g >> 1) + 8 * (g & 1);
       } else {
 #pragma unroll
-        for (int i = 0; i < S::kVReads; ++i)
-          vr[r][i] = row + swz(rows[r], S::kVReads * g + i, S::kSwz) * 16;
+        for (int i = 0; i < S::kVReads; ++i) vr[r][i] = S::at(rows[r], S::kVReads * g + i);
       }
     }
   }
 };
 
-// The warp copies block `phys` of kv head h into the stage at shared address
-// st (asynchronous; the caller commits the group).
+// The warp starts the copy of block `phys` of kv head h into stage st of its
+// region `wr` (shared address). TMA path: lane 0 arms the stage's barrier and
+// issues two tile copies and two 64-byte scale/zero copies. cp.async path:
+// every lane copies its chunks; the caller commits the group.
 template <int KV>
-__device__ __forceinline__ void issue_block(uint32_t st, const DecodeArgs& a,
+__device__ __forceinline__ void issue_block(uint32_t wr, int st, const DecodeArgs& a,
                                             const LaneMap<KV>& lm, int64_t phys, int h,
                                             int lane) {
   using S = Stage<KV>;
-  const int64_t base = (phys * kBlock * a.kv_heads + h) * S::kRow;
-  const uint8_t* kb = a.k + base;
-  const uint8_t* vb = a.v + base;
+  const uint32_t kdst = wr + st * S::kTile, vdst = wr + S::kVOff + st * S::kTile;
+  if constexpr (S::kTma) {
+    if (lane == 0) {
+      const uint32_t bar = wr + S::kBarOff + 8 * st;
+      const uint32_t sz = wr + S::kSzOff + 128 * st;
+      const int64_t szi = (phys * a.kv_heads + h) * kBlock;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // after the reads of the last use
+      mbar_arm(bar, S::kTxBytes);
+      tma_tile_4d(kdst, &a.k_map, 0, h, 0, static_cast<int>(phys), bar);
+      tma_tile_4d(vdst, &a.v_map, 0, h, 0, static_cast<int>(phys), bar);
+      bulk_copy(sz, a.k_sz + szi, 64, bar);
+      bulk_copy(sz + 64, a.v_sz + szi, 64, bar);
+    }
+  } else {
+    const int64_t base = (phys * kBlock * a.kv_heads + h) * S::kRow;
+    const uint8_t* kb = a.k + base;
+    const uint8_t* vb = a.v + base;
 #pragma unroll
-  for (int i = 0; i < S::kCopies; ++i) {
-    cp_async16(st + lm.dst[i], kb + lm.src[i]);
-    cp_async16(st + S::kTile + lm.dst[i], vb + lm.src[i]);
-  }
-  if constexpr (KvTraits<KV>::kQuant) {
-    if (lane < 8) {
-      const uint32_t* src =
-          (lane < 4 ? a.k_sz : a.v_sz) + (phys * a.kv_heads + h) * kBlock + 4 * (lane & 3);
-      cp_async16(st + 2 * S::kTile + 16 * lane, src);
+    for (int i = 0; i < S::kCopies; ++i) {
+      cp_async16(kdst + lm.dst[i], kb + lm.src[i]);
+      cp_async16(vdst + lm.dst[i], vb + lm.src[i]);
+    }
+    if constexpr (KvTraits<KV>::kQuant) {
+      // lanes 0-3 copy the 64 bytes of K scale/zero pairs, lanes 4-7 those of V
+      if (lane < 8) {
+        const uint32_t* src =
+            (lane < 4 ? a.k_sz : a.v_sz) + (phys * a.kv_heads + h) * kBlock + 4 * (lane & 3);
+        cp_async16(wr + S::kSzOff + 128 * st + 16 * lane, src);
+      }
     }
   }
 }
 
-// This lane's fragment bytes of the staged block and the scale/zero words of
-// tokens g and g+8.
+// This lane's fragment bytes of the block in stage st, and the scale/zero
+// words of tokens g and g+8.
 template <int KV>
-__device__ __forceinline__ void read_frag(Frag<KV>& f, uint32_t st, const LaneMap<KV>& lm,
-                                          int g) {
+__device__ __forceinline__ void read_frag(Frag<KV>& f, uint32_t wr, int st,
+                                          const LaneMap<KV>& lm, int g) {
   using S = Stage<KV>;
+  const uint32_t kt = wr + st * S::kTile, vt = wr + S::kVOff + st * S::kTile;
   if constexpr (KV == kF16 || KV == kBF16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      f.k[0][i] = lds128(st + lm.kr[0][i]);
-      f.k[1][i] = lds128(st + lm.kr[1][i]);
+      f.k[0][i] = lds128(kt + lm.kr[0][i]);
+      f.k[1][i] = lds128(kt + lm.kr[1][i]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      f.v[r][0] = lds128(st + lm.vr[r][0]);
-      f.v[r][1] = lds128(st + lm.vr[r][1]);
+      f.v[r][0] = lds128(vt + lm.vr[r][0]);
+      f.v[r][1] = lds128(vt + lm.vr[r][1]);
     }
   } else if constexpr (KV == kI8) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      f.k[0][i] = lds128(st + lm.kr[0][i]);
-      f.k[1][i] = lds128(st + lm.kr[1][i]);
+      f.k[0][i] = lds128(kt + lm.kr[0][i]);
+      f.k[1][i] = lds128(kt + lm.kr[1][i]);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = lds128(st + lm.vr[r][0]);
+    for (int r = 0; r < 4; ++r) f.v[r] = lds128(vt + lm.vr[r][0]);
   } else {
-    f.k[0] = lds128(st + lm.kr[0][0]);
-    f.k[1] = lds128(st + lm.kr[1][0]);
+    f.k[0] = lds128(kt + lm.kr[0][0]);
+    f.k[1] = lds128(kt + lm.kr[1][0]);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) f.v[r] = lds64(st + lm.vr[r][0]);
+    for (int r = 0; r < 4; ++r) f.v[r] = lds64(vt + lm.vr[r][0]);
   }
   if constexpr (KvTraits<KV>::kQuant) {
-    const uint32_t sz = st + 2 * S::kTile + 4 * g;
+    const uint32_t sz = wr + S::kSzOff + 128 * st + 4 * g;
     f.ksz[0] = lds32(sz);
     f.ksz[1] = lds32(sz + 32);
     f.vsz[0] = lds32(sz + 64);
@@ -347,12 +435,12 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
 
 __host__ __device__ constexpr size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 
-// Dynamic shared memory: [prefix sums of the blocks per request][pipeline
-// stages of every warp].
+// Dynamic shared memory: [prefix sums of the blocks per request][slack to a
+// 1024-byte boundary][the stage regions of the 4 warps].
 template <int KV>
 __host__ __device__ constexpr size_t smem_bytes_for(int batch) {
-  return align128((batch + 1) * sizeof(int32_t)) +
-         static_cast<size_t>(kWarps) * Stage<KV>::kDepth * Stage<KV>::kBytes;
+  return align128((batch + 1) * sizeof(int32_t)) + 1024 +
+         static_cast<size_t>(kWarps) * Stage<KV>::kWarpBytes;
 }
 
 // Clamped length of request b.
@@ -395,7 +483,7 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch
 
 template <int KV, bool QBF>
 __global__ void __launch_bounds__(kDecodeThreads)
-    decode_kernel(DecodeArgs a) {
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ int32_t warp_sum[kWarps];
   using S = Stage<KV>;
@@ -466,10 +554,21 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int64_t x0 = gw * P;
   if (x0 >= total) return;  // no block barrier follows: warps are independent from here
   const int n = static_cast<int>(total - x0 < P ? total - x0 : P);
-  const uint32_t my_stages = static_cast<uint32_t>(__cvta_generic_to_shared(stages)) +
-                             static_cast<uint32_t>(warp * D * S::kBytes);
+  // this warp's stage region, 1024-byte aligned (the 128-byte swizzle repeats
+  // every 1024 bytes)
+  const uint32_t region0 =
+      (static_cast<uint32_t>(__cvta_generic_to_shared(stages)) + 1023u) & ~1023u;
+  const uint32_t wr = region0 + static_cast<uint32_t>(warp * S::kWarpBytes);
   LaneMap<KV> lm;
   lm.init(lane, g, t, static_cast<uint32_t>(a.kv_heads * S::kRow));
+  if constexpr (S::kTma) {
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < D; ++i) mbar_init(wr + S::kBarOff + 8 * i);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+  }
 
   // issue side: cursor, a 32-entry window of the block table, validity bits
   Cursor ic;
@@ -477,7 +576,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
   Cursor cc = ic;  // compute side
   int win_b = -1, win_j0 = 0;
   int32_t win = -1;
-  uint32_t ok_mask = 0;
+  uint32_t ok_mask = 0;  // stages holding a valid block in flight
+  uint32_t phase = 0;    // parity to wait for, per stage (TMA path)
   int k_issue = 0;   // next block of the range to issue
   int st_issue = 0;  // its stage
   auto issue_next = [&]() {
@@ -492,8 +592,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       const bool ok = phys >= 0 && phys < a.num_blocks;
       const uint32_t bit = 1u << st_issue;
       if (ok) {
-        issue_block<KV>(my_stages + st_issue * S::kBytes, a, lm, phys, ic.hgi / a.head_groups,
-                        lane);
+        issue_block<KV>(wr, st_issue, a, lm, phys, ic.hgi / a.head_groups, lane);
         ok_mask |= bit;
       } else {
         ok_mask &= ~bit;
@@ -501,7 +600,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       }
       if (k_issue + 1 < n) advance(ic, cum, a.batch);
     }
-    cp_async_commit();
+    if constexpr (!S::kTma) cp_async_commit();
     ++k_issue;
     st_issue = st_issue == D - 1 ? 0 : st_issue + 1;
   };
@@ -574,9 +673,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
   int st = 0;  // stage of block k
   for (int k = 0; k < n; ++k) {
-    issue_next();            // refills the stage block k - 1 used
-    cp_async_wait<D - 1>();  // this lane's copies of block k have landed
-    __syncwarp();            // ... and every other lane's
+    issue_next();  // refills the stage block k - 1 used
+    const bool blk_ok = (ok_mask >> st) & 1u;
+    if constexpr (S::kTma) {
+      if (blk_ok) {
+        if (!mbar_wait(wr + S::kBarOff + 8 * st, (phase >> st) & 1u)) {
+          // a copy did not land: report, wait (bounded) for the other copies
+          // this warp started, and stop
+          if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
+          const uint32_t rest = ok_mask & ~(1u << st);
+          for (int i = 0; i < D; ++i)
+            if ((rest >> i) & 1u) mbar_wait(wr + S::kBarOff + 8 * i, (phase >> i) & 1u);
+          return;
+        }
+        phase ^= 1u << st;
+      }
+    } else {
+      cp_async_wait<D - 1>();  // this lane's copies of block k have landed
+      __syncwarp();            // ... and every other lane's
+    }
 
     if (cc.b != seg_b || cc.hgi != seg_hgi) {
       if (seg_b >= 0) flush();
@@ -636,9 +751,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
       l0 = l1 = z0 = z1 = r0 = r1 = 0.f;
     }
 
-    if ((ok_mask >> st) & 1u) {
+    if (blk_ok) {
+      ok_mask &= ~(1u << st);
       Frag<KV> cur;
-      read_frag<KV>(cur, my_stages + st * S::kBytes, lm, g);
+      read_frag<KV>(cur, wr, st, lm, g);
       // S^T = K Q^T, even and odd k-steps in two accumulators
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -746,7 +862,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     st = st == D - 1 ? 0 : st + 1;
     if (k + 1 < n) advance(cc, cum, a.batch);
   }
-  cp_async_wait<0>();
+  if constexpr (!S::kTma) cp_async_wait<0>();
   flush();
 }
 
@@ -754,7 +870,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 // whose blocks were split between warps (log-sum-exp in the exp2 domain).
 // Requests covered by one warp were written by the decode kernel.
 template <bool QBF>
-__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (bh >= static_cast<int64_t>(a.batch) * a.q_heads) return;

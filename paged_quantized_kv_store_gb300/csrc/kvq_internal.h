@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (kvq_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -41,6 +42,10 @@ struct TablesArgs {
 };
 
 struct DecodeArgs {
+  // TMA descriptors of the K and V pools (quantized pools only): 4-D views
+  // [num_blocks][16][kv_heads][row bytes], one box = one (block, head) tile
+  CUtensorMap k_map;
+  CUtensorMap v_map;
   const uint8_t* k;
   const uint8_t* v;
   const uint32_t* k_sz;  // (scale, zero) fp16 pairs
