@@ -175,14 +175,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha(files=("kvq_decode.cu", "kvq_device.cuh")) -> str:
+    """Hash of the decode kernel's source with // comments and blank lines
+    removed, so that editing a comment keeps a DRAM-traffic record valid."""
+    src = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(ROOT, "paged_quantized_kv_store_gb300", "csrc", fn)) as f:
+            for line in f:
+                code = re.sub(r"\s*//.*$", "", line.rstrip("\n")).rstrip()
+                if code:
+                    src.update(code.encode() + b"\n")
+    return src.hexdigest()[:16]
+
+
 def traffic_from_profile(workload: str):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
-    src = hashlib.sha256()
-    for fn in ("kvq_decode.cu", "kvq_device.cuh"):
-        with open(os.path.join(ROOT, "paged_quantized_kv_store_gb300", "csrc", fn), "rb") as f:
-            src.update(f.read())
-    sha = src.hexdigest()[:16]
+    sha = kernel_source_sha()
     path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
     try:
         text = open(path).read()

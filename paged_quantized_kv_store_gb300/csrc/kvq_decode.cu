@@ -13,7 +13,8 @@
 //   warps is exact whatever the mix of request lengths. Each CTA first scans
 //   the request lengths into per-request block offsets in shared memory.
 //   A warp streams its range through its own ring of shared-memory stages
-//   (cp.async, several blocks in flight), crossing request boundaries without
+//   (several blocks in flight: TMA tensor copies completing on an mbarrier
+//   for INT8 tiles, per-lane cp.async otherwise), crossing request boundaries without
 //   a pause: it writes the output of every request it covers entirely and,
 //   for the request holding the first and the one holding the last block of
 //   its range, a partial record (running max, sum, unnormalised output) that
@@ -27,9 +28,12 @@
 //                K = 16 tokens.
 //   Quantized codes go into the tensor cores as exact 16-bit floats a + c,
 //   made by writing the code into the mantissa of a constant (INT4: a shift
-//   and a lop3 per two codes, a = 16; INT8: a prmt and a packed subtract,
-//   centred: a = -128); the offset is removed outside the products together
-//   with the per-token zero: c S + Z = (a + c) S + Z - a S.
+//   and a lop3 per two codes, a = 16, or a = 128 on the K side of bf16
+//   queries; INT8 K side: one prmt per two codes, a = 1024, or a = -128
+//   through fp32 for bf16 queries; INT8 V side: a
+//   prmt and a packed subtract, centred, a = -128); the offset is removed
+//   outside the products together with the per-token zero:
+//   c S + Z = (a + c) S + Z - a S.
 //     q.k = S (q.(a + c)) + (Z - a S) sum(q)
 //     sum_t p_t v_t = sum_t P'_t (a + c_t) + sum_t p_t (Z_t + mid S_t)
 //                     - (a + mid) sum_t P'_t,   P'_t = fp16(p_t S_t)
