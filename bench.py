@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    p.add_argument("--shared-prefix", choices=["auto", "on", "off"], default="off",
+                   help="decode shared prefixes once per group (auto: when the workload has one)")
     p.add_argument("--json-out", default="")
     return p.parse_args()
 
@@ -78,19 +80,22 @@ def workload_desc(wl) -> dict:
     }
 
 
-def decode_algorithmic_bytes(wl) -> int:
-    """Bytes the decode call must move: KV codes + scale/zero of every context
-    token, Q, the output, the block tables and the lengths."""
+def decode_logical_bytes(wl) -> int:
+    """KV codes + scale/zero of every context token of every request (a block
+    shared by n requests counted n times), Q, the output, the block tables
+    and the lengths."""
     kv = int(np.sum(wl.seq_lens, dtype=np.int64)) * wl.kv_token_bytes()
     q = wl.batch * wl.q_heads * wl.head_dim * 2
     nblk = int(np.sum((wl.seq_lens + 15) // 16))
     return kv + 2 * q + 4 * nblk + 4 * wl.batch
 
 
-def unique_decode_bytes(wl) -> int:
-    """As above but counting each physical block once (shared prefixes)."""
+def decode_algorithmic_bytes(wl) -> int:
+    """Bytes the decode call must move at the least: as above, but every stored
+    token once however many requests attend it (shared prefixes). Equal to
+    the logical bytes when no block is shared."""
     seen = set()
-    total = 0
+    kv = 0
     for b in range(wl.batch):
         L = int(wl.seq_lens[b])
         for j in range((L + 15) // 16):
@@ -98,9 +103,23 @@ def unique_decode_bytes(wl) -> int:
             if blk in seen:
                 continue
             seen.add(blk)
-            total += min(16, L - 16 * j) * wl.kv_token_bytes()
+            kv += min(16, L - 16 * j) * wl.kv_token_bytes()
     q = wl.batch * wl.q_heads * wl.head_dim * 2
-    return total + 2 * q
+    nblk = int(np.sum((wl.seq_lens + 15) // 16))
+    return kv + 2 * q + 4 * nblk + 4 * wl.batch
+
+
+def prefix_groups(wl):
+    """The requests holding the workload's whole common prefix, as one group
+    (what a radix prefix cache knows when it schedules the batch); None when
+    the workload shares nothing."""
+    if wl.prefix_blocks is None or wl.shared_tokens is None:
+        return None
+    full = len(wl.prefix_blocks)
+    members = [b for b in range(wl.batch) if int(wl.shared_tokens[b]) == 16 * full]
+    if len(members) < 2:
+        return None
+    return members, full
 
 
 # ---- clocks (NVML through ctypes, read-only) -----------------------------------
@@ -252,6 +271,14 @@ def run_ours(args, rank: int, world: int, dist):
         "slot_mapping": slots, "seq_lens": wl.seq_lens.astype(np.int32),
         "req_pool_indices": wl.req_pool_indices.astype(np.int32),
     }
+    groups = prefix_groups(wl) if args.shared_prefix != "off" else None
+    if args.shared_prefix == "on" and groups is None:
+        raise SystemExit(f"--shared-prefix on: {wl.name} has no shared prefix")
+    if groups is not None:
+        # the group description is a per-step input like the lengths
+        h_inputs["grp_off"] = np.array([0, len(groups[0])], dtype=np.int32)
+        h_inputs["grp_mem"] = np.array(groups[0], dtype=np.int32)
+        h_inputs["grp_shared"] = np.array([groups[1]], dtype=np.int32)
     views = {"q": tdt[wl.q_dtype], "k_new": tdt[wl.in_dtype], "v_new": tdt[wl.in_dtype]}
 
     def typed(raw):
@@ -271,12 +298,29 @@ def run_ours(args, rank: int, world: int, dist):
                                                step.block_tables, step.dev_err)
         kvq.kv_store_quant(pool, inp["k_new"], inp["v_new"], inp["slot_mapping"], step.dev_err)
 
-    def dec_step(inp):
-        kvq.paged_decode_attn(pool, inp["q"], step.out, step.block_tables, inp["seq_lens"],
-                              wl.max_seq_len, wl.sm_scale, args.num_splits, step.workspace,
-                              step.dev_err)
+    if groups is None:
+        def dec_step(inp):
+            kvq.paged_decode_attn(pool, inp["q"], step.out, step.block_tables, inp["seq_lens"],
+                                  wl.max_seq_len, wl.sm_scale, args.num_splits, step.workspace,
+                                  step.dev_err)
 
-    launches_per_step = 4  # tables, store, decode, combine
+        launches_per_step = 4  # tables, store, decode, combine
+        decode_kernels = "paged_decode_attn (decode_kernel + combine_kernel)"
+    else:
+        sp_bytes = kvq.paged_decode_attn_shared_prefix_workspace_size(
+            wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, groups[1], args.num_splits)
+        sp_ws = torch.empty(sp_bytes, dtype=torch.uint8, device=dev)
+
+        def dec_step(inp):
+            g = kvq.SharedPrefixGroups(inp["grp_off"], inp["grp_mem"], inp["grp_shared"],
+                                       groups[1])
+            kvq.paged_decode_attn_shared_prefix(pool, inp["q"], step.out, step.block_tables,
+                                                inp["seq_lens"], wl.max_seq_len, wl.sm_scale, g,
+                                                args.num_splits, sp_ws, step.dev_err)
+
+        launches_per_step = 5  # tables, store, prefix, decode, combine (+ a memset)
+        decode_kernels = ("paged_decode_attn_shared_prefix (prefix_kernel + decode_kernel + "
+                          "combine_kernel)")
 
     for _ in range(max(args.warmup, 1)):
         pre_step(d_in)
@@ -393,7 +437,7 @@ def run_ours(args, rank: int, world: int, dist):
     # ---- roofline of the dominant call (decode + combine) ---------------------------
     box_copy = copy_bandwidth_gbs(dev)
     alg = decode_algorithmic_bytes(wl)
-    uniq = unique_decode_bytes(wl)
+    logical = decode_logical_bytes(wl)
     mean_decode_ms = float(np.mean(decode_ms))
     peak, peak_kind = measured_peak()
     achieved = alg / (mean_decode_ms / 1e3) / 1e9
@@ -401,14 +445,14 @@ def run_ours(args, rank: int, world: int, dist):
     roofline = {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "traffic": traffic,
-        "kernel": "paged_decode_attn (decode_kernel + combine_kernel)",
+        "kernel": decode_kernels,
         "peak_kind": f"{peak_kind} (hbm_gbs)",
-        "algorithmic_bytes_per_launch": alg, "unique_bytes_per_launch": uniq,
+        "algorithmic_bytes_per_launch": alg, "logical_bytes_per_launch": logical,
         "decode_ms_mean": round(mean_decode_ms, 5),
         "decode_ms_median": round(float(np.median(decode_ms)), 5),
         "decode_ms_min": round(float(np.min(decode_ms)), 5),
         "decode_ms_max": round(float(np.max(decode_ms)), 5),
-        "unique_frac": round(uniq / (mean_decode_ms / 1e3) / 1e9 / peak, 4),
+        "logical_gbs": round(logical / (mean_decode_ms / 1e3) / 1e9, 1),
         "kernel_source_sha": sha,
         "copy_gbs_this_gpu": round(box_copy, 1),
         "frac_of_this_gpu_copy": round(achieved / box_copy, 4),
@@ -422,6 +466,8 @@ def run_ours(args, rank: int, world: int, dist):
         "data": "synthetic (seeded counter-based generator; no dataset)",
         "config": {**workload_desc(wl), "l2": "no flush: the pool is larger than L2",
                    "cuda_graph": use_graph,
+                   "shared_prefix": None if groups is None else
+                   {"groups": 1, "members": len(groups[0]), "shared_blocks": groups[1]},
                    "plan": plan, "parallelism": f"replicas x{world} (no data-path collective)"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -70,6 +70,7 @@ typedef enum kvq_dtype {
 #define KVQ_DEV_ERR_SLOT 16u       /* store: slot >= num_blocks * 16 (token skipped) */
 #define KVQ_DEV_ERR_BLOCK_ID 32u   /* decode: block id outside [0, num_blocks) (block skipped) */
 #define KVQ_DEV_ERR_TIMEOUT 64u    /* decode: a tile copy did not complete within 2 s (warp stopped) */
+#define KVQ_DEV_ERR_PREFIX 128u    /* shared-prefix decode: a group description that does not hold */
 
 /*
  * One layer's KV pool (KVPool of "pymllm Runtime Design"; shape from LMDeploy
@@ -207,6 +208,50 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              int32_t max_seq_len, float sm_scale, int32_t num_splits,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err,
                              void* stream);
+
+/*
+ * paged_decode_attn_shared_prefix -- the same attention as paged_decode_attn,
+ * computed as a cascade for requests that share leading blocks
+ * ("pymllm Runtime Design", section "KV cache 与 prefix cache": radix prefix
+ * cache hits reuse the matched prefix's KV slots; LMDeploy article §2.2:
+ * sequences share physical blocks under prefix caching). Each shared block is
+ * read once per group and kv head and multiplied with the queries of all the
+ * group's members together; each member's own blocks then go through the
+ * decode kernel, and the two parts are merged with a log-sum-exp.
+ *
+ * Arguments not listed here mean what they mean for paged_decode_attn.
+ *  group_offsets       : device int32 [num_groups + 1], non-decreasing;
+ *                        group G's members are
+ *                        group_members[group_offsets[G] .. group_offsets[G + 1]).
+ *  group_members       : device int32 [num_members]: request indices in
+ *                        [0, batch); a request belongs to at most one group.
+ *                        Requests in no group are decoded as usual.
+ *  group_shared_blocks : device int32 [num_groups]: the number of leading
+ *                        blocks that every member's block table holds
+ *                        identically, each full (16 * shared <= seq_lens[b]
+ *                        for every member b); at most max_shared_blocks.
+ *  max_shared_blocks   : host bound of group_shared_blocks, at most
+ *                        max_blocks_per_seq (sizes the workspace).
+ *  workspace           : at least *bytes of
+ *                        paged_decode_attn_shared_prefix_workspace_size.
+ * A group description that does not hold (a member out of range or listed
+ * twice, tables that differ within the shared blocks, a member shorter than
+ * the shared part, a shared count above max_shared_blocks) sets
+ * KVQ_DEV_ERR_PREFIX; the output rows of that group are then unspecified,
+ * and no memory outside the arguments is touched. The result equals
+ * paged_decode_attn's up to rounding order.
+ */
+kvq_status paged_decode_attn_shared_prefix_workspace_size(
+    int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t max_seq_len,
+    int32_t num_splits, int32_t max_shared_blocks, size_t* bytes);
+
+kvq_status paged_decode_attn_shared_prefix(
+    const kvq_pool* pool, const void* q, int32_t q_dtype, void* out, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+    int32_t max_seq_len, float sm_scale, const int32_t* group_offsets,
+    const int32_t* group_members, const int32_t* group_shared_blocks, int32_t num_groups,
+    int32_t num_members, int32_t max_shared_blocks, int32_t num_splits, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
  * paged_decode_attn_noalloc -- the same computation as paged_decode_attn,

@@ -30,7 +30,7 @@ HEAD_DIM = 128
 
 DEV_ERR_BITS = {
     "req_slot": 1, "length": 2, "kv_index": 4, "not_blocked": 8, "slot": 16, "block_id": 32,
-    "timeout": 64,
+    "timeout": 64, "prefix": 128,
 }
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
@@ -61,7 +61,8 @@ class _Plan(ctypes.Structure):
 
 EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decode_attn_plan",
             "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
-            "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc"]
+            "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc",
+            "paged_decode_attn_shared_prefix_workspace_size", "paged_decode_attn_shared_prefix"]
 
 
 def load(build_if_missing: bool = False):
@@ -92,6 +93,13 @@ def load(build_if_missing: bool = False):
     lib.paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, I32, P, I32,
                                               I32, I32, F, I32, P, P]
     lib.paged_decode_attn_noalloc.restype = ctypes.c_int
+    lib.paged_decode_attn_shared_prefix_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32,
+                                                                   I32, ctypes.POINTER(SZ)]
+    lib.paged_decode_attn_shared_prefix_workspace_size.restype = ctypes.c_int
+    lib.paged_decode_attn_shared_prefix.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, I32, P,
+                                                    I32, I32, I32, F, P, P, P, I32, I32, I32,
+                                                    I32, P, SZ, P, P]
+    lib.paged_decode_attn_shared_prefix.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.kvq_check_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -242,6 +250,104 @@ def paged_decode_attn_noalloc(pool: KVPool, q, out, block_tables, seq_lens, max_
                                        int(max_seq_len), float(sm_scale), int(num_splits),
                                        _ptr(dev_err), _stream(stream))
     _check(st, "paged_decode_attn_noalloc")
+
+
+def paged_decode_attn_shared_prefix_workspace_size(batch, q_heads, kv_heads, max_seq_len,
+                                                   max_shared_blocks, num_splits=0,
+                                                   head_dim=HEAD_DIM) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().paged_decode_attn_shared_prefix_workspace_size(
+        batch, q_heads, kv_heads, head_dim, max_seq_len, num_splits, max_shared_blocks,
+        ctypes.byref(n))
+    _check(st, "paged_decode_attn_shared_prefix_workspace_size")
+    return int(n.value)
+
+
+@dataclass
+class SharedPrefixGroups:
+    """Requests that share leading blocks, as paged_decode_attn_shared_prefix
+    takes them: group G's members are members[offsets[G]:offsets[G + 1]] and
+    share their first shared_blocks[G] blocks (device int32 tensors)."""
+
+    offsets: object
+    members: object
+    shared_blocks: object
+    max_shared_blocks: int
+
+    @property
+    def num_groups(self) -> int:
+        return int(self.shared_blocks.numel())
+
+    @property
+    def num_members(self) -> int:
+        return int(self.members.numel())
+
+    @classmethod
+    def from_lists(cls, groups, device="cuda"):
+        """groups: iterable of (member request indices, shared block count)."""
+        import torch
+        offsets, members, shared = [0], [], []
+        for mem, sb in groups:
+            members.extend(int(b) for b in mem)
+            offsets.append(len(members))
+            shared.append(int(sb))
+
+        def t(x):
+            return torch.tensor(x, dtype=torch.int32, device=device)
+
+        return cls(t(offsets), t(members), t(shared), max(shared, default=0))
+
+    @classmethod
+    def detect(cls, block_tables, seq_lens, min_members=2, min_shared_blocks=1, device="cuda"):
+        """Host-side grouping of a batch by common leading blocks (numpy
+        arrays): requests with the same first block form a candidate group;
+        its shared count s is chosen to maximise (members sharing s blocks)
+        x s, and members sharing fewer stay outside (decoded on their own).
+        Only full blocks are shared (16 s <= length)."""
+        import numpy as np
+        bt = np.asarray(block_tables)
+        lens = np.asarray(seq_lens)
+        by_first = {}
+        for b in range(bt.shape[0]):
+            if int(lens[b]) // 16 >= 1:
+                by_first.setdefault(int(bt[b, 0]), []).append(b)
+        groups = []
+        for cand in by_first.values():
+            if len(cand) < min_members:
+                continue
+            lead = cand[0]
+            lcp = {}
+            for b in cand:
+                n = min(int(lens[b]) // 16, int(lens[lead]) // 16)
+                eq = bt[b, :n] == bt[lead, :n]
+                lcp[b] = n if eq.all() else int(np.argmin(eq))
+            best, best_s = 0, 0
+            for s_ in sorted(set(lcp.values())):
+                if s_ < min_shared_blocks:
+                    continue
+                k = sum(1 for v in lcp.values() if v >= s_)
+                if k >= min_members and k * s_ > best:
+                    best, best_s = k * s_, s_
+            if best_s > 0:
+                groups.append(([b for b in cand if lcp[b] >= best_s], best_s))
+        return cls.from_lists(groups, device=device)
+
+
+def paged_decode_attn_shared_prefix(pool: KVPool, q, out, block_tables, seq_lens, max_seq_len,
+                                    sm_scale, groups: SharedPrefixGroups, num_splits=0,
+                                    workspace=None, dev_err=None, stream=None):
+    """paged_decode_attn computed as a cascade over shared leading blocks; see kvq.h."""
+    lib = load()
+    ps = pool.c_struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.paged_decode_attn_shared_prefix(
+        ctypes.byref(ps), _ptr(q), _dtype_code(q), _ptr(out), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(seq_lens), int(q.shape[0]), int(q.shape[1]),
+        int(max_seq_len), float(sm_scale), _ptr(groups.offsets),
+        _ptr(groups.members) if groups.num_members else None, _ptr(groups.shared_blocks),
+        groups.num_groups, groups.num_members, int(groups.max_shared_blocks), int(num_splits),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check(st, "paged_decode_attn_shared_prefix")
 
 
 def kvq_check_error(dev_err, stream=None) -> int:

@@ -90,11 +90,140 @@ bool encode_pool_map(CUtensorMap* map, void* base, int64_t num_blocks, int kv_he
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared-prefix groups as the caller describes them.
+struct PrefixDesc {
+  const int32_t* offsets;
+  const int32_t* members;
+  const int32_t* shared_blocks;
+  int num_groups;
+  int num_members;
+  int max_shared;
+};
+
+// Workspace of a shared-prefix decode: the plain decode's (length header and
+// split-K records), then the per-request shared block counts, then one
+// record per (request, q head, chunk of shared blocks).
+struct SharedPrefixLayout {
+  int chunk;       // shared blocks per prefix work unit
+  int max_chunks;  // chunks of the longest shared prefix
+  size_t skip_off, part_off, total;
+};
+
+SharedPrefixLayout shared_prefix_layout(const kvq_decode_plan& plan, int batch, int q_heads,
+                                        int max_shared) {
+  SharedPrefixLayout l;
+  // about 8 chunks per prefix, 4 to 32 blocks each: enough units to fill the
+  // device for a few dozen members, few records to merge per request
+  l.chunk = std::min(kvq::kMaxPrefixChunk, std::max(4, (max_shared + 7) / 8));
+  l.max_chunks = (max_shared + l.chunk - 1) / l.chunk;
+  l.skip_off = align_up(plan.workspace_bytes, 256);
+  l.part_off = l.skip_off + align_up(static_cast<size_t>(batch) * sizeof(int32_t), 256);
+  l.total = l.part_off + static_cast<size_t>(batch) * q_heads * l.max_chunks * kvq::kPartStride *
+                             sizeof(float);
+  return l;
+}
+
+// Decode attention, plain (pd == nullptr) or with shared prefixes.
+kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+                       int32_t max_seq_len, float sm_scale, int32_t num_splits,
+                       const PrefixDesc* pd, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_err, void* stream) {
+  const kvq_status ps = check_pool(pool);
+  if (ps != KVQ_OK) return ps;
+  if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (is_float16(pool->kv_dtype) && q_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
+  if (batch < 0 || q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  kvq_decode_plan plan;
+  const kvq_status st = paged_decode_attn_plan(batch, q_heads, pool->kv_heads, pool->head_dim,
+                                               max_seq_len, num_splits, 0, &plan);
+  if (st != KVQ_OK) return st;
+  if (batch == 0) return KVQ_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
+  const SharedPrefixLayout lay =
+      shared_prefix_layout(plan, batch, q_heads, pd != nullptr ? pd->max_shared : 0);
+  const size_t need = pd != nullptr ? lay.total : plan.workspace_bytes;
+  if (workspace == nullptr || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  kvq::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (pool->kv_dtype == KVQ_INT8) {  // the INT8 kernel stages its tiles by TMA
+    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
+        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
+      return KVQ_ERR_CUDA;
+  } else {
+    std::memset(&a.k_map, 0, sizeof(a.k_map));
+    std::memset(&a.v_map, 0, sizeof(a.v_map));
+  }
+  a.k = static_cast<const uint8_t*>(pool->k);
+  a.v = static_cast<const uint8_t*>(pool->v);
+  a.k_sz = static_cast<const uint32_t*>(pool->k_sz);
+  a.v_sz = static_cast<const uint32_t*>(pool->v_sz);
+  a.num_blocks = pool->num_blocks;
+  a.kv_heads = pool->kv_heads;
+  a.q = q;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.q_heads = q_heads;
+  a.group = q_heads / pool->kv_heads;
+  a.head_groups = plan.head_groups;
+  a.hpg = plan.heads_per_group;
+  a.min_blocks_per_warp = plan.min_blocks_per_warp;
+  const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
+  a.len_cap = std::min(max_blocks_per_seq, nblk) * kBlock;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.hdr = static_cast<int32_t*>(workspace);
+  a.part = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) +
+      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256));
+  a.dev_err = dev_err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pd != nullptr && pd->num_groups > 0 && pd->max_shared > 0) {
+    a.grp_off = pd->offsets;
+    a.grp_mem = pd->members;
+    a.grp_shared = pd->shared_blocks;
+    a.num_groups = pd->num_groups;
+    a.num_members = pd->num_members;
+    a.max_shared = pd->max_shared;
+    a.pchunk = lay.chunk;
+    a.pmax_chunks = lay.max_chunks;
+    a.skip = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + lay.skip_off);
+    a.ppart = reinterpret_cast<float*>(static_cast<char*>(workspace) + lay.part_off);
+    if (cudaMemsetAsync(a.skip, 0, static_cast<size_t>(batch) * sizeof(int32_t), s) !=
+        cudaSuccess)
+      return KVQ_ERR_CUDA;
+    const int pper_sm = kvq::prefix_ctas_per_sm(pool->kv_dtype, q_dtype, pd->num_groups);
+    if (pper_sm <= 0) return KVQ_ERR_CUDA;
+    if (kvq::launch_prefix(a, pool->kv_dtype, q_dtype, plan.num_sms * pper_sm, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
+  // persistent grid: as many CTAs as fit on the device at once (the
+  // workspace has partial slots for kMaxCtasPerSm per SM)
+  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
+                              kvq::kMaxCtasPerSm);
+  if (per_sm <= 0) return KVQ_ERR_CUDA;
+  const int grid = plan.num_sms * per_sm;
+  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (kvq::launch_combine(a, q_dtype, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t kvq_version(void) { return 100; }
+int32_t kvq_version(void) { return 101; }
 
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
@@ -198,70 +327,44 @@ kvq_status paged_decode_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              int32_t max_seq_len, float sm_scale, int32_t num_splits,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err,
                              void* stream) {
-  const kvq_status ps = check_pool(pool);
-  if (ps != KVQ_OK) return ps;
-  if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
-  if (is_float16(pool->kv_dtype) && q_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
-  if (batch < 0 || q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
-    return KVQ_ERR_INVALID_ARG;
-  if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                     q_heads, max_seq_len, sm_scale, num_splits, nullptr, workspace,
+                     workspace_bytes, dev_err, stream);
+}
+
+kvq_status paged_decode_attn_shared_prefix_workspace_size(
+    int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim, int32_t max_seq_len,
+    int32_t num_splits, int32_t max_shared_blocks, size_t* bytes) {
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (max_shared_blocks < 0) return KVQ_ERR_INVALID_ARG;
   kvq_decode_plan plan;
-  const kvq_status st = paged_decode_attn_plan(batch, q_heads, pool->kv_heads, pool->head_dim,
-                                               max_seq_len, num_splits, 0, &plan);
+  const kvq_status st = paged_decode_attn_plan(batch, q_heads, kv_heads, head_dim, max_seq_len,
+                                               num_splits, 0, &plan);
   if (st != KVQ_OK) return st;
-  if (batch == 0) return KVQ_OK;
-  if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
-    return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return KVQ_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
-  kvq::DecodeArgs a;
-  if (pool->kv_dtype == KVQ_INT8) {  // the INT8 kernel stages its tiles by TMA
-    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
-        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
-      return KVQ_ERR_CUDA;
-  } else {
-    std::memset(&a.k_map, 0, sizeof(a.k_map));
-    std::memset(&a.v_map, 0, sizeof(a.v_map));
-  }
-  a.k = static_cast<const uint8_t*>(pool->k);
-  a.v = static_cast<const uint8_t*>(pool->v);
-  a.k_sz = static_cast<const uint32_t*>(pool->k_sz);
-  a.v_sz = static_cast<const uint32_t*>(pool->v_sz);
-  a.num_blocks = pool->num_blocks;
-  a.kv_heads = pool->kv_heads;
-  a.q = q;
-  a.out = out;
-  a.block_tables = block_tables;
-  a.max_blocks = max_blocks_per_seq;
-  a.seq_lens = seq_lens;
-  a.batch = batch;
-  a.q_heads = q_heads;
-  a.group = q_heads / pool->kv_heads;
-  a.head_groups = plan.head_groups;
-  a.hpg = plan.heads_per_group;
-  a.min_blocks_per_warp = plan.min_blocks_per_warp;
-  const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
-  a.len_cap = std::min(max_blocks_per_seq, nblk) * kBlock;
-  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  a.hdr = static_cast<int32_t*>(workspace);
-  a.part = reinterpret_cast<float*>(
-      static_cast<char*>(workspace) +
-      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256));
-  a.dev_err = dev_err;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // persistent grid: as many CTAs as fit on the device at once (the
-  // workspace has partial slots for kMaxCtasPerSm per SM)
-  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
-                              kvq::kMaxCtasPerSm);
-  if (per_sm <= 0) return KVQ_ERR_CUDA;
-  const int grid = plan.num_sms * per_sm;
-  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  if (kvq::launch_combine(a, q_dtype, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  *bytes = shared_prefix_layout(plan, batch, q_heads, max_shared_blocks).total;
   return KVQ_OK;
+}
+
+kvq_status paged_decode_attn_shared_prefix(
+    const kvq_pool* pool, const void* q, int32_t q_dtype, void* out, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_heads,
+    int32_t max_seq_len, float sm_scale, const int32_t* group_offsets,
+    const int32_t* group_members, const int32_t* group_shared_blocks, int32_t num_groups,
+    int32_t num_members, int32_t max_shared_blocks, int32_t num_splits, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (num_groups < 0 || num_members < 0 || max_shared_blocks < 0) return KVQ_ERR_INVALID_ARG;
+  if (max_shared_blocks > max_blocks_per_seq) return KVQ_ERR_INVALID_ARG;
+  if (num_groups > kvq::kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  if (num_groups > 0 &&
+      (group_offsets == nullptr || group_shared_blocks == nullptr ||
+       (num_members > 0 && group_members == nullptr)))
+    return KVQ_ERR_INVALID_ARG;
+  PrefixDesc pd{group_offsets, group_members, group_shared_blocks, num_groups, num_members,
+                max_shared_blocks};
+  return decode_impl(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                     q_heads, max_seq_len, sm_scale, num_splits, &pd, workspace,
+                     workspace_bytes, dev_err, stream);
 }
 
 kvq_status kvq_check_error(int32_t* dev_err, uint32_t* bits_out, void* stream) {

@@ -69,6 +69,21 @@ struct DecodeArgs {
   int32_t* hdr;          // [0] blocks per head group, [1] blocks per warp,
                          // [2 .. 2 + batch] prefix sums of the blocks per request
   int32_t* dev_err;
+  // shared-prefix decode only (null / 0 otherwise): group G's members are
+  // grp_mem[grp_off[G] .. grp_off[G + 1]) and share their first grp_shared[G]
+  // blocks; the prefix kernel fills skip and ppart, the decode kernel reads
+  // each request's blocks from skip[b] on and, with the combine kernel,
+  // merges ppart
+  const int32_t* grp_off;     // [num_groups + 1]
+  const int32_t* grp_mem;     // [num_members]
+  const int32_t* grp_shared;  // [num_groups]
+  int num_groups;
+  int num_members;
+  int max_shared;             // bound on grp_shared (blocks)
+  int pchunk;                 // shared blocks per prefix work unit (<= 32)
+  int pmax_chunks;            // ceil(max_shared / pchunk): records per (request, q head)
+  int32_t* skip;              // [batch] shared blocks of request b (0: none)
+  float* ppart;               // [batch][q_heads][pmax_chunks][kPartStride]
 };
 
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
@@ -77,13 +92,18 @@ cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                           cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s);
+cudaError_t launch_prefix(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
+                          cudaStream_t s);
 
 // CTAs of the decode kernel resident per SM (occupancy) for a dtype pair and batch
 int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
+// the same for the shared-prefix kernel and a number of groups
+int prefix_ctas_per_sm(int kv_dtype, int q_dtype, int num_groups);
 
 constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared memory
 constexpr int kDecodeThreads = 128;
 constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many CTAs per SM
 constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)
+constexpr int kMaxPrefixChunk = 32;    // shared blocks per prefix unit: one table window
 
 }  // namespace kvq

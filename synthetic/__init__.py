@@ -444,6 +444,36 @@ def cfg5(seed: int = 4, batch: int = 256, lo: int = 256, hi: int = 2048,
                                f"decode requests U[{lo},{hi}]")
 
 
+def shared_prefix(name: str, kv_dtype: str, lens, q_heads: int, kv_heads: int,
+                  prefix_blocks: int, seed: int = 11, in_dtype: str = "f16",
+                  q_dtype: Optional[str] = None, extra_blocks: int = 3) -> Workload:
+    """Small workload with cfg4's structure for any pool type and head counts:
+    request b's first k_b = min(prefix_blocks, (L_b - 1) // 16) blocks are
+    the common prefix's (same physical blocks, same rows); the rest are
+    private random blocks."""
+    lens = np.asarray(lens, dtype=np.int32)
+    k = np.maximum(np.minimum(prefix_blocks, (lens - 1) // BLOCK_SIZE), 0).astype(np.int32)
+    nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    total = prefix_blocks + int((nblk - k).sum()) + extra_blocks
+    perm = permutation(seed, S_PERM, total)
+    pfx = perm[:prefix_blocks].astype(np.int32)
+    bt = np.full((len(lens), max(int(nblk.max()), 1)), -1, dtype=np.int32)
+    c = prefix_blocks
+    for b in range(len(lens)):
+        bt[b, :k[b]] = pfx[:k[b]]
+        n = int(nblk[b] - k[b])
+        bt[b, k[b]:nblk[b]] = perm[c:c + n]
+        c += n
+    if q_dtype is None:
+        q_dtype = kv_dtype if kv_dtype in ("f16", "bf16") else in_dtype
+    if kv_dtype in ("f16", "bf16"):
+        in_dtype = kv_dtype
+    return _finish(name, kv_dtype, in_dtype, q_dtype, q_heads, kv_heads, seed, lens, total, bt,
+                   shared_tokens=(k * BLOCK_SIZE).astype(np.int32), prefix_blocks=pfx,
+                   description=f"{kv_dtype} KV, {q_heads}q/{kv_heads}kv, {len(lens)} requests, "
+                               f"shared {prefix_blocks}-block prefix")
+
+
 def by_name(name: str, **kw) -> Workload:
     return {"cfg1": cfg1, "cfg2": cfg2, "cfg3": cfg3, "cfg4": cfg4, "cfg5": cfg5}[name](**kw)
 

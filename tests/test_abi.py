@@ -7,6 +7,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import paged_quantized_kv_store_gb300 as kvq
@@ -137,3 +138,49 @@ def test_product_path_has_no_oracle_dependency():
                 for banned in ("import oracle", "from oracle", "kvq_oracle", "synthetic",
                                "kvqgen"):
                     assert banned not in text, (fn, banned)
+
+
+def test_shared_prefix_validation(lib):
+    """Argument checks of paged_decode_attn_shared_prefix that run before any
+    device access."""
+    f = lib.paged_decode_attn_shared_prefix
+    p = 256
+    args = dict(q=p, q_dtype=0, out=p, bt=p, mb=4, sl=p, batch=2, hq=4, msl=64, scale=0.1,
+                off=p, mem=p, sh=p, ng=1, nm=2, maxs=2, splits=0, ws=None, wsb=0, err=None,
+                s=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(ctypes.byref(_pool()), a["q"], a["q_dtype"], a["out"], a["bt"], a["mb"],
+                 a["sl"], a["batch"], a["hq"], a["msl"], a["scale"], a["off"], a["mem"],
+                 a["sh"], a["ng"], a["nm"], a["maxs"], a["splits"], a["ws"], a["wsb"],
+                 a["err"], a["s"])
+
+    assert call(ng=-1) == 1
+    assert call(nm=-1) == 1
+    assert call(maxs=-1) == 1
+    assert call(maxs=5) == 1          # more shared blocks than table columns
+    assert call(off=None) == 1
+    assert call(sh=None) == 1
+    assert call(mem=None) == 1
+    assert call(ng=9000) == 2
+
+
+def test_shared_prefix_group_detection():
+    """Host-side grouping by common leading blocks."""
+    bt = np.array([[7, 8, 9, 1], [7, 8, 9, 2], [7, 8, 3, -1], [5, 6, -1, -1], [7, 8, 9, 4]],
+                  dtype=np.int32)
+    lens = np.array([60, 64, 40, 30, 50], dtype=np.int32)
+    g = kvq.SharedPrefixGroups.detect(bt, lens, device="cpu")
+    # requests 0, 1, 4 share 3 blocks (3 x 3 = 9 > 4 x 2 = 8); 2 stays out
+    assert g.num_groups == 1
+    assert g.members.tolist() == [0, 1, 4]
+    assert g.shared_blocks.tolist() == [3] and g.offsets.tolist() == [0, 3]
+    assert g.max_shared_blocks == 3
+    # only full blocks are shared: a 47-token request has 2 full blocks
+    lens2 = np.array([47, 64, 40, 30, 47], dtype=np.int32)
+    g2 = kvq.SharedPrefixGroups.detect(bt, lens2, device="cpu")
+    assert g2.members.tolist() == [0, 1, 2, 4] and g2.shared_blocks.tolist() == [2]
+    e = kvq.SharedPrefixGroups.from_lists([], device="cpu")
+    assert e.num_groups == 0 and e.num_members == 0 and e.max_shared_blocks == 0
