@@ -194,7 +194,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha(files=("kvq_decode.cu", "kvq_device.cuh")) -> str:
+def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh")) -> str:
     """Hash of the decode kernel's source with // comments and blank lines
     removed, so that editing a comment keeps a DRAM-traffic record valid."""
     src = hashlib.sha256()
