@@ -78,6 +78,8 @@ def _load():
                                    _i32, _dbl, _p, _p], _int),
             "oracle_paged_decode": ([_p, _p, _p, _p, _i64, _int, _int, _int, _p, _int, _p, _i32,
                                      _p, _i32, _i32, _dbl, _p], _int),
+            "oracle_copy_blocks": ([_p, _p, _p, _p, _i64, _p, _p, _p, _p, _i64, _int, _int,
+                                    _int, _p, _p, _i64], _i64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -217,6 +219,21 @@ def decode_one(pool: Pool, q_row: np.ndarray, q_dtype: str, bt_row: np.ndarray, 
     if rc != 0:
         raise ValueError(f"oracle_decode_one failed ({rc})")
     return out, probs[:seq_len]
+
+
+def copy_blocks(src: Pool, dst: Pool, src_ids: np.ndarray, dst_ids: np.ndarray) -> int:
+    """Copy whole blocks src_ids[i] of src to dst_ids[i] of dst, in order (LMDeploy
+    article §4.4, the cache engine's swap map). Returns the pairs skipped for an
+    id outside its pool."""
+    assert (src.kv_dtype, src.kv_heads, src.head_dim) == (dst.kv_dtype, dst.kv_heads,
+                                                          dst.head_dim)
+    si = np.ascontiguousarray(src_ids, dtype=np.int32)
+    di = np.ascontiguousarray(dst_ids, dtype=np.int32)
+    assert si.size == di.size
+    return int(_load().oracle_copy_blocks(
+        _ptr(src.k), _ptr(src.v), _ptr(src.k_sz), _ptr(src.v_sz), src.num_blocks,
+        _ptr(dst.k), _ptr(dst.v), _ptr(dst.k_sz), _ptr(dst.v_sz), dst.num_blocks,
+        src.kv_heads, src.head_dim, DTYPES[src.kv_dtype], _ptr(si), _ptr(di), si.size))
 
 
 def run_workload(wl, with_step: bool = True, pool: Optional[Pool] = None):

@@ -413,4 +413,39 @@ int oracle_paged_decode(const void* k_pool, const void* v_pool, const uint16_t* 
   return 0;
 }
 
+// Block copy / swap (LMDeploy article §4.4 "Block Manager 与缓存交换": a
+// swap map {dst: src} moves whole blocks between the GPU and CPU caches, K
+// and V alike). For i = 0 .. n-1 in order, block src_ids[i] of the source
+// pool is copied to block dst_ids[i] of the destination pool: its 16 rows of
+// K and of V for every kv head and, for quantized kinds, its (scale, zero)
+// pairs. Both pools have the same kind, kv heads and head_dim. A pair with an
+// id outside its pool is skipped and counted; the count is returned.
+int64_t oracle_copy_blocks(const void* src_k, const void* src_v, const uint16_t* src_k_sz,
+                           const uint16_t* src_v_sz, int64_t src_blocks, void* dst_k,
+                           void* dst_v, uint16_t* dst_k_sz, uint16_t* dst_v_sz,
+                           int64_t dst_blocks, int kv_heads, int head_dim, int kv_dtype,
+                           const int32_t* src_ids, const int32_t* dst_ids, int64_t n) {
+  const int64_t row_bytes = kv_dtype == 4 ? head_dim / 2 : (kv_dtype == 8 ? head_dim : 2 * head_dim);
+  const int64_t tile = 16 * kv_heads * row_bytes;  // bytes of one block of K (or V)
+  const int64_t pairs = static_cast<int64_t>(kv_heads) * 16 * 2;  // fp16 words of scale/zero
+  const bool quant = kv_dtype == 4 || kv_dtype == 8;
+  int64_t skipped = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t s = src_ids[i], d = dst_ids[i];
+    if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+      ++skipped;
+      continue;
+    }
+    std::memcpy(static_cast<uint8_t*>(dst_k) + d * tile,
+                static_cast<const uint8_t*>(src_k) + s * tile, tile);
+    std::memcpy(static_cast<uint8_t*>(dst_v) + d * tile,
+                static_cast<const uint8_t*>(src_v) + s * tile, tile);
+    if (quant) {
+      std::memcpy(dst_k_sz + d * pairs, src_k_sz + s * pairs, pairs * sizeof(uint16_t));
+      std::memcpy(dst_v_sz + d * pairs, src_v_sz + s * pairs, pairs * sizeof(uint16_t));
+    }
+  }
+  return skipped;
+}
+
 }  // extern "C"
