@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the block copy / swap measurement")
     p.add_argument("--shared-prefix", choices=["auto", "on", "off"], default="off",
                    help="decode shared prefixes once per group (auto: when the workload has one)")
     p.add_argument("--json-out", default="")
@@ -241,6 +243,61 @@ def copy_bandwidth_gbs(dev, n_bytes: int = 1 << 31, reps: int = 10) -> float:
         best = min(best, e0.elapsed_time(e1))
     del a, b
     return 2 * n_bytes / (best / 1e3) / 1e9
+
+
+def measure_block_copy(kvq, pool, wl, dev, peak: float, n_cow: int = 4096, n_swap: int = 1024,
+                       reps: int = 20) -> dict:
+    """kvq_copy_blocks on the workload's pool geometry: a copy-on-write of n_cow
+    random blocks into a second device pool (HBM read + write), and a swap out
+    / in of n_swap blocks through a pinned host pool, each against a plain
+    copy of the same bytes on the same path (torch copy_)."""
+    import torch
+
+    block_bytes = pool.nbytes() // pool.num_blocks
+    n_cow = min(n_cow, pool.num_blocks)
+    n_swap = min(n_swap, pool.num_blocks)
+    ids = torch.from_numpy(synthetic.permutation(wl.seed, 99, pool.num_blocks)
+                           .astype(np.int32)).to(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    out = {"block_bytes": block_bytes}
+    dst = kvq.KVPool.allocate(n_cow, wl.kv_heads, wl.kv_dtype, device=dev)
+    seq = torch.arange(n_cow, dtype=torch.int32, device=dev)
+    ms = timed(lambda: kvq.kvq_copy_blocks(pool, dst, ids[:n_cow], seq))
+    moved = 2 * n_cow * block_bytes  # read + write
+    out["cow"] = {"blocks": n_cow, "ms": round(ms, 4), "gbs": round(moved / ms / 1e6, 1),
+                  "frac_of_peak": round(moved / ms / 1e6 / peak, 4)}
+    del dst
+    host = kvq.KVPool.allocate(n_swap, wl.kv_heads, wl.kv_dtype, pinned=True)
+    seq = torch.arange(n_swap, dtype=torch.int32, device=dev)
+    nbytes = n_swap * block_bytes
+    ref_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ref_h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    for name, fn, ref in (
+            ("swap_out", lambda: kvq.kvq_copy_blocks(pool, host, ids[:n_swap], seq),
+             lambda: ref_h.copy_(ref_d, non_blocking=True)),
+            ("swap_in", lambda: kvq.kvq_copy_blocks(host, pool, seq, ids[:n_swap]),
+             lambda: ref_d.copy_(ref_h, non_blocking=True))):
+        if name == "swap_in":  # the blocks swapped out go back where they were
+            kvq.kvq_copy_blocks(pool, host, ids[:n_swap], seq)
+        ms = timed(fn)
+        ms_ref = timed(ref)
+        out[name] = {"blocks": n_swap, "ms": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1),
+                     "plain_copy_gbs": round(nbytes / ms_ref / 1e6, 1),
+                     "frac_of_plain_copy": round(ms_ref / ms, 4)}
+    del host, ref_d, ref_h
+    return out
 
 
 # ---- our arm ---------------------------------------------------------------------
@@ -458,6 +515,13 @@ def run_ours(args, rank: int, world: int, dist):
         "frac_of_this_gpu_copy": round(achieved / box_copy, 4),
     }
 
+    extras = None
+    if not args.no_extras:
+        extras = {"kvq_copy_blocks": measure_block_copy(kvq, pool, wl, dev, peak)}
+        bits = kvq.kvq_check_error(step.dev_err)
+        if bits:
+            raise RuntimeError(f"device error word {bits:#x} after the copy measurement")
+
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -472,6 +536,7 @@ def run_ours(args, rank: int, world: int, dist):
         "roofline": roofline, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "decode_hbm_gbs": round(achieved, 1),
+        "extras": extras,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, budget_s=20.0)

@@ -287,6 +287,27 @@ kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_
                                      void* stream);
 
 /*
+ * kvq_copy_blocks -- copy whole blocks from one pool to another (LMDeploy
+ * article §4.4: the cache engine swaps blocks between the GPU and the CPU
+ * cache by a {dst: src} map, K and V alike; inside one pool the same copy
+ * forks a shared block before a request writes into it).
+ *  src, dst : pools of the same kv_dtype, kv_heads and head_dim. Either may
+ *             be in pinned host memory the GPU can address (cudaHostAlloc,
+ *             torch pin_memory; under unified addressing the host pointers
+ *             are used as they are): a swap out or in is then this one call,
+ *             reading or writing host memory over the CPU-GPU link.
+ *  src_ids, dst_ids : int32 [n], device-addressable.
+ * For every i, block src_ids[i] of src is copied to block dst_ids[i] of dst:
+ * its K and V tiles (16 x kv_heads rows each) and, for INT8/INT4 pools, its
+ * K and V (scale, zero) pairs. The dst ids must be distinct and, when src and
+ * dst are the same pool, none of them may also be a src id (the pairs run in
+ * parallel). A pair with an id outside its pool is skipped and flagged
+ * KVQ_DEV_ERR_BLOCK_ID. Asynchronous on `stream`; allocates nothing.
+ */
+kvq_status kvq_copy_blocks(const kvq_pool* src, const kvq_pool* dst, const int32_t* src_ids,
+                           const int32_t* dst_ids, int64_t n, int32_t* dev_err, void* stream);
+
+/*
  * kvq_check_error -- synchronize `stream`, read the device error word and
  * clear it. Returns KVQ_OK if it was 0, KVQ_ERR_OUT_OF_RANGE otherwise (the
  * bits are stored to *bits_out when bits_out is not NULL), KVQ_ERR_CUDA if the

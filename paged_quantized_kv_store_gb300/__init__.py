@@ -62,7 +62,8 @@ class _Plan(ctypes.Structure):
 EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decode_attn_plan",
             "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
             "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc",
-            "paged_decode_attn_shared_prefix_workspace_size", "paged_decode_attn_shared_prefix"]
+            "paged_decode_attn_shared_prefix_workspace_size", "paged_decode_attn_shared_prefix",
+            "kvq_copy_blocks"]
 
 
 def load(build_if_missing: bool = False):
@@ -100,6 +101,8 @@ def load(build_if_missing: bool = False):
                                                     I32, I32, I32, F, P, P, P, I32, I32, I32,
                                                     I32, P, SZ, P, P]
     lib.paged_decode_attn_shared_prefix.restype = ctypes.c_int
+    lib.kvq_copy_blocks.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), P, P, I64, P, P]
+    lib.kvq_copy_blocks.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.kvq_check_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -148,18 +151,21 @@ class KVPool:
 
     @staticmethod
     def allocate(num_blocks: int, kv_heads: int, kv_dtype: str, device="cuda",
-                 head_dim: int = HEAD_DIM) -> "KVPool":
-        """Zero-filled pool tensors (allocation is the caller's side of the ABI)."""
+                 head_dim: int = HEAD_DIM, pinned: bool = False) -> "KVPool":
+        """Zero-filled pool tensors (allocation is the caller's side of the ABI).
+        pinned: a host pool in page-locked memory the GPU addresses directly
+        (the swap target of kvq_copy_blocks)."""
         import torch
         row = {"f16": 2 * head_dim, "bf16": 2 * head_dim, "int8": head_dim,
                "int4": head_dim // 2}[kv_dtype]
         shape = (num_blocks, BLOCK_SIZE, kv_heads, row)
-        k = torch.zeros(shape, dtype=torch.uint8, device=device)
-        v = torch.zeros(shape, dtype=torch.uint8, device=device)
+        kw = dict(device="cpu", pin_memory=True) if pinned else dict(device=device)
+        k = torch.zeros(shape, dtype=torch.uint8, **kw)
+        v = torch.zeros(shape, dtype=torch.uint8, **kw)
         if kv_dtype in ("int8", "int4"):
             szs = (num_blocks, kv_heads, BLOCK_SIZE)
-            k_sz = torch.zeros(szs, dtype=torch.int32, device=device)
-            v_sz = torch.zeros(szs, dtype=torch.int32, device=device)
+            k_sz = torch.zeros(szs, dtype=torch.int32, **kw)
+            v_sz = torch.zeros(szs, dtype=torch.int32, **kw)
         else:
             k_sz = v_sz = None
         return KVPool(k, v, k_sz, v_sz, num_blocks, kv_heads, kv_dtype, head_dim)
@@ -348,6 +354,19 @@ def paged_decode_attn_shared_prefix(pool: KVPool, q, out, block_tables, seq_lens
         groups.num_groups, groups.num_members, int(groups.max_shared_blocks), int(num_splits),
         _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
     _check(st, "paged_decode_attn_shared_prefix")
+
+
+def kvq_copy_blocks(src: KVPool, dst: KVPool, src_ids, dst_ids, dev_err=None, stream=None):
+    """Copy blocks src_ids[i] of src to dst_ids[i] of dst (int32 tensors the GPU
+    can address); either pool may be in pinned host memory. See kvq.h."""
+    lib = load()
+    sp, dp = src.c_struct(), dst.c_struct()
+    n = int(src_ids.numel())
+    if int(dst_ids.numel()) != n:
+        raise ValueError("src_ids and dst_ids differ in length")
+    st = lib.kvq_copy_blocks(ctypes.byref(sp), ctypes.byref(dp), _ptr(src_ids), _ptr(dst_ids), n,
+                             _ptr(dev_err), _stream(stream))
+    _check(st, "kvq_copy_blocks")
 
 
 def kvq_check_error(dev_err, stream=None) -> int:

@@ -367,6 +367,38 @@ kvq_status paged_decode_attn_shared_prefix(
                      workspace_bytes, dev_err, stream);
 }
 
+kvq_status kvq_copy_blocks(const kvq_pool* src, const kvq_pool* dst, const int32_t* src_ids,
+                           const int32_t* dst_ids, int64_t n, int32_t* dev_err, void* stream) {
+  kvq_status st = check_pool(src);
+  if (st != KVQ_OK) return st;
+  st = check_pool(dst);
+  if (st != KVQ_OK) return st;
+  if (src->kv_dtype != dst->kv_dtype || src->kv_heads != dst->kv_heads) return KVQ_ERR_INVALID_ARG;
+  if (n < 0) return KVQ_ERR_INVALID_ARG;
+  if (n == 0) return KVQ_OK;
+  if (src_ids == nullptr || dst_ids == nullptr) return KVQ_ERR_INVALID_ARG;
+  const int row = is_quant(src->kv_dtype) ? (src->kv_dtype == KVQ_INT8 ? kHeadDim : kHeadDim / 2)
+                                          : 2 * kHeadDim;
+  kvq::CopyArgs a;
+  a.src_k = static_cast<const uint4*>(src->k);
+  a.src_v = static_cast<const uint4*>(src->v);
+  a.src_k_sz = static_cast<const uint4*>(src->k_sz);
+  a.src_v_sz = static_cast<const uint4*>(src->v_sz);
+  a.dst_k = static_cast<uint4*>(dst->k);
+  a.dst_v = static_cast<uint4*>(dst->v);
+  a.dst_k_sz = static_cast<uint4*>(dst->k_sz);
+  a.dst_v_sz = static_cast<uint4*>(dst->v_sz);
+  a.src_blocks = src->num_blocks;
+  a.dst_blocks = dst->num_blocks;
+  a.tile_chunks = static_cast<int64_t>(kBlock) * src->kv_heads * row / 16;
+  a.sz_chunks = is_quant(src->kv_dtype) ? static_cast<int64_t>(src->kv_heads) * kBlock * 4 / 16 : 0;
+  a.src_ids = src_ids;
+  a.dst_ids = dst_ids;
+  a.dev_err = dev_err;
+  return kvq::launch_copy(a, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK
+                                                                                  : KVQ_ERR_CUDA;
+}
+
 kvq_status kvq_check_error(int32_t* dev_err, uint32_t* bits_out, void* stream) {
   if (dev_err == nullptr) return KVQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

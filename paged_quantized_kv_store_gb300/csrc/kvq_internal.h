@@ -86,7 +86,26 @@ struct DecodeArgs {
   float* ppart;               // [batch][q_heads][pmax_chunks][kPartStride]
 };
 
+struct CopyArgs {
+  const uint4* src_k;
+  const uint4* src_v;
+  const uint4* src_k_sz;  // null for 16-bit pools (sz_chunks = 0)
+  const uint4* src_v_sz;
+  uint4* dst_k;
+  uint4* dst_v;
+  uint4* dst_k_sz;
+  uint4* dst_v_sz;
+  int64_t src_blocks;
+  int64_t dst_blocks;
+  int64_t tile_chunks;  // 16-byte chunks of one block's K (or V) tile
+  int64_t sz_chunks;    // 16-byte chunks of one block's K (or V) scale/zero run
+  const int32_t* src_ids;
+  const int32_t* dst_ids;
+  int32_t* dev_err;
+};
+
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+cudaError_t launch_copy(const CopyArgs& a, int64_t n, cudaStream_t s);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
 // kv_dtype / q_dtype select the template instance
 cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid_ctas,

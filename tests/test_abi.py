@@ -184,3 +184,16 @@ def test_shared_prefix_group_detection():
     assert g2.members.tolist() == [0, 1, 2, 4] and g2.shared_blocks.tolist() == [2]
     e = kvq.SharedPrefixGroups.from_lists([], device="cpu")
     assert e.num_groups == 0 and e.num_members == 0 and e.max_shared_blocks == 0
+
+
+def test_copy_blocks_validation(lib):
+    f = lib.kvq_copy_blocks
+    p = 256
+    a, b = _pool(), _pool(num_blocks=9)
+    assert f(ctypes.byref(a), ctypes.byref(b), p, p, 0, None, None) == 0   # nothing to do
+    assert f(ctypes.byref(a), ctypes.byref(b), p, p, -1, None, None) == 1
+    assert f(ctypes.byref(a), ctypes.byref(b), None, p, 3, None, None) == 1
+    assert f(ctypes.byref(a), ctypes.byref(_pool(kv_dtype=kvq.KVQ_INT4)), p, p, 3, None,
+             None) == 1  # different kinds
+    assert f(ctypes.byref(a), ctypes.byref(_pool(kv_heads=4)), p, p, 3, None, None) == 1
+    assert f(None, ctypes.byref(b), p, p, 3, None, None) == 1
