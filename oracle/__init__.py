@@ -80,6 +80,8 @@ def _load():
                                      _p, _i32, _i32, _dbl, _p], _int),
             "oracle_copy_blocks": ([_p, _p, _p, _p, _i64, _p, _p, _p, _p, _i64, _int, _int,
                                     _int, _p, _p, _i64], _i64),
+            "oracle_paged_extend": ([_p, _p, _p, _p, _i64, _int, _int, _int, _p, _int, _p, _p,
+                                     _i32, _p, _i32, _i32, _dbl, _p], _int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -219,6 +221,26 @@ def decode_one(pool: Pool, q_row: np.ndarray, q_dtype: str, bt_row: np.ndarray, 
     if rc != 0:
         raise ValueError(f"oracle_decode_one failed ({rc})")
     return out, probs[:seq_len]
+
+
+def paged_extend(pool: Pool, q: np.ndarray, q_dtype: str, qo_indptr: np.ndarray,
+                 block_tables_: np.ndarray, kv_lens: np.ndarray, sm_scale: float) -> np.ndarray:
+    """fp64 extend (chunked prefill) attention [total_q, Hq, D]: chunk query i of
+    request b sits at position kv_lens[b] - C_b + i and attends positions 0 ..
+    that position through the block table ("pymllm Runtime Design", forward
+    stage, extend; LMDeploy article §2.3, prefills split into chunks)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    qi = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables_, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    T, Hq, D = q.shape
+    assert qi.size == kl.size + 1 and qi[-1] == T
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    rc = _load().oracle_paged_extend(*pool._args(), _ptr(q), DTYPES[q_dtype], _ptr(qi), _ptr(bt),
+                                     bt.shape[1], _ptr(kl), kl.size, Hq, sm_scale, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_extend failed ({rc})")
+    return out
 
 
 def copy_blocks(src: Pool, dst: Pool, src_ids: np.ndarray, dst_ids: np.ndarray) -> int:

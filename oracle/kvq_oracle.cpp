@@ -413,6 +413,44 @@ int oracle_paged_decode(const void* k_pool, const void* v_pool, const uint16_t* 
   return 0;
 }
 
+// Extend (chunked prefill) attention: "pymllm Runtime Design", forward stage
+// (an extend / prefill batch writes its prompt tokens to the KV cache and
+// attends over them); LMDeploy article §2.3 "动态拆分与融合" (a prefill longer
+// than the 4096-token threshold is split into chunks prefilled in turn). Request b has kv_lens[b] tokens in the pool, the last
+// C_b = qo_indptr[b + 1] - qo_indptr[b] of them being the chunk whose
+// queries are q rows qo_indptr[b] .. qo_indptr[b + 1] - 1. Chunk query i sits
+// at position kv_lens[b] - C_b + i and attends positions 0 .. that position
+// (causal): the plain paged attention of that row with seq_len = position + 1.
+// q, out: [total_q, Hq, D]. Returns 0, or the first nonzero code of
+// decode_one, or -3 on a chunk longer than its request.
+int oracle_paged_extend(const void* k_pool, const void* v_pool, const uint16_t* k_sz,
+                        const uint16_t* v_sz, int64_t num_blocks, int kv_heads, int head_dim,
+                        int kv_dtype, const uint16_t* q, int q_dtype, const int32_t* qo_indptr,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* kv_lens, int32_t batch, int32_t q_heads, double sm_scale,
+                        double* out) {
+  if (q_heads % kv_heads != 0) return -2;
+  const int group = q_heads / kv_heads;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t c = qo_indptr[b + 1] - qo_indptr[b];
+    if (c > kv_lens[b]) return -3;
+    for (int32_t i = 0; i < c; ++i) {
+      const int32_t pos = kv_lens[b] - c + i;
+      const int64_t r = qo_indptr[b] + i;
+      for (int h = 0; h < q_heads; ++h) {
+        const int64_t row = r * q_heads + h;
+        const int rc = oracle_decode_one(
+            k_pool, v_pool, k_sz, v_sz, num_blocks, kv_heads, head_dim, kv_dtype,
+            q + row * head_dim, q_dtype,
+            block_tables + static_cast<int64_t>(b) * max_blocks_per_seq, pos + 1, h / group,
+            sm_scale, out + row * head_dim, nullptr);
+        if (rc != 0) return rc;
+      }
+    }
+  }
+  return 0;
+}
+
 // Block copy / swap (LMDeploy article §4.4 "Block Manager 与缓存交换": a
 // swap map {dst: src} moves whole blocks between the GPU and CPU caches, K
 // and V alike). For i = 0 .. n-1 in order, block src_ids[i] of the source

@@ -48,6 +48,7 @@ _POS_STRIDE = 1 << 14
 # generator streams
 S_Q, S_K_CTX, S_V_CTX, S_K_PREFIX, S_V_PREFIX, S_K_CHUNK, S_V_CHUNK = 1, 2, 3, 4, 5, 6, 7
 S_LENS, S_PERM, S_OUT_K, S_OUT_V, S_FREE, S_REQSLOT = 16, 17, 18, 19, 20, 21
+S_Q_EXT = 22
 
 _DT = {"f32": 0, "f16": 1, "bf16": 2}
 
@@ -472,6 +473,57 @@ def shared_prefix(name: str, kv_dtype: str, lens, q_heads: int, kv_heads: int,
                    shared_tokens=(k * BLOCK_SIZE).astype(np.int32), prefix_blocks=pfx,
                    description=f"{kv_dtype} KV, {q_heads}q/{kv_heads}kv, {len(lens)} requests, "
                                f"shared {prefix_blocks}-block prefix")
+
+
+@dataclass
+class ExtendWorkload:
+    """Chunked-prefill (extend) attention input: the pool holds kv_lens[b]
+    tokens of request b (its prefix, then its chunk, stored like a decode
+    workload's context), and the last chunk_lens[b] of them have queries,
+    packed as rows qo_indptr[b] .. qo_indptr[b + 1] - 1 of q_ext()."""
+
+    wl: Workload
+    chunk_lens: np.ndarray
+
+    @property
+    def qo_indptr(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk_lens)]).astype(np.int32)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.chunk_lens.sum())
+
+    @property
+    def kv_lens(self) -> np.ndarray:
+        return self.wl.seq_lens
+
+    def q_ext(self) -> np.ndarray:
+        """Queries as uint16 [total_q, Hq, D] (dtype q_dtype)."""
+        w = self.wl
+        n = self.total_q * w.q_heads * w.head_dim
+        return normal(w.seed, S_Q_EXT, 0, n, w.value_scale, None,
+                      w.q_dtype).reshape(self.total_q, w.q_heads, w.head_dim)
+
+
+def extend(name: str, kv_dtype: str, kv_lens, chunk_lens, q_heads: int, kv_heads: int,
+           seed: int = 31, in_dtype: str = "f16", q_dtype: Optional[str] = None,
+           outliers: bool = False) -> ExtendWorkload:
+    """Requests with kv_lens[b] tokens in the pool whose last chunk_lens[b]
+    tokens are the chunk being prefilled (chunk_lens[b] == kv_lens[b]: a fresh
+    prefill; < kv_lens[b]: an extend over a cached prefix)."""
+    kv_lens = np.asarray(kv_lens, dtype=np.int32)
+    chunk_lens = np.asarray(chunk_lens, dtype=np.int32)
+    assert kv_lens.shape == chunk_lens.shape and (chunk_lens <= kv_lens).all()
+    wl = custom(name, kv_dtype, kv_lens, q_heads, kv_heads, seed=seed, in_dtype=in_dtype,
+                q_dtype=q_dtype, outliers=outliers)
+    return ExtendWorkload(wl, chunk_lens)
+
+
+def cfg5_prefill(seed: int = 4, chunk: int = 4096) -> ExtendWorkload:
+    """The mixed step's prefill chunk on its own: one fresh 4096-token prompt
+    chunk (max_prefill_token_num) over INT8 KV, GQA 32q/8kv, attended
+    causally after it is stored."""
+    return extend("cfg5_prefill", "int8", [chunk], [chunk], 32, 8, seed=seed)
 
 
 def by_name(name: str, **kw) -> Workload:
