@@ -287,6 +287,46 @@ kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_
                                      void* stream);
 
 /*
+ * paged_extend_attn -- extend (chunked prefill) attention over the paged pool
+ * ("pymllm Runtime Design", forward stage: an extend / prefill batch writes
+ * its prompt tokens to the KV cache and attends over them; LMDeploy article
+ * §2.3: a prefill longer than the 4096-token threshold is split into chunks
+ * prefilled in turn). The chunk's K/V rows are stored first (kv_store_quant);
+ * every query then reads the request's K/V through its block table,
+ * dequantized in registers.
+ *  q, out      : [total_q, q_heads, head_dim] of q_dtype (KVQ_F16/KVQ_BF16;
+ *                equal to the pool dtype for F16/BF16 pools), 16-byte aligned.
+ *  qo_indptr   : device int32 [batch + 1], non-decreasing, qo_indptr[0] = 0,
+ *                qo_indptr[batch] = total_q: request b's chunk queries are
+ *                rows qo_indptr[b] .. qo_indptr[b + 1] - 1.
+ *  kv_lens     : device int32 [batch]: tokens of request b in the pool, its
+ *                chunk included (kv_lens[b] >= its chunk length).
+ *  block_tables: [batch, max_blocks_per_seq] int32 physical block ids.
+ *  max_kv_len  : host upper bound of kv_lens (sizes the plan); a longer
+ *                request is skipped and flagged KVQ_DEV_ERR_LENGTH.
+ *  workspace   : at least *bytes of paged_extend_attn_workspace_size, 16-byte
+ *                aligned; nothing in it needs to start at zero.
+ * Chunk query i of request b (chunk length C) sits at position
+ * kv_lens[b] - C + i and attends positions 0 .. that position:
+ *   out[row][h] = sum_t softmax_t(sm_scale * q . k_t) v_t, t <= position,
+ * fp32 accumulation, rounded once to q_dtype. A request whose rows fall
+ * outside [0, total_q), whose chunk is longer than its context or whose
+ * context exceeds the table is skipped and flagged KVQ_DEV_ERR_LENGTH (its
+ * rows are not written); block ids outside the pool are skipped and flagged
+ * KVQ_DEV_ERR_BLOCK_ID.
+ */
+kvq_status paged_extend_attn_workspace_size(int32_t batch, int32_t total_q, int32_t q_heads,
+                                            int32_t kv_heads, int32_t head_dim,
+                                            int32_t max_kv_len, size_t* bytes);
+
+kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
+                             const int32_t* qo_indptr, const int32_t* kv_lens,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             int32_t batch, int32_t total_q, int32_t q_heads, int32_t max_kv_len,
+                             float sm_scale, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_err, void* stream);
+
+/*
  * kvq_copy_blocks -- copy whole blocks from one pool to another (LMDeploy
  * article §4.4: the cache engine swaps blocks between the GPU and the CPU
  * cache by a {dst: src} map, K and V alike; inside one pool the same copy

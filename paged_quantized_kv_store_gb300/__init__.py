@@ -63,7 +63,7 @@ EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decod
             "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
             "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc",
             "paged_decode_attn_shared_prefix_workspace_size", "paged_decode_attn_shared_prefix",
-            "kvq_copy_blocks"]
+            "kvq_copy_blocks", "paged_extend_attn_workspace_size", "paged_extend_attn"]
 
 
 def load(build_if_missing: bool = False):
@@ -101,6 +101,12 @@ def load(build_if_missing: bool = False):
                                                     I32, I32, I32, F, P, P, P, I32, I32, I32,
                                                     I32, P, SZ, P, P]
     lib.paged_decode_attn_shared_prefix.restype = ctypes.c_int
+    lib.paged_extend_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32,
+                                                     ctypes.POINTER(SZ)]
+    lib.paged_extend_attn_workspace_size.restype = ctypes.c_int
+    lib.paged_extend_attn.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, P, P, I32, I32, I32,
+                                      I32, I32, F, P, SZ, P, P]
+    lib.paged_extend_attn.restype = ctypes.c_int
     lib.kvq_copy_blocks.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), P, P, I64, P, P]
     lib.kvq_copy_blocks.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -354,6 +360,31 @@ def paged_decode_attn_shared_prefix(pool: KVPool, q, out, block_tables, seq_lens
         groups.num_groups, groups.num_members, int(groups.max_shared_blocks), int(num_splits),
         _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
     _check(st, "paged_decode_attn_shared_prefix")
+
+
+def paged_extend_attn_workspace_size(batch, total_q, q_heads, kv_heads, max_kv_len,
+                                     head_dim=HEAD_DIM) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().paged_extend_attn_workspace_size(batch, total_q, q_heads, kv_heads, head_dim,
+                                                 max_kv_len, ctypes.byref(n))
+    _check(st, "paged_extend_attn_workspace_size")
+    return int(n.value)
+
+
+def paged_extend_attn(pool: KVPool, q, out, qo_indptr, kv_lens, block_tables, max_kv_len,
+                      sm_scale, workspace=None, dev_err=None, stream=None):
+    """Extend (chunked prefill) attention: q rows qo_indptr[b]..qo_indptr[b+1]-1
+    are the last tokens of request b and attend causally; see kvq.h."""
+    lib = load()
+    ps = pool.c_struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.paged_extend_attn(ctypes.byref(ps), _ptr(q), _dtype_code(q), _ptr(out),
+                               _ptr(qo_indptr), _ptr(kv_lens), _ptr(block_tables),
+                               int(block_tables.shape[1]), int(kv_lens.numel()),
+                               int(q.shape[0]), int(q.shape[1]), int(max_kv_len),
+                               float(sm_scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
+                               _stream(stream))
+    _check(st, "paged_extend_attn")
 
 
 def kvq_copy_blocks(src: KVPool, dst: KVPool, src_ids, dst_ids, dev_err=None, stream=None):

@@ -219,6 +219,41 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   return KVQ_OK;
 }
 
+// Launch plan of an extend call: the context is cut into parts of pchunk
+// blocks only when the batch has too few 16-row tiles to keep every warp
+// busy (a short chunk over a long prefix); the workspace holds the work
+// counter and, then, the parts' records.
+struct ExtendPlan {
+  int pchunk, max_splits;
+  size_t part_off, total;
+};
+
+ExtendPlan extend_plan(int batch, int total_q, int q_heads, int kv_heads, int max_kv_len,
+                       int num_sms) {
+  ExtendPlan p;
+  const int group = q_heads / kv_heads;
+  const int64_t units = static_cast<int64_t>(kv_heads) *
+                        ((static_cast<int64_t>(total_q) * group + 15) / 16 + batch);
+  const int64_t warps = static_cast<int64_t>(num_sms) * 3 * (kvq::kDecodeThreads / 32);
+  const int nblk = std::max(1, (max_kv_len + kBlock - 1) / kBlock);
+  p.pchunk = 0;
+  p.max_splits = 1;
+  if (units < 2 * warps) {
+    const int want = static_cast<int>(std::min<int64_t>(32, (2 * warps + units - 1) / units));
+    const int chunk = std::max(8, (nblk + want - 1) / want);
+    const int splits = (nblk + chunk - 1) / chunk;
+    if (splits > 1) {
+      p.pchunk = chunk;
+      p.max_splits = splits;
+    }
+  }
+  p.part_off = 256;  // the work counter
+  p.total = p.part_off + (p.pchunk > 0 ? static_cast<size_t>(total_q) * q_heads * p.max_splits *
+                                             kvq::kPartStride * sizeof(float)
+                                       : 0);
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -365,6 +400,86 @@ kvq_status paged_decode_attn_shared_prefix(
   return decode_impl(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens, batch,
                      q_heads, max_seq_len, sm_scale, num_splits, &pd, workspace,
                      workspace_bytes, dev_err, stream);
+}
+
+kvq_status paged_extend_attn_workspace_size(int32_t batch, int32_t total_q, int32_t q_heads,
+                                            int32_t kv_heads, int32_t head_dim,
+                                            int32_t max_kv_len, size_t* bytes) {
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (batch < 0 || total_q < 0 || q_heads <= 0 || kv_heads <= 0 || max_kv_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (q_heads % kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  const int sms = current_sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  *bytes = extend_plan(batch, total_q, q_heads, kv_heads, max_kv_len, sms).total;
+  return KVQ_OK;
+}
+
+kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
+                             const int32_t* qo_indptr, const int32_t* kv_lens,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             int32_t batch, int32_t total_q, int32_t q_heads, int32_t max_kv_len,
+                             float sm_scale, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_err, void* stream) {
+  const kvq_status ps = check_pool(pool);
+  if (ps != KVQ_OK) return ps;
+  if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (is_float16(pool->kv_dtype) && q_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
+  if (batch < 0 || total_q < 0 || q_heads <= 0 || max_blocks_per_seq <= 0 || max_kv_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (batch > kvq::kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0) return KVQ_OK;
+  if (q == nullptr || out == nullptr || qo_indptr == nullptr || kv_lens == nullptr ||
+      block_tables == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  const ExtendPlan plan =
+      extend_plan(batch, total_q, q_heads, pool->kv_heads, max_kv_len, sms);
+  if (workspace == nullptr || workspace_bytes < plan.total) return KVQ_ERR_WORKSPACE;
+  kvq::ExtendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (pool->kv_dtype == KVQ_INT8) {
+    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
+        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
+      return KVQ_ERR_CUDA;
+  }
+  a.k = static_cast<const uint8_t*>(pool->k);
+  a.v = static_cast<const uint8_t*>(pool->v);
+  a.k_sz = static_cast<const uint32_t*>(pool->k_sz);
+  a.v_sz = static_cast<const uint32_t*>(pool->v_sz);
+  a.num_blocks = pool->num_blocks;
+  a.kv_heads = pool->kv_heads;
+  a.q = q;
+  a.out = out;
+  a.qo_indptr = qo_indptr;
+  a.kv_lens = kv_lens;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.batch = batch;
+  a.q_heads = q_heads;
+  a.group = q_heads / pool->kv_heads;
+  a.total_q = total_q;
+  a.pchunk = plan.pchunk;
+  a.max_splits = plan.max_splits;
+  a.len_cap = std::min(max_blocks_per_seq, std::max(1, (max_kv_len + kBlock - 1) / kBlock)) *
+              kBlock;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.counter = static_cast<int32_t*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.part_off);
+  a.dev_err = dev_err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(a.counter, 0, sizeof(int32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  const int per_sm = kvq::extend_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
+  if (per_sm <= 0) return KVQ_ERR_CUDA;
+  return kvq::launch_extend(a, pool->kv_dtype, q_dtype, sms * per_sm, s) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
 
 kvq_status kvq_copy_blocks(const kvq_pool* src, const kvq_pool* dst, const int32_t* src_ids,

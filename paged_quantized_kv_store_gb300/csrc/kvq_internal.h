@@ -104,7 +104,38 @@ struct CopyArgs {
   int32_t* dev_err;
 };
 
+struct ExtendArgs {
+  CUtensorMap k_map;  // as in DecodeArgs (INT8 pools)
+  CUtensorMap v_map;
+  const uint8_t* k;
+  const uint8_t* v;
+  const uint32_t* k_sz;
+  const uint32_t* v_sz;
+  int64_t num_blocks;
+  int kv_heads;
+  const void* q;               // [total_q, Hq, D]
+  void* out;                   // [total_q, Hq, D]
+  const int32_t* qo_indptr;    // [batch + 1]
+  const int32_t* kv_lens;      // [batch]
+  const int32_t* block_tables;
+  int max_blocks;
+  int batch;
+  int q_heads;
+  int group;                   // q_heads / kv_heads
+  int total_q;
+  int pchunk;                  // blocks per work unit along the context (split), or 0: none
+  int max_splits;              // records per (query row, q head) when split
+  int len_cap;                 // longest context accepted (tokens)
+  float sm_scale_log2;
+  int32_t* counter;            // work counter (zero at launch)
+  float* part;                 // [total_q][Hq][max_splits][kPartStride] when split
+  int32_t* dev_err;
+};
+
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+cudaError_t launch_extend(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
+                          cudaStream_t s);
+int extend_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
 cudaError_t launch_copy(const CopyArgs& a, int64_t n, cudaStream_t s);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
 // kv_dtype / q_dtype select the template instance

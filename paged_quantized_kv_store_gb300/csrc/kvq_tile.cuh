@@ -228,8 +228,8 @@ struct LaneMap {
 // region `wr` (shared address). TMA path: lane 0 arms the stage's barrier and
 // issues two tile copies and two 64-byte scale/zero copies. cp.async path:
 // every lane copies its chunks; the caller commits the group.
-template <int KV>
-__device__ __forceinline__ void issue_block(uint32_t wr, int st, const DecodeArgs& a,
+template <int KV, class Args>
+__device__ __forceinline__ void issue_block(uint32_t wr, int st, const Args& a,
                                             const LaneMap<KV>& lm, int64_t phys, int h,
                                             int lane) {
   using S = Stage<KV>;

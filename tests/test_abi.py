@@ -197,3 +197,27 @@ def test_copy_blocks_validation(lib):
              None) == 1  # different kinds
     assert f(ctypes.byref(a), ctypes.byref(_pool(kv_heads=4)), p, p, 3, None, None) == 1
     assert f(None, ctypes.byref(b), p, p, 3, None, None) == 1
+
+
+def test_extend_validation(lib):
+    f = lib.paged_extend_attn
+    p = 256
+    args = dict(q=p, q_dtype=0, out=p, qo=p, kl=p, bt=p, mb=4, batch=2, tq=8, hq=4, mkl=64,
+                scale=0.1, ws=p, wsb=1 << 20, err=None, s=None)
+
+    def call(pool=None, **kw):
+        a = dict(args)
+        a.update(kw)
+        return f(ctypes.byref(pool or _pool()), a["q"], a["q_dtype"], a["out"], a["qo"],
+                 a["kl"], a["bt"], a["mb"], a["batch"], a["tq"], a["hq"], a["mkl"], a["scale"],
+                 a["ws"], a["wsb"], a["err"], a["s"])
+
+    assert call(batch=-1) == 1
+    assert call(tq=-1) == 1
+    assert call(hq=3) == 1                 # not a multiple of kv heads
+    assert call(q_dtype=kvq.KVQ_INT8) == 2
+    assert call(pool=_pool(kv_dtype=kvq.KVQ_F16), q_dtype=kvq.KVQ_BF16) == 2
+    assert call(scale=float("nan")) == 1
+    assert call(batch=0) == 0 and call(tq=0) == 0
+    assert call(qo=None) == 1
+    assert call(q=p + 8) == 1              # misaligned
