@@ -300,6 +300,90 @@ def measure_block_copy(kvq, pool, wl, dev, peak: float, n_cow: int = 4096, n_swa
     return out
 
 
+def measured_tensor_peak():
+    """(bf16 dense TFLOP/s burst, where it came from)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        if v > 0:
+            return v, "measured"
+    except (OSError, KeyError, ValueError, TypeError):
+        pass
+    return 1900.0, "fallback"
+
+
+def measure_extend(kvq, dev, reps: int = 10) -> dict:
+    """paged_extend_attn on the mixed step's prefill chunk alone: one fresh
+    4096-token prompt chunk over INT8 KV (GQA 32q/8kv), stored, then attended
+    causally. FLOPs: 4 * head_dim * q_heads * sum over queries of (position + 1);
+    the products run on fp16 tensor cores (mma.sync), against the measured
+    bf16 dense peak. torch's causal scaled_dot_product_attention on the same
+    shapes (K/V dequantized to fp16, heads expanded) is timed for context."""
+    import torch
+
+    ew = synthetic.cfg5_prefill()
+    wl = ew.wl
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+    def to_dev(bits, dt):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt[dt]).to(dev)
+
+    pool = kvq.KVPool.allocate(wl.num_blocks, wl.kv_heads, wl.kv_dtype, device=dev)
+    for slots, k, v in wl.setup_chunks():
+        kvq.kv_store_quant(pool, to_dev(k, wl.in_dtype), to_dev(v, wl.in_dtype),
+                           torch.from_numpy(slots).to(dev))
+    slots, k, v = wl.step_store()
+    kvq.kv_store_quant(pool, to_dev(k, wl.in_dtype), to_dev(v, wl.in_dtype),
+                       torch.from_numpy(slots).to(dev))
+    q = to_dev(ew.q_ext(), wl.q_dtype)
+    out = torch.empty_like(q)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    qo, kl, bt = i32(ew.qo_indptr), i32(ew.kv_lens), i32(wl.block_tables)
+    ws = torch.empty(max(kvq.paged_extend_attn_workspace_size(
+        wl.batch, ew.total_q, wl.q_heads, wl.kv_heads, wl.max_seq_len), 16),
+        dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    C = ew.total_q
+    flops = 4.0 * wl.head_dim * wl.q_heads * (C * (C + 1) / 2)
+    peak, kind = measured_tensor_peak()
+    res = {"workload": f"prefill chunk of {C} tokens, INT8 KV, GQA {wl.q_heads}q/{wl.kv_heads}kv",
+           "flops_per_launch": flops, "peak_tflops": peak,
+           "peak_kind": f"{kind} (bf16_tflops)", "default_variant": "tcgen05"}
+    for variant in ("tcgen05", "mma_sync"):
+        ms = timed(lambda: kvq.paged_extend_attn(pool, q, out, qo, kl, bt, wl.max_seq_len,
+                                                 wl.sm_scale, ws, err, variant=variant))
+        if kvq.kvq_check_error(err):
+            raise RuntimeError("device error word set by the extend measurement")
+        res[variant] = {"ms": round(ms, 4), "tflops": round(flops / ms / 1e9, 1),
+                        "frac": round(flops / ms / 1e9 / peak, 4)}
+    # context: the library's causal attention on dequantized fp16 K/V, same shapes
+    try:
+        import torch.nn.functional as F
+        kd = torch.randn(1, wl.q_heads, C, wl.head_dim, dtype=torch.float16, device=dev)
+        vd = torch.randn_like(kd)
+        qd = q.view(1, C, wl.q_heads, wl.head_dim).transpose(1, 2).to(torch.float16)
+        ms_ref = timed(lambda: F.scaled_dot_product_attention(qd, kd, vd, is_causal=True))
+        res["torch_sdpa_fp16_ms"] = round(ms_ref, 4)
+        res["torch_sdpa_fp16_tflops"] = round(flops / ms_ref / 1e9, 1)
+    except Exception as e:  # noqa: BLE001 - context only
+        res["torch_sdpa_fp16"] = f"not measured: {e}"
+    del pool, ws
+    return res
+
+
 # ---- our arm ---------------------------------------------------------------------
 
 def run_ours(args, rank: int, world: int, dist):
@@ -517,7 +601,8 @@ def run_ours(args, rank: int, world: int, dist):
 
     extras = None
     if not args.no_extras:
-        extras = {"kvq_copy_blocks": measure_block_copy(kvq, pool, wl, dev, peak)}
+        extras = {"kvq_copy_blocks": measure_block_copy(kvq, pool, wl, dev, peak),
+                  "paged_extend_attn": measure_extend(kvq, dev)}
         bits = kvq.kvq_check_error(step.dev_err)
         if bits:
             raise RuntimeError(f"device error word {bits:#x} after the copy measurement")

@@ -304,6 +304,14 @@ kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_
  *  block_tables: [batch, max_blocks_per_seq] int32 physical block ids.
  *  max_kv_len  : host upper bound of kv_lens (sizes the plan); a longer
  *                request is skipped and flagged KVQ_DEV_ERR_LENGTH.
+ *  variant     : KVQ_EXTEND_AUTO, or a kernel to use:
+ *                KVQ_EXTEND_MMA_SYNC (tiles of 16 rows on mma.sync; every pool
+ *                kind; cuts long contexts into parts when the batch has few
+ *                query tiles) or KVQ_EXTEND_TCGEN05 (tiles of 128 rows on
+ *                tcgen05 with tensor-memory accumulators; INT8, INT4 and
+ *                fp16 pools; KVQ_ERR_UNSUPPORTED otherwise). AUTO takes the
+ *                tcgen05 kernel when the pool allows it and the batch has at
+ *                least as many 128-row tiles as the device has SMs.
  *  workspace   : at least *bytes of paged_extend_attn_workspace_size, 16-byte
  *                aligned; nothing in it needs to start at zero.
  * Chunk query i of request b (chunk length C) sits at position
@@ -315,6 +323,10 @@ kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_
  * rows are not written); block ids outside the pool are skipped and flagged
  * KVQ_DEV_ERR_BLOCK_ID.
  */
+#define KVQ_EXTEND_AUTO 0
+#define KVQ_EXTEND_MMA_SYNC 1
+#define KVQ_EXTEND_TCGEN05 2
+
 kvq_status paged_extend_attn_workspace_size(int32_t batch, int32_t total_q, int32_t q_heads,
                                             int32_t kv_heads, int32_t head_dim,
                                             int32_t max_kv_len, size_t* bytes);
@@ -323,8 +335,8 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              const int32_t* qo_indptr, const int32_t* kv_lens,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              int32_t batch, int32_t total_q, int32_t q_heads, int32_t max_kv_len,
-                             float sm_scale, void* workspace, size_t workspace_bytes,
-                             int32_t* dev_err, void* stream);
+                             float sm_scale, int32_t variant, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
  * kvq_copy_blocks -- copy whole blocks from one pool to another (LMDeploy

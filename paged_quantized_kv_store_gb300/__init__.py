@@ -105,7 +105,7 @@ def load(build_if_missing: bool = False):
                                                      ctypes.POINTER(SZ)]
     lib.paged_extend_attn_workspace_size.restype = ctypes.c_int
     lib.paged_extend_attn.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, P, P, I32, I32, I32,
-                                      I32, I32, F, P, SZ, P, P]
+                                      I32, I32, F, I32, P, SZ, P, P]
     lib.paged_extend_attn.restype = ctypes.c_int
     lib.kvq_copy_blocks.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), P, P, I64, P, P]
     lib.kvq_copy_blocks.restype = ctypes.c_int
@@ -371,10 +371,14 @@ def paged_extend_attn_workspace_size(batch, total_q, q_heads, kv_heads, max_kv_l
     return int(n.value)
 
 
+EXTEND_VARIANTS = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+
+
 def paged_extend_attn(pool: KVPool, q, out, qo_indptr, kv_lens, block_tables, max_kv_len,
-                      sm_scale, workspace=None, dev_err=None, stream=None):
+                      sm_scale, workspace=None, dev_err=None, stream=None, variant="auto"):
     """Extend (chunked prefill) attention: q rows qo_indptr[b]..qo_indptr[b+1]-1
-    are the last tokens of request b and attend causally; see kvq.h."""
+    are the last tokens of request b and attend causally; variant: "auto",
+    "mma_sync" or "tcgen05" (see kvq.h)."""
     lib = load()
     ps = pool.c_struct()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -382,8 +386,8 @@ def paged_extend_attn(pool: KVPool, q, out, qo_indptr, kv_lens, block_tables, ma
                                _ptr(qo_indptr), _ptr(kv_lens), _ptr(block_tables),
                                int(block_tables.shape[1]), int(kv_lens.numel()),
                                int(q.shape[0]), int(q.shape[1]), int(max_kv_len),
-                               float(sm_scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
-                               _stream(stream))
+                               float(sm_scale), EXTEND_VARIANTS[variant], _ptr(workspace),
+                               ws_bytes, _ptr(dev_err), _stream(stream))
     _check(st, "paged_extend_attn")
 
 

@@ -421,8 +421,8 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              const int32_t* qo_indptr, const int32_t* kv_lens,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              int32_t batch, int32_t total_q, int32_t q_heads, int32_t max_kv_len,
-                             float sm_scale, void* workspace, size_t workspace_bytes,
-                             int32_t* dev_err, void* stream) {
+                             float sm_scale, int32_t variant, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err, void* stream) {
   const kvq_status ps = check_pool(pool);
   if (ps != KVQ_OK) return ps;
   if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
@@ -431,6 +431,9 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
     return KVQ_ERR_INVALID_ARG;
   if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (variant < KVQ_EXTEND_AUTO || variant > KVQ_EXTEND_TCGEN05) return KVQ_ERR_INVALID_ARG;
+  if (variant == KVQ_EXTEND_TCGEN05 && !kvq::extend_tc_supported(pool->kv_dtype, q_dtype))
+    return KVQ_ERR_UNSUPPORTED;
   if (batch > kvq::kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0) return KVQ_OK;
   if (q == nullptr || out == nullptr || qo_indptr == nullptr || kv_lens == nullptr ||
@@ -475,6 +478,21 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.counter, 0, sizeof(int32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  // tcgen05 (128-row tiles) when the pool kind allows it and the batch has at
+  // least one tile per SM; else 16-row tiles on mma.sync (which can also cut
+  // the context of a short chunk into parts)
+  const int64_t tc_tiles = static_cast<int64_t>(pool->kv_heads) *
+                           ((static_cast<int64_t>(total_q) * a.group + 127) / 128);
+  const bool use_tc = variant == KVQ_EXTEND_TCGEN05 ||
+                      (variant == KVQ_EXTEND_AUTO &&
+                       kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_tiles >= sms);
+  if (use_tc) {
+    const int tc_per_sm = kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
+    if (tc_per_sm <= 0) return KVQ_ERR_CUDA;
+    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * tc_per_sm, s) == cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
+  }
   const int per_sm = kvq::extend_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
   if (per_sm <= 0) return KVQ_ERR_CUDA;
   return kvq::launch_extend(a, pool->kv_dtype, q_dtype, sms * per_sm, s) == cudaSuccess

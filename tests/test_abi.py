@@ -203,14 +203,14 @@ def test_extend_validation(lib):
     f = lib.paged_extend_attn
     p = 256
     args = dict(q=p, q_dtype=0, out=p, qo=p, kl=p, bt=p, mb=4, batch=2, tq=8, hq=4, mkl=64,
-                scale=0.1, ws=p, wsb=1 << 20, err=None, s=None)
+                scale=0.1, var=0, ws=p, wsb=1 << 20, err=None, s=None)
 
     def call(pool=None, **kw):
         a = dict(args)
         a.update(kw)
         return f(ctypes.byref(pool or _pool()), a["q"], a["q_dtype"], a["out"], a["qo"],
                  a["kl"], a["bt"], a["mb"], a["batch"], a["tq"], a["hq"], a["mkl"], a["scale"],
-                 a["ws"], a["wsb"], a["err"], a["s"])
+                 a["var"], a["ws"], a["wsb"], a["err"], a["s"])
 
     assert call(batch=-1) == 1
     assert call(tq=-1) == 1
@@ -221,3 +221,5 @@ def test_extend_validation(lib):
     assert call(batch=0) == 0 and call(tq=0) == 0
     assert call(qo=None) == 1
     assert call(q=p + 8) == 1              # misaligned
+    assert call(var=3) == 1 and call(var=-1) == 1
+    assert call(var=2, pool=_pool(kv_dtype=kvq.KVQ_BF16), q_dtype=kvq.KVQ_BF16) == 2

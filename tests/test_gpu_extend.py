@@ -30,7 +30,7 @@ def _stored_pool(wl):
     return pool
 
 
-def _gpu_extend(ew, pool, dev_err=None, q=None):
+def _gpu_extend(ew, pool, dev_err=None, q=None, variant="auto"):
     kvq = _kvq()
     wl = ew.wl
     if dev_err is None:
@@ -41,7 +41,8 @@ def _gpu_extend(ew, pool, dev_err=None, q=None):
                                               wl.max_seq_len)
     workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
     kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), i32(ew.kv_lens),
-                          i32(wl.block_tables), wl.max_seq_len, wl.sm_scale, workspace, dev_err)
+                          i32(wl.block_tables), wl.max_seq_len, wl.sm_scale, workspace, dev_err,
+                          variant=variant)
     return out, dev_err
 
 
@@ -69,11 +70,14 @@ KV_LENS = [300, 100, 517, 16, 40]
 CHUNKS = [300, 37, 200, 16, 1]
 
 
+@pytest.mark.parametrize("variant", ["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("kv_dtype,q_dtype,hq,hkv", CASES)
-def test_extend_matches_oracle(gpu, kv_dtype, q_dtype, hq, hkv):
+def test_extend_matches_oracle(gpu, kv_dtype, q_dtype, hq, hkv, variant):
+    if variant == "tcgen05" and kv_dtype == "bf16":
+        pytest.skip("the tcgen05 kernel takes INT8, INT4 and fp16 pools")
     ew = synthetic.extend("ext", kv_dtype, KV_LENS, CHUNKS, hq, hkv, q_dtype=q_dtype)
     pool = _stored_pool(ew.wl)
-    out, dev_err = _gpu_extend(ew, pool)
+    out, dev_err = _gpu_extend(ew, pool, variant=variant)
     assert gpu.kvq_check_error(dev_err) == 0
     assert_close(out_to_f64(out), _oracle(ew))
 
@@ -121,22 +125,25 @@ def test_bad_requests_are_reported_and_skipped(gpu):
     ws = kvq.paged_extend_attn_workspace_size(wl.batch, ew.total_q, wl.q_heads, wl.kv_heads, 64)
     w = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
     bad_lens = i32([64, 30])  # request 1: chunk of 40 over a context of 30
-    kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), bad_lens, i32(wl.block_tables), 64,
-                          wl.sm_scale, w, dev_err)
-    assert gpu.kvq_check_error(dev_err) == kvq.DEV_ERR_BITS["length"]
-    assert not out[10:].any()  # its rows are not written
     ref = _oracle(synthetic.extend("exb", "int8", [64], [10], 16, 8))
-    assert_close(out_to_f64(out[:10]), ref)
+    for variant in ("mma_sync", "tcgen05"):
+        out.zero_()
+        kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), bad_lens, i32(wl.block_tables),
+                              64, wl.sm_scale, w, dev_err, variant=variant)
+        assert gpu.kvq_check_error(dev_err) == kvq.DEV_ERR_BITS["length"]
+        assert not out[10:].any()  # its rows are not written
+        assert_close(out_to_f64(out[:10]), ref)
 
 
 @pytest.mark.slow
-def test_full_size_prefill_chunk_sampled(gpu):
+@pytest.mark.parametrize("variant", ["mma_sync", "tcgen05"])
+def test_full_size_prefill_chunk_sampled(gpu, variant):
     """The mixed step's 4096-token chunk (INT8, GQA 32q/8kv) prefilled on its own;
     sampled rows (first, last, middle, a block boundary) against the oracle."""
     ew = synthetic.cfg5_prefill()
     wl = ew.wl
     pool = _stored_pool(wl)
-    out, dev_err = _gpu_extend(ew, pool)
+    out, dev_err = _gpu_extend(ew, pool, variant=variant)
     assert gpu.kvq_check_error(dev_err) == 0
     got = out_to_f64(out)
     assert np.isfinite(got).all()
