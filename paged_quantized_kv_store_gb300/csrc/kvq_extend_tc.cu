@@ -15,7 +15,8 @@
 //   3. every thread reads its row of S (tcgen05.ld), applies
 //      s = S_k (q.(c - mid)) + (Z_k + mid S_k) sum(q), the causal mask and the
 //      online softmax (no shuffles: a thread owns its row); when its running
-//      maximum moves, the warp rescales its rows of O in TMEM; P' = p S_v goes
+//      maximum moves by more than a threshold, the warp rescales its rows of
+//      O in TMEM (a stale maximum only scales every term alike); P' = p S_v goes
 //      to shared memory in fp16 and sum p (Z_v + mid S_v) stays in a register;
 //   4. one thread issues O += P' V (M 128, N 128, K 64: 4 MMAs) into TMEM.
 // At the end each thread reads its row of O, adds the zero term, divides by
@@ -48,6 +49,7 @@ constexpr uint32_t kSzOff = kPOff + 128 * 128;      // 64 tokens x 4 floats
 constexpr uint32_t kOkOff = kSzOff + kTcTok * 16;   // 64 token flags
 constexpr uint32_t kBarOff = kOkOff + kTcTok * 4;   // 2 mbarriers
 constexpr uint32_t kSlotOff = kBarOff + 16;         // TMEM base address
+constexpr uint32_t kSvMaxOff = kSlotOff + 8;        // largest V scale of the tile (2 halves)
 constexpr uint32_t kFixedBytes = kSlotOff + 16;
 
 __host__ __device__ constexpr size_t tc_smem_bytes(int batch) {
@@ -85,6 +87,16 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -104,71 +116,156 @@ __device__ __forceinline__ uint32_t lo_hi(uint32_t x, uint32_t y, bool hi) {
   return hi ? ((x >> 16) | (y & 0xFFFF0000u)) : ((x & 0xFFFFu) | (y << 16));
 }
 
-// Stage the context tile [tok0, tok0 + 64) of kv head h: K as rows of the
-// K-major tile, V transposed, scale/zero and validity per token.
-template <int KV, bool QBF>
-__device__ __forceinline__ void stage_tile(const ExtendArgs& a, const int32_t* bt, int tok0,
-                                           int L, int h, uint32_t base, int tid) {
-  constexpr int kMid = KV == kI8 ? 128 : 8;
+// Raw bytes of one 64-token context tile that this thread stages: K chunks
+// (16 bytes of one token row each), V pieces (8 dims of 8 consecutive tokens),
+// and, for threads < 64, the scale/zero words and validity of token tid.
+template <int KV>
+struct RawTile {
+  static constexpr int kRow = KvTraits<KV>::kRowBytes;
+  static constexpr int kKChunks = kTcTok * (kRow / 16) / kTcThreads;  // 4 / 2 / 8
+  static constexpr int kVWords = kRow / 64;  // 32-bit words per token of an 8-dim piece: 2 / 1 / 4
+  uint4 k[kKChunks];
+  uint32_t v[8][kVWords];
+  uint32_t ksz, vsz;
+  bool ok;
+};
+
+// Global row (token t of the tile, kv head h) of a pool, or null when the
+// token is past the context or its block id is outside the pool.
+template <int KV>
+__device__ __forceinline__ const uint8_t* tc_row(const ExtendArgs& a, const int32_t* bt,
+                                                 const uint8_t* pool, int tt, int L, int h) {
   constexpr int kRow = KvTraits<KV>::kRowBytes;
-  const int64_t tok_stride = static_cast<int64_t>(a.kv_heads) * kRow;
-  // per-token block address (or -1), scale/zero, validity
-  if (tid < kTcTok) {
-    const int t = tok0 + tid;
-    int64_t phys = -1;
-    if (t < L) {
-      const int32_t blk = bt[t / kBlock];
-      if (blk >= 0 && blk < a.num_blocks) phys = blk;
-      else report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
-    }
-    float Sk = 0.f, Zk = 0.f, Sv = 0.f, Zv = 0.f;
-    if (phys >= 0 && KvTraits<KV>::kQuant) {
-      const int64_t i = (phys * a.kv_heads + h) * kBlock + t % kBlock;
-      const uint32_t wk = __ldg(a.k_sz + i), wv = __ldg(a.v_sz + i);
-      Sk = half_lo(wk); Zk = half_hi(wk) + kMid * Sk;
-      Sv = half_lo(wv); Zv = half_hi(wv) + kMid * Sv;
-    }
-    const uint32_t sz = base + kSzOff + 16 * tid;
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(sz), "f"(Sk), "f"(Zk), "f"(Sv),
-                 "f"(Zv)
-                 : "memory");
-    sts32(base + kOkOff + 4 * tid, phys >= 0 ? 1u : 0u);
+  if (tt >= L) return nullptr;
+  const int32_t blk = bt[tt / kBlock];
+  if (blk < 0 || blk >= a.num_blocks) return nullptr;
+  return pool + ((static_cast<int64_t>(blk) * kBlock + tt % kBlock) * a.kv_heads + h) * kRow;
+}
+
+template <int KV>
+__device__ __forceinline__ void load_tile(const ExtendArgs& a, const int32_t* bt, int tok0, int L,
+                                          int h, int tid, RawTile<KV>& r) {
+  using R = RawTile<KV>;
+  constexpr int kChunks = R::kRow / 16;
+#pragma unroll
+  for (int i = 0; i < R::kKChunks; ++i) {
+    const int e = tid + kTcThreads * i;
+    const uint8_t* src = tc_row<KV>(a, bt, a.k, tok0 + e / kChunks, L, h);
+    r.k[i] = src ? __ldg(reinterpret_cast<const uint4*>(src) + e % kChunks)
+                 : make_uint4(0u, 0u, 0u, 0u);
   }
-  auto row_ptr = [&](const uint8_t* pool, int t) -> const uint8_t* {
-    const int tt = tok0 + t;
-    if (tt >= L) return nullptr;
-    const int32_t blk = bt[tt / kBlock];
-    if (blk < 0 || blk >= a.num_blocks) return nullptr;
-    return pool + (static_cast<int64_t>(blk) * kBlock + tt % kBlock) * tok_stride +
-           static_cast<int64_t>(h) * kRow;
-  };
-  // K: 64 token rows of 128 elements; one 16-byte chunk of codes per step
-  constexpr int kChunks = kRow / 16;
-  for (int e = tid; e < kTcTok * kChunks; e += kTcThreads) {
+  // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
+  const int tg = tid >> 4, dc = tid & 15;
+  const int tv = tok0 + 8 * tg;
+  const int32_t vblk = tv < L ? bt[tv / kBlock] : -1;
+  const bool vok = vblk >= 0 && vblk < a.num_blocks;
+  const uint8_t* vrow =
+      a.v + ((static_cast<int64_t>(vok ? vblk : 0) * kBlock + tv % kBlock) * a.kv_heads + h) *
+                R::kRow +
+      dc * 4 * R::kVWords;
+  const int64_t vstride = static_cast<int64_t>(a.kv_heads) * R::kRow;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const bool ok = vok && tv + t < L;
+    const uint8_t* src = vrow + t * vstride;
+    if constexpr (R::kVWords == 4) {
+      const uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0u, 0u, 0u, 0u);
+      r.v[t][0] = w.x; r.v[t][R::kVWords > 1 ? 1 : 0] = w.y;
+      r.v[t][R::kVWords > 2 ? 2 : 0] = w.z; r.v[t][R::kVWords > 3 ? 3 : 0] = w.w;
+    } else if constexpr (R::kVWords == 2) {
+      const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0u, 0u);
+      r.v[t][0] = w.x; r.v[t][R::kVWords > 1 ? 1 : 0] = w.y;
+    } else {
+      r.v[t][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
+    }
+  }
+  r.ok = false;
+  r.ksz = r.vsz = 0u;
+  if (tid < kTcTok) {
+    const int tt = tok0 + tid;
+    if (tt < L) {
+      const int32_t blk = bt[tt / kBlock];
+      r.ok = blk >= 0 && blk < a.num_blocks;
+      if (r.ok && KvTraits<KV>::kQuant) {
+        const int64_t i = (static_cast<int64_t>(blk) * a.kv_heads + h) * kBlock + tt % kBlock;
+        r.ksz = __ldg(a.k_sz + i);
+        r.vsz = __ldg(a.v_sz + i);
+      }
+      if (!r.ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+    }
+  }
+}
+
+// The four 16-bit pairs (dims 0-1, 2-3, 4-5, 6-7) of one token's 8-dim piece.
+template <int KV>
+__device__ __forceinline__ void piece_pairs(const uint32_t (&w)[RawTile<KV>::kVWords],
+                                            uint32_t (&p)[4]) {
+  constexpr int kMid = KV == kI8 ? 128 : 8;
+  if constexpr (KV == kF16) {
+    p[0] = w[0]; p[1] = w[1]; p[2] = w[2]; p[3] = w[3];
+  } else if constexpr (KV == kI8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t word = w[q >> 1] >> (16 * (q & 1));
+      p[q] = centred_pair<false>(word & 0xFF, (word >> 8) & 0xFF, kMid);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t byte = (w[0] >> (8 * q)) & 0xFF;
+      p[q] = centred_pair<false>(byte & 0xF, byte >> 4, kMid);
+    }
+  }
+}
+
+// Registers -> shared memory: the K tile (K-major, Q's type), V transposed
+// (fp16), per-token (S_k', Z_k', S_v, Z_v') with the softmax scale folded
+// into the K pair, and validity flags. Returns (for the whole CTA) whether
+// any token of the tile is missing.
+template <int KV, bool QBF>
+__device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV>& r,
+                                           uint32_t base, int tid) {
+  using R = RawTile<KV>;
+  constexpr int kMid = KV == kI8 ? 128 : 8;
+  constexpr int kChunks = R::kRow / 16;
+  if (tid < kTcTok) {
+    float Sk = a.sm_scale_log2, Zk = 0.f, Sv = 1.f, Zv = 0.f;
+    if constexpr (KvTraits<KV>::kQuant) {
+      const float s_k = half_lo(r.ksz), s_v = half_lo(r.vsz);
+      Sk = s_k * a.sm_scale_log2;
+      Zk = (half_hi(r.ksz) + kMid * s_k) * a.sm_scale_log2;
+      Sv = s_v;
+      Zv = half_hi(r.vsz) + kMid * s_v;
+    }
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(base + kSzOff + 16 * tid), "f"(Sk),
+                 "f"(Zk), "f"(Sv), "f"(Zv)
+                 : "memory");
+    sts32(base + kOkOff + 4 * tid, r.ok ? 1u : 0u);
+    float mx = Sv;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    if ((tid & 31) == 0) sts32(base + kSvMaxOff + 4 * (tid >> 5), __float_as_uint(mx));
+  }
+#pragma unroll
+  for (int i = 0; i < R::kKChunks; ++i) {
+    const int e = tid + kTcThreads * i;
     const int t = e / kChunks, ch = e % kChunks;
-    const uint8_t* src = row_ptr(a.k, t);
-    const uint4 w = src ? __ldg(reinterpret_cast<const uint4*>(src + 16 * ch))
-                        : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t x[4] = {r.k[i].x, r.k[i].y, r.k[i].z, r.k[i].w};
     if constexpr (KV == kF16) {
-      // 8 elements (dims 8 ch ..): one swizzled 16-byte chunk
-      sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 8 * ch), w.x, w.y, w.z, w.w);
+      sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
     } else if constexpr (KV == kI8) {
-      // 16 codes (dims 16 ch ..): two chunks
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t word = x[2 * hf + (q >> 1)];
-          const int sh = 16 * (q & 1);
-          v[q] = centred_pair<QBF>((word >> sh) & 0xFF, (word >> (sh + 8)) & 0xFF, kMid);
+          const uint32_t word = x[2 * hf + (q >> 1)] >> (16 * (q & 1));
+          v[q] = centred_pair<QBF>(word & 0xFF, (word >> 8) & 0xFF, kMid);
         }
         sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 16 * ch + 8 * hf), v[0], v[1], v[2],
                v[3]);
       }
     } else {
-      // 32 codes (dims 32 ch ..), low nibble = even dim: four chunks
 #pragma unroll
       for (int qt = 0; qt < 4; ++qt) {
         uint32_t v[4];
@@ -182,42 +279,23 @@ __device__ __forceinline__ void stage_tile(const ExtendArgs& a, const int32_t* b
       }
     }
   }
-  // V transposed: row = dim, reduction index = token; a step takes two
-  // consecutive tokens and one 16-byte chunk of dims, and writes one 32-bit
-  // word (the two tokens) per dim
-  for (int e = tid; e < (kTcTok / 2) * kChunks; e += kTcThreads) {
-    const int tp = e % (kTcTok / 2), ch = e / (kTcTok / 2);
-    const int t = 2 * tp;
-    const uint8_t* s0 = row_ptr(a.v, t);
-    const uint8_t* s1 = row_ptr(a.v, t + 1);
-    const uint4 w0 = s0 ? __ldg(reinterpret_cast<const uint4*>(s0 + 16 * ch))
-                        : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 w1 = s1 ? __ldg(reinterpret_cast<const uint4*>(s1 + 16 * ch))
-                        : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
-    if constexpr (KV == kF16) {
+  // V: 8 tokens x 8 dims -> 8 rows (dims) of 8 tokens, one 16-byte store each
+  const int tg = tid >> 4, dc = tid & 15;
+  uint32_t pr[8][4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t word = lo_hi(x0[q >> 1], x1[q >> 1], q & 1);
-        sts32(base + kVOff + umma_kmajor_offset(128, 8 * ch + q, t), word);
-      }
-    } else if constexpr (KV == kI8) {
+  for (int t = 0; t < 8; ++t) piece_pairs<KV>(r.v[t], pr[t]);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int c0 = (x0[q >> 2] >> (8 * (q & 3))) & 0xFF;
-        const int c1 = (x1[q >> 2] >> (8 * (q & 3))) & 0xFF;
-        sts32(base + kVOff + umma_kmajor_offset(128, 16 * ch + q, t),
-              centred_pair<false>(c0, c1, kMid));
-      }
-    } else {
+  for (int q = 0; q < 4; ++q) {
+    uint32_t lo[4], hi[4];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int c0 = (x0[q >> 3] >> (4 * (q & 7))) & 0xF;
-        const int c1 = (x1[q >> 3] >> (4 * (q & 7))) & 0xF;
-        sts32(base + kVOff + umma_kmajor_offset(128, 32 * ch + q, t),
-              centred_pair<false>(c0, c1, kMid));
-      }
+    for (int tp = 0; tp < 4; ++tp) {
+      lo[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x5410u);
+      hi[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x7632u);
     }
+    sts128(base + kVOff + umma_kmajor_offset(128, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2],
+           lo[3]);
+    sts128(base + kVOff + umma_kmajor_offset(128, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1],
+           hi[2], hi[3]);
   }
 }
 
@@ -331,8 +409,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     float m = -INFINITY, l = 0.f, z = 0.f;
 
+    RawTile<KV> raw;
+    load_tile<KV>(a, bt, 0, s.L, h, tid, raw);
     for (int j = 0; j < ntiles && alive; ++j) {
-      stage_tile<KV, QBF>(a, bt, j * kTcTok, s.L, h, base, tid);
+      store_tile<KV, QBF>(a, raw, base, tid);
+      // the tile's missing tokens (rare: block ids outside the pool)
+      const bool holes = __syncthreads_or(tid < kTcTok && !raw.ok &&
+                                          j * kTcTok + tid < s.L) != 0;
+      if (j + 1 < ntiles) load_tile<KV>(a, bt, (j + 1) * kTcTok, s.L, h, tid, raw);
       fence_async_smem();
       __syncthreads();
       if (tid == 0) {
@@ -365,19 +449,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) sc[32 + i] = v[i];
       }
+      // s = S_k' raw + Z_k' sum(q) (scale folded in); positions past the row's
+      // own, and missing tokens, are masked
       float bm = -INFINITY;
+      const bool diag = j * kTcTok + kTcTok - 1 > pos;
 #pragma unroll
       for (int i = 0; i < kTcTok; ++i) {
-        const float4 szv = lds_f4(base + kSzOff + 16 * i);
-        const int t = j * kTcTok + i;
-        float x;
-        if constexpr (kQuant) x = (szv.x * sc[i] + szv.y * qsum) * a.sm_scale_log2;
-        else x = sc[i] * a.sm_scale_log2;
-        const bool ok = t <= pos && lds_f32(base + kOkOff + 4 * i) != 0.f;
-        sc[i] = ok ? x : -INFINITY;
-        bm = fmaxf(bm, sc[i]);
+        const float2 kz = lds_f2(base + kSzOff + 16 * i);
+        float x = kz.x * sc[i] + kz.y * qsum;
+        if (diag && j * kTcTok + i > pos) x = -INFINITY;
+        sc[i] = x;
+        bm = fmaxf(bm, x);
       }
-      const float mn = fmaxf(m, bm);
+      if (holes) {
+        bm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kTcTok; ++i) {
+          if (lds_u32(base + kOkOff + 4 * i) == 0u) sc[i] = -INFINITY;
+          bm = fmaxf(bm, sc[i]);
+        }
+      }
+      // the reference maximum moves only when a score exceeds it by more than
+      // tau (log2 units): p <= 2^tau then, and P' = p S_v stays within fp16
+      // when the tile's largest V scale is at most 240 (else tau = 0: exact)
+      const float sv_max = fmaxf(__uint_as_float(lds_u32(base + kSvMaxOff)),
+                                 __uint_as_float(lds_u32(base + kSvMaxOff + 4)));
+      const float tau = sv_max <= 240.f ? 8.f : 0.f;
+      const float mn = (m == -INFINITY || bm > m + tau) ? fmaxf(m, bm) : m;
       const float al = (m == -INFINITY || mn == m) ? 1.f : ex2(m - mn);
       // rescale this warp's rows of O when some row's maximum moved
       if (j > 0 && __any_sync(kFull, al != 1.f)) {
@@ -406,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v0 = p0, v1 = p1;
           if constexpr (kQuant) {
             const float4 s0 = lds_f4(base + kSzOff + 16 * i0);
-            const float4 s1 = lds_f4(base + kSzOff + 16 * (i0 + 1));
+            const float4 s1 = lds_f4(base + kSzOff + 16 * i0 + 16);
             z += p0 * s0.w + p1 * s1.w;
             v0 = p0 * s0.z;
             v1 = p1 * s1.z;
@@ -486,6 +584,11 @@ cudaError_t launch_tc_t(const ExtendArgs& a, int grid, cudaStream_t s) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tc_smem_bytes(kMaxBatch)));
     if (e != cudaSuccess) return e;
+    // two CTAs per SM need the largest shared-memory carveout
+    e = cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     opted_in_device = dev;
   }
   extend_tc_kernel<KV, QBF><<<grid, kTcThreads, tc_smem_bytes(a.batch), s>>>(a);
@@ -499,7 +602,10 @@ int tc_occupancy_t(int batch) {
   static int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(tc_smem_bytes(kMaxBatch))) != cudaSuccess)
+                           static_cast<int>(tc_smem_bytes(kMaxBatch))) != cudaSuccess ||
+      cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>,
+                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, extend_tc_kernel<KV, QBF>, kTcThreads,
