@@ -487,9 +487,10 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                       (variant == KVQ_EXTEND_AUTO &&
                        kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_tiles >= sms);
   if (use_tc) {
-    const int tc_per_sm = kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch);
-    if (tc_per_sm <= 0) return KVQ_ERR_CUDA;
-    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * tc_per_sm, s) == cudaSuccess
+    // two persistent CTAs per SM: each holds 256 of the SM's 512 TMEM columns
+    // and about 86 KB of shared memory (more than two never fit)
+    if (kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch) <= 0) return KVQ_ERR_CUDA;
+    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * 2, s) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
   }

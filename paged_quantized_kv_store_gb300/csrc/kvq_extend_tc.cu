@@ -205,10 +205,7 @@ __device__ __forceinline__ void piece_pairs(const uint32_t (&w)[RawTile<KV>::kVW
     p[0] = w[0]; p[1] = w[1]; p[2] = w[2]; p[3] = w[3];
   } else if constexpr (KV == kI8) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t word = w[q >> 1] >> (16 * (q & 1));
-      p[q] = centred_pair<false>(word & 0xFF, (word >> 8) & 0xFF, kMid);
-    }
+    for (int q = 0; q < 4; ++q) p[q] = bytes_to_f16(w[q >> 1], (q & 1) ? 0x4342u : 0x4140u);
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -254,13 +251,19 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
     if constexpr (KV == kF16) {
       sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
     } else if constexpr (KV == kI8) {
+      // c - 128 exactly: fp16 by a byte permute into 1024 + c and one packed
+      // subtract; bf16 through fp32
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t word = x[2 * hf + (q >> 1)] >> (16 * (q & 1));
-          v[q] = centred_pair<QBF>(word & 0xFF, (word >> 8) & 0xFF, kMid);
+          const uint32_t word = x[2 * hf + (q >> 1)];
+          if constexpr (QBF) {
+            v[q] = (q & 1) ? bytes_to_bf16_pair(word, 2, 3) : bytes_to_bf16_pair(word, 0, 1);
+          } else {
+            v[q] = bytes_to_f16(word, (q & 1) ? 0x4342u : 0x4140u);
+          }
         }
         sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 16 * ch + 8 * hf), v[0], v[1], v[2],
                v[3]);
