@@ -487,10 +487,12 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                       (variant == KVQ_EXTEND_AUTO &&
                        kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_tiles >= sms);
   if (use_tc) {
-    // two persistent CTAs per SM: each holds 256 of the SM's 512 TMEM columns
-    // and about 86 KB of shared memory (more than two never fit)
+    // persistent CTAs: two per SM (each holds 256 of the SM's 512 TMEM
+    // columns) while their shared memory fits, else one
     if (kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch) <= 0) return KVQ_ERR_CUDA;
-    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * 2, s) == cudaSuccess
+    const size_t per_cta = kvq::extend_tc_smem_bytes(batch) + 2048;  // + static + reserved
+    const int per_sm = per_cta * 2 <= 228 * 1024 ? 2 : 1;
+    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * per_sm, s) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
   }

@@ -622,6 +622,8 @@ int tc_occupancy_t(int batch) {
 
 }  // namespace
 
+size_t extend_tc_smem_bytes(int batch) { return tc_smem_bytes(batch); }
+
 bool extend_tc_supported(int kv_dtype, int q_dtype) {
   return kv_dtype == kI8 || kv_dtype == kI4 || (kv_dtype == kF16 && q_dtype == kF16);
 }

@@ -141,6 +141,7 @@ bool extend_tc_supported(int kv_dtype, int q_dtype);
 cudaError_t launch_extend_tc(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                              cudaStream_t s);
 int extend_tc_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
+size_t extend_tc_smem_bytes(int batch);  // dynamic shared memory of one CTA
 cudaError_t launch_copy(const CopyArgs& a, int64_t n, cudaStream_t s);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
 // kv_dtype / q_dtype select the template instance
