@@ -155,7 +155,7 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int32_t* bt
                  : make_uint4(0u, 0u, 0u, 0u);
   }
   // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
-  const int tg = tid >> 4, dc = tid & 15;
+  const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
   const int tv = tok0 + 8 * tg;
   const int32_t vblk = tv < L ? bt[tv / kBlock] : -1;
   const bool vok = vblk >= 0 && vblk < a.num_blocks;
@@ -283,7 +283,7 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
     }
   }
   // V: 8 tokens x 8 dims -> 8 rows (dims) of 8 tokens, one 16-byte store each
-  const int tg = tid >> 4, dc = tid & 15;
+  const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
   uint32_t pr[8][4];
 #pragma unroll
   for (int t = 0; t < 8; ++t) piece_pairs<KV>(r.v[t], pr[t]);
