@@ -53,7 +53,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the block copy / swap measurement")
+                   help="skip the block copy / swap and extend measurements")
+    p.add_argument("--extend-only", action="store_true",
+                   help="only the extend (prefill) attention measurement (profiling)")
     p.add_argument("--shared-prefix", choices=["auto", "on", "off"], default="off",
                    help="decode shared prefixes once per group (auto: when the workload has one)")
     p.add_argument("--json-out", default="")
@@ -734,7 +736,13 @@ def main():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group(backend=backend)
         dist = tdist
-    if args.impl == "reference":
+    if args.extend_only:
+        import torch
+
+        import paged_quantized_kv_store_gb300 as kvq
+        kvq.load()
+        res = {"paged_extend_attn": measure_extend(kvq, torch.device("cuda"), reps=3)}
+    elif args.impl == "reference":
         res = run_reference(args, rank)
     else:
         res = run_ours(args, rank, world, dist)
