@@ -227,6 +227,18 @@ def traffic_from_profile(workload: str):
     return float(m_b.group(1)), sha
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (x itself without a process group). The
+    value travels in a tensor on `device`: a CUDA device for NCCL, the CPU for
+    gloo."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def copy_bandwidth_gbs(dev, n_bytes: int = 1 << 31, reps: int = 10) -> float:
     """This GPU's device-to-device copy bandwidth right now (read + write bytes),
     best of `reps` copies of a 2 GiB buffer (larger than L2)."""
@@ -518,9 +530,7 @@ def run_ours(args, rank: int, world: int, dist):
     ms_total = t0.elapsed_time(t1)
     decode_ms = [ev_d0[i].elapsed_time(ev_d1[i]) for i in range(K)]
     if dist is not None:
-        t = torch.tensor([ms_total], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
     tokens_per_step = wl.batch * world
     value = tokens_per_step / (ms_step / 1e3)
@@ -567,9 +577,7 @@ def run_ours(args, rank: int, world: int, dist):
         torch.cuda.synchronize()
         ms_e2e = e0.elapsed_time(e1)
         if dist is not None:
-            t = torch.tensor([ms_e2e], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+            ms_e2e = max_over_ranks(ms_e2e, dist, dev)
         e2e = {"value": tokens_per_step / (ms_e2e / K / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
