@@ -154,3 +154,28 @@ def test_full_size_prefill_chunk_sampled(gpu, variant):
             ref, _ = oracle.decode_one(opool, q[i, h], wl.q_dtype, wl.block_tables[0], i + 1,
                                        h // wl.group, wl.sm_scale)
             assert_close(got[i, h], ref)
+
+
+@pytest.mark.parametrize("variant", ["mma_sync", "tcgen05"])
+def test_block_ids_outside_the_pool_are_skipped_and_reported(gpu, variant):
+    """A block id past the pool in one request: the bit is set, that block's
+    tokens are left out (its rows stay finite), the other request is exact."""
+    ew = synthetic.extend("exh", "int8", [300, 200], [300, 120], 32, 8)
+    wl = ew.wl
+    pool = _stored_pool(wl)
+    kvq = _kvq()
+    bt = wl.block_tables.copy()
+    bt[1, 3] = wl.num_blocks + 7  # request 1, tokens 48 .. 63
+    q = to_dev(ew.q_ext(), wl.q_dtype)
+    out = torch.full_like(q, float("nan"))
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = kvq.paged_extend_attn_workspace_size(wl.batch, ew.total_q, wl.q_heads, wl.kv_heads,
+                                              wl.max_seq_len)
+    w = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), i32(ew.kv_lens), i32(bt),
+                          wl.max_seq_len, wl.sm_scale, w, dev_err, variant=variant)
+    assert gpu.kvq_check_error(dev_err) == kvq.DEV_ERR_BITS["block_id"]
+    got = out_to_f64(out)
+    assert np.isfinite(got).all()
+    ref = _oracle(ew)
+    assert_close(got[:300], ref[:300])

@@ -202,3 +202,16 @@ def test_full_size_int4_shared_prefix_sampled(gpu):
     for b in sorted({0, wl.batch - 1, int(lens.argmax()), int(lens.argmin()), wl.batch // 2}):
         _, oout = oracle_request(wl, b)
         assert_close(got[b], oout)
+
+
+def test_block_id_outside_the_pool_in_the_shared_part(gpu):
+    """A bad id among the shared blocks: reported, no fault, finite outputs."""
+    import paged_quantized_kv_store_gb300 as kvq
+    pool, _ = _pool_pair("int4", 12, 8)
+    bt = np.array([[4, 99, 2, 1], [4, 99, 2, 7], [4, 99, 2, 8]], dtype=np.int32)
+    lens = np.array([60, 60, 55], dtype=np.int32)
+    q = to_dev(synthetic.normal(5, 905, 0, 3 * 32 * 128).reshape(3, 32, 128), "f16")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _shared_call(pool, q, i32(bt), i32(lens), [([0, 1, 2], 3)], 64, dev_err)
+    assert gpu.kvq_check_error(dev_err) & kvq.DEV_ERR_BITS["block_id"]
+    assert torch.isfinite(out.float()).all()
