@@ -58,6 +58,8 @@ def parse_args():
                    help="only the extend (prefill) attention measurement (profiling)")
     p.add_argument("--shared-prefix", choices=["auto", "on", "off"], default="off",
                    help="decode shared prefixes once per group (auto: when the workload has one)")
+    p.add_argument("--fused-step", action="store_true",
+                   help="time the step as the one cooperative launch of kvq_decode_step")
     p.add_argument("--json-out", default="")
     return p.parse_args()
 
@@ -314,6 +316,46 @@ def measure_block_copy(kvq, pool, wl, dev, peak: float, n_cow: int = 4096, n_swa
     return out
 
 
+def measure_step_forms(sep_step, fused_step, out_sep, out_fused, reps: int = 50) -> dict:
+    """The decode step as three calls (four kernels) and as kvq_decode_step
+    (one cooperative kernel when the step carries no prefill chunk), each
+    replayed from a CUDA graph, interleaved in
+    blocks of ten so that both see the same clocks; the two outputs must agree
+    to the decode tolerance."""
+    import torch
+
+    graphs = []
+    for fn in (sep_step, fused_step):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    for g in graphs:
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    diff = (out_sep.float() - out_fused.float()).abs()
+    tol = 2e-3 + 1e-2 * out_sep.float().abs()
+    if not bool((diff <= tol).all()):
+        raise RuntimeError("fused step output differs from the three-call step")
+    ms = [0.0, 0.0]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for blk in range(reps // 10):
+        for i, g in enumerate(graphs):
+            ev[0].record()
+            for _ in range(10):
+                g.replay()
+            ev[1].record()
+            torch.cuda.synchronize()
+            ms[i] += ev[0].elapsed_time(ev[1])
+    n = (reps // 10) * 10
+    return {"three_calls_ms": round(ms[0] / n, 5), "fused_ms": round(ms[1] / n, 5),
+            "speedup": round(ms[0] / ms[1], 4), "cuda_graph": True, "reps": n}
+
+
 def measured_tensor_peak():
     """(bf16 dense TFLOP/s burst, where it came from)."""
     try:
@@ -444,6 +486,13 @@ def run_ours(args, rank: int, world: int, dist):
     r2t = torch.from_numpy(wl.req_to_token).to(dev)
     step = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq, wl.max_seq_len,
                           tdt[wl.q_dtype], num_splits=args.num_splits, device=dev)
+    fstep = None
+    if groups is None and wl.in_dtype == wl.q_dtype:
+        fstep = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq,
+                               wl.max_seq_len, tdt[wl.q_dtype], num_splits=args.num_splits,
+                               device=dev, fused=True)
+    if args.fused_step and fstep is None:
+        raise SystemExit("--fused-step: needs no shared prefix and new rows in q's dtype")
     plan = kvq.paged_decode_attn_plan(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
                                       args.num_splits)
     stream = torch.cuda.current_stream(dev)
@@ -453,7 +502,26 @@ def run_ours(args, rank: int, world: int, dist):
                                                step.block_tables, step.dev_err)
         kvq.kv_store_quant(pool, inp["k_new"], inp["v_new"], inp["slot_mapping"], step.dev_err)
 
-    if groups is None:
+    def fused(inp):
+        fstep(r2t, inp["req_pool_indices"], inp["seq_lens"], inp["q"], inp["k_new"],
+              inp["v_new"], inp["slot_mapping"], wl.sm_scale)
+
+    if args.fused_step:
+        def pre_step(inp):
+            pass
+
+        def dec_step(inp):
+            fused(inp)
+
+        step = fstep
+        if kvq.kvq_decode_step_fused(wl.batch, len(wl.step_store()[0])):
+            launches_per_step = 1
+            decode_kernels = "kvq_decode_step (step_kernel: tables + store, decode, combine)"
+        else:
+            launches_per_step = 4
+            decode_kernels = ("kvq_decode_step as four kernels (prefill chunk in the step): "
+                              "tables, store, decode, combine")
+    elif groups is None:
         def dec_step(inp):
             kvq.paged_decode_attn(pool, inp["q"], step.out, step.block_tables, inp["seq_lens"],
                                   wl.max_seq_len, wl.sm_scale, args.num_splits, step.workspace,
@@ -488,12 +556,18 @@ def run_ours(args, rank: int, world: int, dist):
     if use_graph:
         # the step as two CUDA graphs (a decode step is replayed as a graph in
         # serving runtimes); the decode call is timed between the two replays
-        g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_pre):
-            pre_step(d_in)
+        g_dec = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_dec):
             dec_step(d_in)
-        run_pre, run_dec = g_pre.replay, g_dec.replay
+        run_dec = g_dec.replay
+        if args.fused_step:  # nothing runs before the one launch
+            def run_pre():
+                pass
+        else:
+            g_pre = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_pre):
+                pre_step(d_in)
+            run_pre = g_pre.replay
         for _ in range(args.warmup):
             run_pre()
             run_dec()
@@ -613,6 +687,21 @@ def run_ours(args, rank: int, world: int, dist):
     if not args.no_extras:
         extras = {"kvq_copy_blocks": measure_block_copy(kvq, pool, wl, dev, peak),
                   "paged_extend_attn": measure_extend(kvq, dev)}
+        if fstep is not None:
+            sep = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq,
+                                 wl.max_seq_len, tdt[wl.q_dtype], num_splits=args.num_splits,
+                                 device=dev)
+
+            def sep_call():
+                sep(r2t, d_in["req_pool_indices"], d_in["seq_lens"], d_in["q"], d_in["k_new"],
+                    d_in["v_new"], d_in["slot_mapping"], wl.sm_scale)
+
+            extras["kvq_decode_step"] = measure_step_forms(sep_call, lambda: fused(d_in),
+                                                           sep.out, fstep.out)
+            extras["kvq_decode_step"]["single_launch"] = kvq.kvq_decode_step_fused(
+                wl.batch, int(d_in["slot_mapping"].numel()))
+            if kvq.kvq_check_error(sep.dev_err) or kvq.kvq_check_error(fstep.dev_err):
+                raise RuntimeError("device error word set by the step-form measurement")
         bits = kvq.kvq_check_error(step.dev_err)
         if bits:
             raise RuntimeError(f"device error word {bits:#x} after the copy measurement")
@@ -624,7 +713,7 @@ def run_ours(args, rank: int, world: int, dist):
         "dtype": {"int8": "u8", "int4": "u4", "f16": "f16", "bf16": "bf16"}[wl.kv_dtype],
         "data": "synthetic (seeded counter-based generator; no dataset)",
         "config": {**workload_desc(wl), "l2": "no flush: the pool is larger than L2",
-                   "cuda_graph": use_graph,
+                   "cuda_graph": use_graph, "fused_step": bool(args.fused_step),
                    "shared_prefix": None if groups is None else
                    {"groups": 1, "members": len(groups[0]), "shared_blocks": groups[1]},
                    "plan": plan, "parallelism": f"replicas x{world} (no data-path collective)"},

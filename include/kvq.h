@@ -339,6 +339,41 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
                              size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
+ * kvq_decode_step -- one decode step of a layer in a single launch: the
+ * block tables from the ReqToTokenPool rows (as
+ * kvq_block_tables_from_req_to_token), the quantizing store of the step's new
+ * K/V rows (as kv_store_quant, the rows in q_dtype), then the attention (as
+ * paged_decode_attn, reading the tables just built). "pymllm Runtime Design",
+ * forward stage: a decode step stores each request's new token and attends
+ * over its cache; one kernel instead of four, its phases (tables + store,
+ * attention, split-K combine) separated by grid barriers (a cooperative
+ * launch: every CTA resident; each barrier wait gives up after 2 s with
+ * KVQ_DEV_ERR_TIMEOUT). Arguments mean what they mean for the three calls it
+ * replaces; block_tables is written. The workspace is at least *bytes of
+ * kvq_decode_step_workspace_size (the decode's plus a barrier counter).
+ * The single launch is used when the step stores at most two tokens per
+ * request (kvq_decode_step_fused): its first phase runs at the attention's
+ * occupancy, which suits a decode batch's new tokens but not a prefill chunk
+ * stored in the same step (LMDeploy article §2.3, chunked prefill beside the
+ * decodes); with more tokens the same work runs as four kernels.
+ */
+int32_t kvq_decode_step_fused(int32_t batch, int64_t num_tokens);
+
+kvq_status kvq_decode_step_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                          int32_t head_dim, int32_t max_seq_len,
+                                          int32_t num_splits, size_t* bytes);
+
+kvq_status kvq_decode_step(const kvq_pool* pool, const int32_t* req_to_token,
+                           int32_t num_req_slots, int32_t max_context_len,
+                           const int32_t* req_pool_indices, const int32_t* seq_lens,
+                           int32_t batch, int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           int64_t num_tokens, const void* q, int32_t q_dtype, void* out,
+                           int32_t q_heads, int32_t max_seq_len, float sm_scale,
+                           int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_err, void* stream);
+
+/*
  * kvq_copy_blocks -- copy whole blocks from one pool to another (LMDeploy
  * article §4.4: the cache engine swaps blocks between the GPU and the CPU
  * cache by a {dst: src} map, K and V alike; inside one pool the same copy

@@ -63,7 +63,8 @@ EXPORTED = ["kv_store_quant", "kvq_block_tables_from_req_to_token", "paged_decod
             "paged_decode_attn_workspace_size", "paged_decode_attn", "kvq_check_error",
             "kvq_status_string", "kvq_version", "paged_decode_attn_noalloc",
             "paged_decode_attn_shared_prefix_workspace_size", "paged_decode_attn_shared_prefix",
-            "kvq_copy_blocks", "paged_extend_attn_workspace_size", "paged_extend_attn"]
+            "kvq_copy_blocks", "paged_extend_attn_workspace_size", "paged_extend_attn",
+            "kvq_decode_step_workspace_size", "kvq_decode_step", "kvq_decode_step_fused"]
 
 
 def load(build_if_missing: bool = False):
@@ -107,6 +108,14 @@ def load(build_if_missing: bool = False):
     lib.paged_extend_attn.argtypes = [ctypes.POINTER(_Pool), P, I32, P, P, P, P, I32, I32, I32,
                                       I32, I32, F, I32, P, SZ, P, P]
     lib.paged_extend_attn.restype = ctypes.c_int
+    lib.kvq_decode_step_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32,
+                                                   ctypes.POINTER(SZ)]
+    lib.kvq_decode_step_workspace_size.restype = ctypes.c_int
+    lib.kvq_decode_step.argtypes = [ctypes.POINTER(_Pool), P, I32, I32, P, P, I32, P, I32, P, P,
+                                    P, I64, P, I32, P, I32, I32, F, I32, P, SZ, P, P]
+    lib.kvq_decode_step.restype = ctypes.c_int
+    lib.kvq_decode_step_fused.argtypes = [I32, I64]
+    lib.kvq_decode_step_fused.restype = I32
     lib.kvq_copy_blocks.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), P, P, I64, P, P]
     lib.kvq_copy_blocks.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -262,6 +271,43 @@ def paged_decode_attn_noalloc(pool: KVPool, q, out, block_tables, seq_lens, max_
                                        int(max_seq_len), float(sm_scale), int(num_splits),
                                        _ptr(dev_err), _stream(stream))
     _check(st, "paged_decode_attn_noalloc")
+
+
+def kvq_decode_step_workspace_size(batch, q_heads, kv_heads, max_seq_len, num_splits=0,
+                                   head_dim=HEAD_DIM) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().kvq_decode_step_workspace_size(batch, q_heads, kv_heads, head_dim, max_seq_len,
+                                               num_splits, ctypes.byref(n))
+    _check(st, "kvq_decode_step_workspace_size")
+    return int(n.value)
+
+
+def kvq_decode_step_fused(batch: int, num_tokens: int) -> bool:
+    """Whether kvq_decode_step runs as one launch for this many requests and
+    stored tokens (else as four kernels); see kvq.h."""
+    return bool(load().kvq_decode_step_fused(int(batch), int(num_tokens)))
+
+
+def kvq_decode_step(pool: KVPool, req_to_token, req_pool_indices, seq_lens, block_tables, k_new,
+                    v_new, slot_mapping, q, out, max_seq_len, sm_scale, num_splits=0,
+                    workspace=None, dev_err=None, stream=None):
+    """One decode step in one launch: block_tables [B, max_blocks] from the
+    ReqToTokenPool rows, the store of k_new/v_new [N, Hkv, D] (q's dtype) at
+    slot_mapping, then out[b, h] = attention of q[b, h] over the pool; see
+    kvq.h."""
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype or out.dtype != q.dtype:
+        raise ValueError("kvq_decode_step: k_new, v_new and out must have q's dtype")
+    lib = load()
+    ps = pool.c_struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kvq_decode_step(
+        ctypes.byref(ps), _ptr(req_to_token), int(req_to_token.shape[0]),
+        int(req_to_token.shape[1]), _ptr(req_pool_indices), _ptr(seq_lens),
+        int(seq_lens.numel()), _ptr(block_tables), int(block_tables.shape[1]), _ptr(k_new),
+        _ptr(v_new), _ptr(slot_mapping), int(slot_mapping.numel()), _ptr(q), _dtype_code(q),
+        _ptr(out), int(q.shape[1]), int(max_seq_len), float(sm_scale), int(num_splits),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check(st, "kvq_decode_step")
 
 
 def paged_decode_attn_shared_prefix_workspace_size(batch, q_heads, kv_heads, max_seq_len,
@@ -426,27 +472,39 @@ class DecodeStep:
     """One decode step of a layer through the C ABI: block tables, store, attention.
 
     Holds the per-step device buffers (block tables, workspace, error word) so
-    the call itself allocates nothing.
+    the call itself allocates nothing. fused=True runs the step as the one
+    cooperative launch of kvq_decode_step; otherwise as its three calls.
     """
 
     def __init__(self, pool: KVPool, batch: int, q_heads: int, max_blocks_per_seq: int,
-                 max_seq_len: int, q_dtype, num_splits: int = 0, device="cuda"):
+                 max_seq_len: int, q_dtype, num_splits: int = 0, device="cuda",
+                 fused: bool = False):
         import torch
         self.pool = pool
         self.batch = batch
         self.q_heads = q_heads
         self.max_seq_len = max_seq_len
         self.num_splits = num_splits
+        self.fused = fused
         self.block_tables = torch.empty((batch, max_blocks_per_seq), dtype=torch.int32,
                                         device=device)
         ws = paged_decode_attn_workspace_size(batch, q_heads, pool.kv_heads, max_seq_len,
                                               num_splits)
+        if fused:
+            ws = max(ws, kvq_decode_step_workspace_size(batch, q_heads, pool.kv_heads,
+                                                        max_seq_len, num_splits))
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
         self.out = torch.empty((batch, q_heads, pool.head_dim), dtype=q_dtype, device=device)
 
     def __call__(self, req_to_token, req_pool_indices, seq_lens, q, k_new, v_new, slot_mapping,
                  sm_scale, stream=None):
+        if self.fused:
+            kvq_decode_step(self.pool, req_to_token, req_pool_indices, seq_lens,
+                            self.block_tables, k_new, v_new, slot_mapping, q, self.out,
+                            self.max_seq_len, sm_scale, self.num_splits, self.workspace,
+                            self.dev_err, stream)
+            return self.out
         kvq_block_tables_from_req_to_token(req_to_token, req_pool_indices, seq_lens,
                                            self.block_tables, self.dev_err, stream)
         kv_store_quant(self.pool, k_new, v_new, slot_mapping, self.dev_err, stream)

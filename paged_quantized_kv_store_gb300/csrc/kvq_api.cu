@@ -124,12 +124,24 @@ SharedPrefixLayout shared_prefix_layout(const kvq_decode_plan& plan, int batch, 
 }
 
 // Decode attention, plain (pd == nullptr) or with shared prefixes.
+// The fused step's first phase (block tables and the store of the new
+// tokens), when the decode runs as one launch with them.
+struct StepPre {
+  kvq::TablesArgs t;
+  kvq::StoreArgs st;
+};
+
+// Workspace of the fused step: the decode's, then its barrier counter.
+size_t step_workspace(const kvq_decode_plan& plan) {
+  return align_up(plan.workspace_bytes, 256) + 256;
+}
+
 kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                        const int32_t* seq_lens, int32_t batch, int32_t q_heads,
                        int32_t max_seq_len, float sm_scale, int32_t num_splits,
                        const PrefixDesc* pd, void* workspace, size_t workspace_bytes,
-                       int32_t* dev_err, void* stream) {
+                       int32_t* dev_err, void* stream, const StepPre* pre = nullptr) {
   const kvq_status ps = check_pool(pool);
   if (ps != KVQ_OK) return ps;
   if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
@@ -148,7 +160,8 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
   const SharedPrefixLayout lay =
       shared_prefix_layout(plan, batch, q_heads, pd != nullptr ? pd->max_shared : 0);
-  const size_t need = pd != nullptr ? lay.total : plan.workspace_bytes;
+  const size_t need =
+      pd != nullptr ? lay.total : (pre != nullptr ? step_workspace(plan) : plan.workspace_bytes);
   if (workspace == nullptr || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
@@ -206,6 +219,24 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
     if (pper_sm <= 0) return KVQ_ERR_CUDA;
     if (kvq::launch_prefix(a, pool->kv_dtype, q_dtype, plan.num_sms * pper_sm, s) != cudaSuccess)
       return KVQ_ERR_CUDA;
+  }
+  if (pre != nullptr) {
+    // one cooperative launch: tables + store, barrier, decode, barrier, combine
+    kvq::StepArgs sa;
+    sa.t = pre->t;
+    sa.st = pre->st;
+    sa.d = a;
+    sa.barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
+                                                 align_up(plan.workspace_bytes, 256));
+    if (cudaMemsetAsync(sa.barrier, 0, sizeof(unsigned int), s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    const int sper_sm = std::min(kvq::step_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
+                                 kvq::kMaxCtasPerSm);
+    if (sper_sm <= 0) return KVQ_ERR_CUDA;
+    return kvq::launch_step(sa, pool->kv_dtype, q_dtype, plan.num_sms * sper_sm, s) ==
+                   cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
   }
   // persistent grid: as many CTAs as fit on the device at once (the
   // workspace has partial slots for kMaxCtasPerSm per SM)
@@ -501,6 +532,80 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   return kvq::launch_extend(a, pool->kv_dtype, q_dtype, sms * per_sm, s) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_decode_step_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads,
+                                          int32_t head_dim, int32_t max_seq_len,
+                                          int32_t num_splits, size_t* bytes) {
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  *bytes = 0;
+  kvq_decode_plan plan;
+  const kvq_status st = paged_decode_attn_plan(batch, q_heads, kv_heads, head_dim, max_seq_len,
+                                               num_splits, 0, &plan);
+  if (st != KVQ_OK) return st;
+  *bytes = step_workspace(plan);
+  return KVQ_OK;
+}
+
+int32_t kvq_decode_step_fused(int32_t batch, int64_t num_tokens) {
+  return batch > 0 && num_tokens <= 2 * static_cast<int64_t>(batch) ? 1 : 0;
+}
+
+kvq_status kvq_decode_step(const kvq_pool* pool, const int32_t* req_to_token,
+                           int32_t num_req_slots, int32_t max_context_len,
+                           const int32_t* req_pool_indices, const int32_t* seq_lens,
+                           int32_t batch, int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           int64_t num_tokens, const void* q, int32_t q_dtype, void* out,
+                           int32_t q_heads, int32_t max_seq_len, float sm_scale,
+                           int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_err, void* stream) {
+  const kvq_status ps = check_pool(pool);
+  if (ps != KVQ_OK) return ps;
+  if (num_req_slots < 0 || max_context_len < 0 || num_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (!is_float16(q_dtype)) return KVQ_ERR_UNSUPPORTED;
+  if (batch > 0 && (req_to_token == nullptr || req_pool_indices == nullptr))
+    return KVQ_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr)
+      return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  }
+  if (batch < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0)  // nothing to attend: the step is the store alone
+    return kv_store_quant(pool, k_new, v_new, q_dtype, slot_mapping, num_tokens, dev_err, stream);
+  if (!kvq_decode_step_fused(batch, num_tokens)) {
+    // a prefill chunk rides along: its store runs at full occupancy in a
+    // kernel of its own, and so do the tables and the attention
+    kvq_status st = kvq_block_tables_from_req_to_token(
+        req_to_token, num_req_slots, max_context_len, req_pool_indices, seq_lens, batch,
+        max_blocks_per_seq, block_tables, dev_err, stream);
+    if (st != KVQ_OK) return st;
+    st = kv_store_quant(pool, k_new, v_new, q_dtype, slot_mapping, num_tokens, dev_err, stream);
+    if (st != KVQ_OK) return st;
+    return decode_impl(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                       q_heads, max_seq_len, sm_scale, num_splits, nullptr, workspace,
+                       workspace_bytes, dev_err, stream);
+  }
+  StepPre pre;
+  pre.t = kvq::TablesArgs{req_to_token, num_req_slots, max_context_len, req_pool_indices,
+                          seq_lens, batch, max_blocks_per_seq, block_tables, dev_err};
+  pre.st.k_pool = pool->k;
+  pre.st.v_pool = pool->v;
+  pre.st.k_sz = pool->k_sz;
+  pre.st.v_sz = pool->v_sz;
+  pre.st.num_blocks = pool->num_blocks;
+  pre.st.kv_heads = pool->kv_heads;
+  pre.st.kv_dtype = pool->kv_dtype;
+  pre.st.in_dtype = q_dtype;  // the new rows come in Q's dtype
+  pre.st.k_new = k_new;
+  pre.st.v_new = v_new;
+  pre.st.slot_mapping = slot_mapping;
+  pre.st.num_tokens = num_tokens;
+  pre.st.dev_err = dev_err;
+  return decode_impl(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens, batch,
+                     q_heads, max_seq_len, sm_scale, num_splits, nullptr, workspace,
+                     workspace_bytes, dev_err, stream, &pre);
 }
 
 kvq_status kvq_copy_blocks(const kvq_pool* src, const kvq_pool* dst, const int32_t* src_ids,

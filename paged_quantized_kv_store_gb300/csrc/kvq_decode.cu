@@ -53,6 +53,8 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_store_row.cuh"
+#include "kvq_tables_item.cuh"
 #include "kvq_tile.cuh"
 
 namespace kvq {
@@ -146,11 +148,11 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch
   } while (c.nblk == 0);
 }
 
+// The decode of CTA `cta` out of `ncta` (the persistent grid); dsmem is the
+// CTA's dynamic shared memory, warp_sum 4 ints of static shared memory.
 template <int KV, bool QBF>
-__global__ void __launch_bounds__(kDecodeThreads)
-    decode_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ __align__(128) unsigned char dsmem[];
-  __shared__ int32_t warp_sum[kWarps];
+__device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* dsmem,
+                                            int32_t* warp_sum, int cta, int ncta) {
   using S = Stage<KV>;
   constexpr bool kQuant = KvTraits<KV>::kQuant;
   constexpr bool kPvBf = KV == kBF16;  // P.V product type: bf16 only for bf16 pools
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     int sum = 0;
     for (int b = b0; b < b1; ++b) {
       sum += own_blocks(a, b);
-      if (blockIdx.x == 0 && a.seq_lens[b] > a.len_cap) report(a.dev_err, KVQ_DEV_ERR_LENGTH);
+      if (cta == 0 && a.seq_lens[b] > a.len_cap) report(a.dev_err, KVQ_DEV_ERR_LENGTH);
     }
     int incl = sum;
 #pragma unroll
@@ -196,11 +198,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int tb = cum[a.batch];  // blocks of one q-head group over all requests
   const int groups = a.kv_heads * a.head_groups;
   const int64_t total = static_cast<int64_t>(tb) * groups;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t nwarps = static_cast<int64_t>(ncta) * kWarps;
   const int64_t even_share = (total + nwarps - 1) / nwarps;
   const int P = static_cast<int>(even_share > a.min_blocks_per_warp ? even_share
                                                                     : a.min_blocks_per_warp);
-  if (blockIdx.x == 0) {
+  if (cta == 0) {
     // what the combine kernel needs, and the all-zero rows of empty requests
     // (a request whose only blocks are shared ones is written by the combine
     // kernel)
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   }
 
   // ---- this warp's range [x0, x0 + n) of the stream -----------------------------
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t gw = static_cast<int64_t>(cta) * kWarps + warp;
   const int64_t x0 = gw * P;
   if (x0 >= total) return;  // no block barrier follows: warps are independent from here
   const int n = static_cast<int>(total - x0 < P ? total - x0 : P);
@@ -543,17 +545,81 @@ __global__ void __launch_bounds__(kDecodeThreads)
   flush();
 }
 
-// One warp per (request, q head): merges the pieces of a request that the
-// decode kernel did not finish itself: the split-K records of the warps its
+template <int KV, bool QBF>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ int32_t warp_sum[kWarps];
+  decode_body<KV, QBF>(a, dsmem, warp_sum, blockIdx.x, gridDim.x);
+}
+
+// The merge of one (request, q head) row that the decode did not finish
+// itself, by one warp: the split-K records of the warps its
 // blocks were split between (slot 1 for the first when the request starts
 // inside that warp's range), then its shared-prefix records, if any (a
 // request made of shared blocks only has nothing else). Log-sum-exp in the
 // exp2 domain; the pieces' maxima and sums are read in one round, one piece
 // per lane.
 template <bool QBF>
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t bh, int hh, int lane,
+                                             int64_t w_first, int64_t nd, int64_t seg_start,
+                                             int P, int npc) {
+  auto rec_of = [&](int64_t i) -> const float* {
+    if (i < nd) {
+      const int slot = (i == 0 && seg_start != w_first * P) ? 1 : 0;
+      return a.part + (((w_first + i) * 2 + slot) * a.hpg + hh) * kPartStride;
+    }
+    return a.ppart + (bh * a.pmax_chunks + (i - nd)) * kPartStride;
+  };
+  const int64_t npieces = nd + npc;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f, M = -INFINITY;
+  constexpr int kBatch = 8;  // pieces whose loads are in flight together
+  for (int64_t base = 0; base < npieces; base += kBatch) {
+    // every lane reads each piece's maximum and sum (one address: broadcast)
+    // and its own 4 columns, all loads of the batch issued before any use;
+    // through L2, as other SMs wrote the records
+    float mm[kBatch], ll[kBatch];
+    float4 x[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      mm[i] = -INFINITY;
+      ll[i] = 0.f;
+      x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (base + i < npieces) {
+        const float* rec = rec_of(base + i);
+        mm[i] = __ldcg(rec + kHeadDim);
+        ll[i] = __ldcg(rec + kHeadDim + 1);
+        x[i] = __ldcg(reinterpret_cast<const float4*>(rec) + lane);
+      }
+    }
+    float Mb = mm[0];
+#pragma unroll
+    for (int i = 1; i < kBatch; ++i) Mb = fmaxf(Mb, mm[i]);
+    const float Mn = fmaxf(M, Mb);
+    if (Mn == -INFINITY) continue;
+    if (M != Mn && M != -INFINITY) {  // this batch raised the maximum
+      const float al = exp2f(M - Mn);
+      lsum *= al;
+      acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
+    }
+    M = Mn;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float e = mm[i] == -INFINITY ? 0.f : exp2f(mm[i] - M);
+      lsum += e * ll[i];
+      acc.x += e * x[i].x; acc.y += e * x[i].y; acc.z += e * x[i].z; acc.w += e * x[i].w;
+    }
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  uint2 w;
+  w.x = pack2<QBF>(acc.x * inv, acc.y * inv);
+  w.y = pack2<QBF>(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + bh * kHeadDim)[lane] = w;
+}
+
+template <bool QBF>
+__device__ __forceinline__ void combine_row(const DecodeArgs& a, int64_t bh, int lane) {
   if (bh >= static_cast<int64_t>(a.batch) * a.q_heads) return;
   const int b = static_cast<int>(bh / a.q_heads);
   const int hq = static_cast<int>(bh - static_cast<int64_t>(b) * a.q_heads);
@@ -574,52 +640,129 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     if (w_first == w_last) return;  // one warp: written by the decode kernel
     nd = w_last - w_first + 1;
   }
-  auto rec_of = [&](int64_t i) -> const float* {
-    if (i < nd) {
-      const int slot = (i == 0 && seg_start != w_first * P) ? 1 : 0;
-      return a.part + (((w_first + i) * 2 + slot) * a.hpg + hh) * kPartStride;
+  merge_pieces<QBF>(a, bh, hh, lane, w_first, nd, seg_start, P, npc);
+}
+
+template <bool QBF>
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeArgs a) {
+  combine_row<QBF>(a, static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5),
+                   threadIdx.x & 31);
+}
+
+// ---- the fused step ------------------------------------------------------------
+
+constexpr int kStepUnroll = 4;  // table entries / pool rows a half-warp has in flight
+
+// Grid-wide barrier of a cooperative launch: thread 0 of every CTA counts in
+// and waits, with acquire loads, until `target` CTAs have; the wait gives up
+// after 2 s (KVQ_DEV_ERR_TIMEOUT, false: the caller stops).
+__device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target,
+                                          int32_t* dev_err) {
+  __shared__ int ok_s;
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // global writes before TMA reads
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if (global_ns() - t0 > 2000000000ull) {
+        ok = 0;
+        report(dev_err, KVQ_DEV_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(128);
     }
-    return a.ppart + (bh * a.pmax_chunks + (i - nd)) * kPartStride;
-  };
-  const int64_t npieces = nd + npc;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f, M = -INFINITY;
-  for (int64_t base = 0; base < npieces; base += 32) {
-    // this batch's maxima and sums, one piece per lane
-    float mw = -INFINITY, lw = 0.f;
-    if (base + lane < npieces) {
-      const float* rec = rec_of(base + lane);
-      mw = rec[kHeadDim];
-      lw = rec[kHeadDim + 1];
-    }
-    float Mb = mw;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(kFull, Mb, off));
-    const float Mn = fmaxf(M, Mb);
-    if (Mn == -INFINITY) continue;
-    if (M != Mn && M != -INFINITY) {  // a later batch raised the maximum
-      const float al = exp2f(M - Mn);
-      lsum *= al;
-      acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
-    }
-    M = Mn;
-    const float e = mw == -INFINITY ? 0.f : exp2f(mw - M);
-    lsum += e * lw;
-    const int cnt = static_cast<int>(npieces - base < 32 ? npieces - base : 32);
-#pragma unroll 8
-    for (int i = 0; i < cnt; ++i) {
-      const float ei = __shfl_sync(kFull, e, i);
-      const float4 x = reinterpret_cast<const float4*>(rec_of(base + i))[lane];
-      acc.x += ei * x.x; acc.y += ei * x.y; acc.z += ei * x.z; acc.w += ei * x.w;
-    }
+    __threadfence();
+    ok_s = ok;
   }
+  __syncthreads();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return ok_s != 0;
+}
+
+// One decode step: (1) block tables and the quantizing store of the new
+// tokens, spread over the whole grid; (2) the decode, as decode_kernel; (3)
+// the combine, one warp per (request, q head). The phases are separated by
+// grid barriers, so the step is one launch instead of four.
+template <int KV, bool QBF>
+__global__ void __launch_bounds__(kDecodeThreads, KvTraits<KV>::kQuant ? kMaxCtasPerSm : 3)
+    step_kernel(const __grid_constant__ StepArgs s) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ int32_t warp_sum[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + (tid >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  // (1) block tables, then the store: a half-warp per table entry and per pool
+  // row, kStepUnroll of them with their loads in flight together
+  const int lane16 = lane & 15;
+  const int64_t hw = 2 * gwarp + (lane >> 4), nhw = 2 * nwarps;
+  const int64_t entries = static_cast<int64_t>(s.t.batch) * s.t.max_blocks_per_seq;
+  for (int64_t i = hw; i < entries; i += kStepUnroll * nhw)
+    tables_blocks<kStepUnroll>(s.t, i, nhw, lane16);
+  const int64_t rows = s.st.num_tokens * 2 * s.st.kv_heads;
+  for (int64_t r = hw; r < rows; r += kStepUnroll * nhw) {
+    RowIn in[kStepUnroll];
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  uint2 w;
-  w.x = pack2<QBF>(acc.x * inv, acc.y * inv);
-  w.y = pack2<QBF>(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + bh * kHeadDim)[lane] = w;
+    for (int u = 0; u < kStepUnroll; ++u) in[u] = load_row<KV, QBF>(s.st, r + u * nhw, lane16);
+#pragma unroll
+    for (int u = 0; u < kStepUnroll; ++u) write_row<KV, QBF>(s.st, in[u], lane16);
+  }
+  if (!grid_sync(s.barrier, gridDim.x, s.d.dev_err)) return;
+  // (2) decode
+  decode_body<KV, QBF>(s.d, dsmem, warp_sum, blockIdx.x, gridDim.x);
+  if (!grid_sync(s.barrier, 2 * gridDim.x, s.d.dev_err)) return;
+  // (3) combine
+  for (int64_t bh = gwarp; bh < static_cast<int64_t>(s.d.batch) * s.d.q_heads; bh += nwarps)
+    combine_row<QBF>(s.d, bh, lane);
+}
+
+template <int KV, bool QBF>
+cudaError_t launch_step_t(const StepArgs& a, int grid, cudaStream_t s) {
+  static int opted_in_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (opted_in_device != dev) {
+    e = cudaFuncSetAttribute(step_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
+    if (e != cudaSuccess) return e;
+    opted_in_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem_bytes_for<KV>(a.d.batch);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;  // every CTA resident: the barriers need it
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<KV, QBF>, a);
+}
+
+template <int KV, bool QBF>
+int step_occupancy_t(int batch) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  if (dev == cached_dev && batch == cached_batch) return cached_n;
+  if (cudaFuncSetAttribute(step_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<KV, QBF>, kDecodeThreads,
+                                                    smem_bytes_for<KV>(batch)) != cudaSuccess)
+    return 0;
+  cached_dev = dev;
+  cached_batch = batch;
+  cached_n = n;
+  return n;
 }
 
 template <int KV, bool QBF>
@@ -687,6 +830,34 @@ cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
   else
     combine_kernel<false><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid,
+                        cudaStream_t s) {
+  const bool qbf = q_dtype == kBF16;
+  switch (kv_dtype) {
+    case kF16:
+      return launch_step_t<kF16, false>(a, grid, s);
+    case kBF16:
+      return launch_step_t<kBF16, true>(a, grid, s);
+    case kI8:
+      return qbf ? launch_step_t<kI8, true>(a, grid, s) : launch_step_t<kI8, false>(a, grid, s);
+    case kI4:
+      return qbf ? launch_step_t<kI4, true>(a, grid, s) : launch_step_t<kI4, false>(a, grid, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch) {
+  const bool qbf = q_dtype == kBF16;
+  switch (kv_dtype) {
+    case kF16: return step_occupancy_t<kF16, false>(batch);
+    case kBF16: return step_occupancy_t<kBF16, true>(batch);
+    case kI8: return qbf ? step_occupancy_t<kI8, true>(batch) : step_occupancy_t<kI8, false>(batch);
+    case kI4: return qbf ? step_occupancy_t<kI4, true>(batch) : step_occupancy_t<kI4, false>(batch);
+    default: return 0;
+  }
 }
 
 int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch) {

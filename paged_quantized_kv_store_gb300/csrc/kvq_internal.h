@@ -132,7 +132,20 @@ struct ExtendArgs {
   int32_t* dev_err;
 };
 
+// One decode step in a single cooperative launch: block tables, the store of
+// the step's new tokens, decode and combine, separated by grid barriers.
+struct StepArgs {
+  TablesArgs t;
+  StoreArgs st;
+  DecodeArgs d;
+  unsigned int* barrier;  // zero at launch
+};
+
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+// kv_dtype / q_dtype as for launch_decode (the new rows have Q's dtype)
+cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
+                        cudaStream_t s);
+int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
 cudaError_t launch_extend(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                           cudaStream_t s);
 int extend_ctas_per_sm(int kv_dtype, int q_dtype, int batch);

@@ -223,3 +223,45 @@ def test_extend_validation(lib):
     assert call(q=p + 8) == 1              # misaligned
     assert call(var=3) == 1 and call(var=-1) == 1
     assert call(var=2, pool=_pool(kv_dtype=kvq.KVQ_BF16), q_dtype=kvq.KVQ_BF16) == 2
+
+
+def test_decode_step_validation(lib):
+    f = lib.kvq_decode_step
+    p = 256
+    args = dict(r2t=p, nslots=4, mctx=64, rpi=p, sl=p, batch=2, bt=p, mb=4, k=p, v=p, sm=p,
+                ntok=2, q=p, q_dtype=0, out=p, hq=4, msl=64, scale=0.1, splits=0, ws=None,
+                wsb=0, err=None, s=None)
+
+    def call(pool=None, **kw):
+        a = dict(args)
+        a.update(kw)
+        return f(ctypes.byref(pool or _pool()), a["r2t"], a["nslots"], a["mctx"], a["rpi"],
+                 a["sl"], a["batch"], a["bt"], a["mb"], a["k"], a["v"], a["sm"], a["ntok"],
+                 a["q"], a["q_dtype"], a["out"], a["hq"], a["msl"], a["scale"], a["splits"],
+                 a["ws"], a["wsb"], a["err"], a["s"])
+
+    assert f(None, *args.values()) == 1        # args are in the C order
+    assert call(q_dtype=kvq.KVQ_INT8) == 2
+    assert call(k=None) == 1 and call(sm=None) == 1
+    assert call(v=p + 4) == 1                     # misaligned new rows
+    assert call(batch=-1) == 1 and call(ntok=-1) == 1 and call(nslots=-1) == 1
+    assert call(rpi=None) == 1
+    assert call(batch=0, ntok=0) == 0             # nothing to do
+    # no requests: the step is the store, which refuses a 16-bit pool of another dtype
+    assert call(pool=_pool(kv_dtype=kvq.KVQ_F16), q_dtype=kvq.KVQ_BF16, batch=0) == 2
+    n = ctypes.c_size_t(7)
+    g = lib.kvq_decode_step_workspace_size
+    assert g(2, 4, 2, 128, 64, 0, None) == 1
+    assert g(-1, 4, 2, 128, 64, 0, ctypes.byref(n)) == 1 and n.value == 0
+    assert g(2, 3, 2, 128, 64, 0, ctypes.byref(n)) == 1
+    assert g(2, 4, 2, 256, 64, 0, ctypes.byref(n)) == 2
+
+
+def test_decode_step_form(lib):
+    """One launch for a decode batch's tokens, four kernels with a prefill chunk."""
+    assert lib.kvq_decode_step_fused(4, 4) == 1
+    assert lib.kvq_decode_step_fused(4, 8) == 1
+    assert lib.kvq_decode_step_fused(4, 9) == 0
+    assert lib.kvq_decode_step_fused(256, 4352) == 0
+    assert lib.kvq_decode_step_fused(0, 0) == 0
+    assert kvq.kvq_decode_step_fused(128, 128) is True

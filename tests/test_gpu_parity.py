@@ -278,3 +278,52 @@ def test_full_size_sampled(gpu, name):
             if key.endswith("_sz"):
                 g = g.view(np.uint16).reshape(g.shape + (2,))
             assert np.array_equal(g, getattr(opool, key)[blk]), key
+
+
+def _near_tie_rows(kv_dtype, in_dtype, n_rows, seed):
+    """Rows whose codes (x - Z) / S sit on or next to rounding ties k + 1/2:
+    each row's min and max set the scale, the other 126 elements are the
+    representable inputs in between whose quotients are nearest a tie."""
+    qmax = 255 if kv_dtype == "int8" else 15
+    bits = np.arange(65536, dtype=np.uint32)
+    if in_dtype == "f16":
+        with np.errstate(invalid="ignore"):
+            vals = bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    else:
+        vals = (bits << 16).view(np.float32)
+    ok = np.isfinite(vals)
+    rng = np.random.default_rng(seed)
+    rows = np.empty((n_rows, 128), np.uint16)
+    for r in range(n_rows):
+        if r == 0:
+            mn, mx = 0.0, float(qmax)  # S = 1: exact ties
+        else:
+            mn = float(rng.uniform(-4, 1))
+            mx = mn + float(rng.uniform(0.01, 8))
+        sel = ok & (vals >= mn) & (vals <= mx)
+        cand, cbits = vals[sel], bits[sel].astype(np.uint16)
+        lo, hi = cand.min(), cand.max()
+        S = np.float32(np.float16(np.float32(np.float32(hi) - np.float32(lo)) / np.float32(qmax)))
+        Z = np.float32(np.float16(lo))
+        q = (cand.astype(np.float64) - float(Z)) / float(S)
+        dist = np.abs(q - np.floor(q) - 0.5)
+        pick = np.resize(cbits[np.argsort(dist, kind="stable")], 126)  # repeats in a narrow range
+        rows[r] = np.concatenate([[cbits[cand.argmin()], cbits[cand.argmax()]], pick])
+    return rows
+
+
+@pytest.mark.parametrize("kv_dtype", ["int8", "int4"])
+@pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
+def test_store_rounding_ties(gpu, kv_dtype, in_dtype):
+    """Inputs on and next to rounding ties: the stored codes must equal the
+    oracle's (a correctly rounded fp32 division, round half to even)."""
+    N, Hkv = 48, 2
+    rows = _near_tie_rows(kv_dtype, in_dtype, 2 * N * Hkv, seed=81)
+    k = rows[:N * Hkv].reshape(N, Hkv, 128)
+    v = rows[N * Hkv:].reshape(N, Hkv, 128)
+    slots = np.arange(N, dtype=np.int64) * 3 % (4 * 16)
+    pool = gpu.KVPool.allocate(4, Hkv, kv_dtype)
+    gpu.kv_store_quant(pool, to_dev(k, in_dtype), to_dev(v, in_dtype), i64(slots))
+    opool = oracle.Pool(4, Hkv, 128, kv_dtype)
+    oracle.kv_store(opool, k, v, in_dtype, slots)
+    _compare_pools(pool, opool)
