@@ -213,11 +213,16 @@ def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh"))
     return src.hexdigest()[:16]
 
 
-def traffic_from_profile(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
+STEP_SOURCES = ("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh", "kvq_store_row.cuh",
+                "kvq_tables_item.cuh")
+
+
+def traffic_from_profile(workload: str, kind: str = "decode"):
+    """DRAM bytes per launch of the decode kernel (kind "decode") or of the
+    fused step kernel (kind "step") from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
-    sha = kernel_source_sha()
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+    sha = kernel_source_sha() if kind == "decode" else kernel_source_sha(STEP_SOURCES)
+    path = os.path.join(ROOT, "profiles", f"{kind}_{workload}_traffic.txt")
     try:
         text = open(path).read()
     except OSError:
@@ -666,7 +671,8 @@ def run_ours(args, rank: int, world: int, dist):
     mean_decode_ms = float(np.mean(decode_ms))
     peak, peak_kind = measured_peak()
     achieved = alg / (mean_decode_ms / 1e3) / 1e9
-    traffic, sha = traffic_from_profile(wl.name)
+    single = args.fused_step and launches_per_step == 1
+    traffic, sha = traffic_from_profile(wl.name, "step" if single else "decode")
     roofline = {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "traffic": traffic,
