@@ -148,9 +148,13 @@ kvq_status kvq_block_tables_from_req_to_token(const int32_t* req_to_token,
  * Launch plan of paged_decode_attn (host-only arithmetic; no device access
  * when num_sms > 0). The decode work is one stream of (kv head, q-head group,
  * request, block) items; a persistent grid of warps cuts it into equal
- * contiguous ranges, at least min_blocks_per_warp blocks each. A warp writes
- * the output of every request it covers completely and, for the first and
- * last request of its range, a partial result (running max, sum,
+ * contiguous ranges, at least min_blocks_per_warp blocks each. With an
+ * automatic split and at least 16 blocks per warp, the static ranges cover
+ * about nine tenths of the stream and the rest is cut into tail chunks of 4
+ * to 8 (or more) blocks that warps take from a counter as they finish, so
+ * that warps running at different speeds end together. A warp writes the
+ * output of every request a range covers completely and, for the first and
+ * last request of the range, a partial result (running max, sum,
  * unnormalised output) that a combine kernel merges with a log-sum-exp.
  *  num_splits : 0 = automatic; else requests are cut into at most
  *               num_splits + 1 pieces (min_blocks_per_warp =
@@ -164,7 +168,8 @@ typedef struct kvq_decode_plan {
   int32_t heads_per_group;     /* min(q_heads / kv_heads, 8) */
   int32_t num_sms;
   int32_t max_ctas_per_sm;     /* persistent CTAs per SM the workspace allows */
-  size_t workspace_bytes;      /* header (lengths prefix) + 2 partial slots per warp */
+  size_t workspace_bytes;      /* counters, header (lengths prefix), 2 partial slots per
+                                  range for 5 ranges per warp (static + tail) */
 } kvq_decode_plan;
 
 kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_heads,
@@ -192,9 +197,11 @@ size_t paged_decode_attn_workspace_size(int32_t batch, int32_t q_heads, int32_t 
  *                 requests are clamped and flagged KVQ_DEV_ERR_LENGTH.
  *  sm_scale     : softmax scale (e.g. 1/sqrt(head_dim)).
  *  num_splits   : as in paged_decode_attn_plan.
- *  workspace    : device scratch of at least
- *                 paged_decode_attn_workspace_size(...) bytes (may be NULL
- *                 when that is 0), 16-byte aligned.
+ *  workspace    : device scratch of paged_decode_attn_workspace_size(...)
+ *                 bytes, 16-byte aligned. A smaller one is accepted down to
+ *                 one range per warp (256 + header + warps * 2 *
+ *                 heads_per_group * 132 floats) and then runs without the
+ *                 tail; below that KVQ_ERR_WORKSPACE.
  * For request b and q head h (kv head h / (q_heads / kv_heads)):
  *   out[b][h] = sum_t softmax_t(sm_scale * q . k_t) v_t over t < seq_lens[b],
  * with k_t, v_t read from slot block_tables[b][t / 16] * 16 + t % 16 and
@@ -269,9 +276,9 @@ kvq_status paged_decode_attn_shared_prefix(
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
- *  - Sizes whose paged_decode_attn_workspace_size exceeds
- *    KVQ_NOALLOC_SCRATCH_BYTES are rejected with KVQ_ERR_WORKSPACE before
- *    anything is launched.
+ *  - Sizes whose static ranges alone need more than KVQ_NOALLOC_SCRATCH_BYTES
+ *    are rejected with KVQ_ERR_WORKSPACE before anything is launched; sizes
+ *    whose full workspace does not fit run without the tail.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero (every entry read is first written
  *    by the same call). Calls whose work overlaps on the GPU (other streams,
@@ -350,7 +357,8 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
  * launch: every CTA resident; each barrier wait gives up after 2 s with
  * KVQ_DEV_ERR_TIMEOUT). Arguments mean what they mean for the three calls it
  * replaces; block_tables is written. The workspace is at least *bytes of
- * kvq_decode_step_workspace_size (the decode's plus a barrier counter).
+ * kvq_decode_step_workspace_size (the decode's; its barrier counter sits in
+ * the workspace's counters).
  * The single launch is used when the step stores at most two tokens per
  * request (kvq_decode_step_fused): its first phase runs at the attention's
  * occupancy, which suits a decode batch's new tokens but not a prefill chunk

@@ -20,6 +20,21 @@ namespace {
 
 constexpr int kAutoMinBlocksPerWarp = 4;  // a warp's range is never shorter than this
 
+// Decode workspace: [256 bytes: the tail-chunk counter, the fused step's
+// barrier counter][header: 4 ints + batch + 1 prefix sums][partial records:
+// 2 per q head of the group slot, per range; kRangesPerWarp ranges per warp of
+// the plan, at least one (the static ranges alone) for a smaller workspace].
+constexpr size_t kCounterBytes = 256;
+
+size_t decode_records_offset(int32_t batch) {
+  return kCounterBytes +
+         (static_cast<size_t>(batch + kvq::kHdrCum + 1) * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+size_t range_record_bytes(const kvq_decode_plan& p) {
+  return static_cast<size_t>(2) * p.heads_per_group * kvq::kPartStride * sizeof(float);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool is_quant(int dt) { return dt == KVQ_INT8 || dt == KVQ_INT4; }
@@ -131,10 +146,9 @@ struct StepPre {
   kvq::StoreArgs st;
 };
 
-// Workspace of the fused step: the decode's, then its barrier counter.
-size_t step_workspace(const kvq_decode_plan& plan) {
-  return align_up(plan.workspace_bytes, 256) + 256;
-}
+// Workspace of the fused step: the decode's (its barrier counter sits in the
+// counters at the start).
+size_t step_workspace(const kvq_decode_plan& plan) { return plan.workspace_bytes; }
 
 kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, void* out,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -160,9 +174,13 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
   const SharedPrefixLayout lay =
       shared_prefix_layout(plan, batch, q_heads, pd != nullptr ? pd->max_shared : 0);
-  const size_t need =
-      pd != nullptr ? lay.total : (pre != nullptr ? step_workspace(plan) : plan.workspace_bytes);
+  // the static ranges need one record slot per warp; the plan's size also holds
+  // the tail's
+  const size_t rec = range_record_bytes(plan);
+  const size_t need = pd != nullptr ? lay.total
+                                    : decode_records_offset(batch) + plan.warps * rec;
   if (workspace == nullptr || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  const size_t decode_bytes = pd != nullptr ? plan.workspace_bytes : workspace_bytes;
   if (!aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
   kvq::DecodeArgs a;
@@ -195,12 +213,24 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   const int nblk = std::max(1, (max_seq_len + kBlock - 1) / kBlock);
   a.len_cap = std::min(max_blocks_per_seq, nblk) * kBlock;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  a.hdr = static_cast<int32_t*>(workspace);
-  a.part = reinterpret_cast<float*>(
-      static_cast<char*>(workspace) +
-      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256));
+  a.hdr = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kCounterBytes);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    decode_records_offset(batch));
+  a.max_ranges = std::min<int64_t>(
+      static_cast<int64_t>((decode_bytes - decode_records_offset(batch)) / rec),
+      static_cast<int64_t>(kvq::kRangesPerWarp) * plan.warps);
+  // a tail needs an automatic split (an explicit count keeps every request to
+  // num_splits + 1 pieces) and sizes whose per-warp share can reach
+  // kTailMinShare blocks
+  const int64_t max_total = static_cast<int64_t>(batch) * pool->kv_heads * plan.head_groups *
+                            (a.len_cap / kBlock);
+  const bool tail = num_splits == 0 && max_total >= int64_t{kvq::kTailMinShare} * plan.warps;
+  a.tail_ctr = tail ? static_cast<unsigned int*>(workspace) : nullptr;
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((tail || pre != nullptr) &&
+      cudaMemsetAsync(workspace, 0, 2 * sizeof(unsigned int), s) != cudaSuccess)
+    return KVQ_ERR_CUDA;  // the tail counter and the step's barrier
   if (pd != nullptr && pd->num_groups > 0 && pd->max_shared > 0) {
     a.grp_off = pd->offsets;
     a.grp_mem = pd->members;
@@ -226,11 +256,8 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
     sa.t = pre->t;
     sa.st = pre->st;
     sa.d = a;
-    sa.barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
-                                                 align_up(plan.workspace_bytes, 256));
-    if (cudaMemsetAsync(sa.barrier, 0, sizeof(unsigned int), s) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    const int sper_sm = std::min(kvq::step_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
+    sa.barrier = static_cast<unsigned int*>(workspace) + 1;  // zeroed above
+    const int sper_sm = std::min(kvq::step_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
                                  kvq::kMaxCtasPerSm);
     if (sper_sm <= 0) return KVQ_ERR_CUDA;
     return kvq::launch_step(sa, pool->kv_dtype, q_dtype, plan.num_sms * sper_sm, s) ==
@@ -240,7 +267,7 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   }
   // persistent grid: as many CTAs as fit on the device at once (the
   // workspace has partial slots for kMaxCtasPerSm per SM)
-  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch),
+  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
                               kvq::kMaxCtasPerSm);
   if (per_sm <= 0) return KVQ_ERR_CUDA;
   const int grid = plan.num_sms * per_sm;
@@ -371,9 +398,8 @@ kvq_status paged_decode_attn_plan(int32_t batch, int32_t q_heads, int32_t kv_hea
   plan->num_sms = num_sms;
   plan->max_ctas_per_sm = kvq::kMaxCtasPerSm;
   plan->workspace_bytes =
-      align_up(static_cast<size_t>(batch + 3) * sizeof(int32_t), 256) +
-      static_cast<size_t>(plan->warps) * 2 * plan->heads_per_group * kvq::kPartStride *
-          sizeof(float);
+      decode_records_offset(batch) +
+      static_cast<size_t>(kvq::kRangesPerWarp) * plan->warps * range_record_bytes(*plan);
   return KVQ_OK;
 }
 

@@ -148,9 +148,59 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch
   } while (c.nblk == 0);
 }
 
+// How the block stream is cut into ranges, each ending in at most two partial
+// records per q head. Static part: warp w owns blocks [w Pst, (w + 1) Pst) of
+// the first nwarps * Pst. Tail (C > 0): the rest in chunks of C blocks, taken
+// one at a time from a counter by whichever warp is free, so that warps whose
+// static part ran slower (the co-resident CTAs of an SM do not get equal
+// shares of it) are not waited for. Range ids: warps 0 .. nwarps - 1, then
+// nwarps + tail chunk.
+struct RangeMap {
+  int64_t nwarps;
+  int Pst;        // blocks per static range
+  int C;          // blocks per tail chunk; 0: no tail (static ranges cover all)
+  int64_t ntail;  // tail chunks
+};
+
+__host__ __device__ __forceinline__ int64_t range_of(const RangeMap& m, int64_t x) {
+  if (m.C == 0) return x / m.Pst;
+  const int64_t ns = m.nwarps * m.Pst;
+  return x < ns ? x / m.Pst : m.nwarps + (x - ns) / m.C;
+}
+
+__host__ __device__ __forceinline__ int64_t range_start(const RangeMap& m, int64_t r) {
+  if (m.C == 0 || r < m.nwarps) return r * m.Pst;
+  return m.nwarps * m.Pst + (r - m.nwarps) * m.C;
+}
+
+// The map for `total` blocks over `nwarps` warps with per-warp range length P
+// (the even share, at least the plan's minimum). A tail needs a counter (an
+// automatic split) and P >= kTailMinShare: only long ranges drift apart by
+// more than a short chunk, and a chunk pays a pipeline fill and its own
+// partial records. It takes about a tenth of the blocks, in at most 4 chunks
+// per warp of at least 8 blocks, and is dropped when the workspace holds
+// fewer than nwarps + ntail ranges.
+__device__ __forceinline__ RangeMap make_range_map(const DecodeArgs& a, int64_t total,
+                                                   int64_t nwarps, int P) {
+  RangeMap m{nwarps, P, 0, 0};
+  if (a.tail_ctr == nullptr || P < kTailMinShare) return m;
+  constexpr int c0 = 8;
+  const int64_t per = (9 * total) / (10 * nwarps * c0);  // static chunks per warp
+  const int64_t rem = total - nwarps * per * c0;
+  const int64_t c = max(static_cast<int64_t>(c0), (rem + 4 * nwarps - 1) / (4 * nwarps));
+  const int64_t ntail = (rem + c - 1) / c;
+  if (nwarps + ntail > a.max_ranges) return m;
+  m.Pst = static_cast<int>(per * c0);
+  m.C = static_cast<int>(c);
+  m.ntail = ntail;
+  return m;
+}
+
 // The decode of CTA `cta` out of `ncta` (the persistent grid); dsmem is the
 // CTA's dynamic shared memory, warp_sum 4 ints of static shared memory.
-template <int KV, bool QBF>
+// TAIL: the instantiation that can hand out tail chunks (make_range_map);
+// without it a warp has one range, as the tail-free sizes want.
+template <int KV, bool QBF, bool TAIL>
 __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* dsmem,
                                             int32_t* warp_sum, int cta, int ncta) {
   using S = Stage<KV>;
@@ -202,15 +252,18 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
   const int64_t even_share = (total + nwarps - 1) / nwarps;
   const int P = static_cast<int>(even_share > a.min_blocks_per_warp ? even_share
                                                                     : a.min_blocks_per_warp);
+  const RangeMap rm = TAIL ? make_range_map(a, total, nwarps, P) : RangeMap{nwarps, P, 0, 0};
   if (cta == 0) {
     // what the combine kernel needs, and the all-zero rows of empty requests
     // (a request whose only blocks are shared ones is written by the combine
     // kernel)
     if (tid == 0) {
       a.hdr[0] = tb;
-      a.hdr[1] = P;
+      a.hdr[1] = rm.Pst;
+      a.hdr[2] = rm.C;
+      a.hdr[3] = static_cast<int32_t>(nwarps);
     }
-    for (int b = tid; b <= a.batch; b += kDecodeThreads) a.hdr[2 + b] = cum[b];
+    for (int b = tid; b <= a.batch; b += kDecodeThreads) a.hdr[kHdrCum + b] = cum[b];
     for (int b = 0; b < a.batch; ++b) {
       if (cum[b + 1] != cum[b] || skip_of(a, b) > 0) continue;
       for (int e = tid; e < a.q_heads * kHeadDim; e += kDecodeThreads)
@@ -218,11 +271,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
     }
   }
 
-  // ---- this warp's range [x0, x0 + n) of the stream -----------------------------
+  // ---- this warp's ranges: its static range, then tail chunks ----------------------
+  // (no block barrier follows: warps are independent from here)
   const int64_t gw = static_cast<int64_t>(cta) * kWarps + warp;
-  const int64_t x0 = gw * P;
-  if (x0 >= total) return;  // no block barrier follows: warps are independent from here
-  const int n = static_cast<int>(total - x0 < P ? total - x0 : P);
+  const int64_t static_end = rm.C == 0 ? total : nwarps * rm.Pst;
   // this warp's stage region, 1024-byte aligned (the 128-byte swizzle repeats
   // every 1024 bytes)
   const uint32_t region0 =
@@ -239,6 +291,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
     __syncwarp();
   }
 
+  uint32_t phase = 0;  // parity to wait for, per stage (TMA path), across ranges
+  // the range [x0, x0 + n), its records filed under range id rid; false when a
+  // copy timed out (the warp stops)
+  auto run_range = [&](const int64_t x0, const int n, const int64_t rid) -> bool {
   // issue side: cursor, a 32-entry window of the block table, validity bits
   Cursor ic;
   locate(ic, x0, cum, a.batch, tb);
@@ -246,7 +302,6 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
   int win_b = -1, win_j0 = 0;
   int32_t win = -1;
   uint32_t ok_mask = 0;  // stages holding a valid block in flight
-  uint32_t phase = 0;    // parity to wait for, per stage (TMA path)
   int k_issue = 0;   // next block of the range to issue
   int st_issue = 0;  // its stage
   auto issue_next = [&]() {
@@ -335,7 +390,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
       } else {
         const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
-        float* rec = a.part + ((gw * 2 + slot) * a.hpg + hh) * kPartStride;
+        float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
         float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
 #pragma unroll
         for (int i = 0; i < 8; i += 2)
@@ -362,7 +417,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
           const uint32_t rest = ok_mask & ~(1u << st);
           for (int i = 0; i < D; ++i)
             if ((rest >> i) & 1u) mbar_wait(wr + S::kBarOff + 8 * i, (phase >> i) & 1u);
-          return;
+          return false;
         }
         phase ^= 1u << st;
       }
@@ -543,14 +598,36 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
   }
   if constexpr (!S::kTma) cp_async_wait<0>();
   flush();
+  return true;
+  };  // run_range
+
+  // the static range (the whole share when there is no tail) ...
+  const int64_t xs = gw * rm.Pst;
+  if (xs < static_end &&
+      !run_range(xs, static_cast<int>(min(static_end - xs, static_cast<int64_t>(rm.Pst))), gw))
+    return;
+  if constexpr (TAIL) {
+    if (rm.C == 0) return;
+    // ... then tail chunks while there are any
+    for (;;) {
+      unsigned int c = 0;
+      if (lane == 0) c = atomicAdd(a.tail_ctr, 1u);
+      c = __shfl_sync(kFull, c, 0);
+      if (c >= rm.ntail) return;
+      const int64_t x0 = static_end + static_cast<int64_t>(c) * rm.C;
+      if (!run_range(x0, static_cast<int>(min(total - x0, static_cast<int64_t>(rm.C))),
+                     nwarps + c))
+        return;
+    }
+  }
 }
 
-template <int KV, bool QBF>
-__global__ void __launch_bounds__(kDecodeThreads)
+template <int KV, bool QBF, bool TAIL>
+__global__ void __launch_bounds__(kDecodeThreads, TAIL && KV != kI4 ? 3 : 1)
     decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ int32_t warp_sum[kWarps];
-  decode_body<KV, QBF>(a, dsmem, warp_sum, blockIdx.x, gridDim.x);
+  decode_body<KV, QBF, TAIL>(a, dsmem, warp_sum, blockIdx.x, gridDim.x);
 }
 
 // The merge of one (request, q head) row that the decode did not finish
@@ -562,12 +639,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
 // per lane.
 template <bool QBF>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t bh, int hh, int lane,
-                                             int64_t w_first, int64_t nd, int64_t seg_start,
-                                             int P, int npc) {
+                                             int64_t r_first, int64_t nd, int64_t seg_start,
+                                             const RangeMap& rm, int npc) {
   auto rec_of = [&](int64_t i) -> const float* {
     if (i < nd) {
-      const int slot = (i == 0 && seg_start != w_first * P) ? 1 : 0;
-      return a.part + (((w_first + i) * 2 + slot) * a.hpg + hh) * kPartStride;
+      const int slot = (i == 0 && seg_start != range_start(rm, r_first)) ? 1 : 0;
+      return a.part + (((r_first + i) * 2 + slot) * a.hpg + hh) * kPartStride;
     }
     return a.ppart + (bh * a.pmax_chunks + (i - nd)) * kPartStride;
   };
@@ -623,8 +700,13 @@ __device__ __forceinline__ void combine_row(const DecodeArgs& a, int64_t bh, int
   if (bh >= static_cast<int64_t>(a.batch) * a.q_heads) return;
   const int b = static_cast<int>(bh / a.q_heads);
   const int hq = static_cast<int>(bh - static_cast<int64_t>(b) * a.q_heads);
-  const int tb = a.hdr[0], P = a.hdr[1];
-  const int32_t* cum = a.hdr + 2;
+  const int tb = a.hdr[0];
+  RangeMap rm;
+  rm.Pst = a.hdr[1];
+  rm.C = a.hdr[2];
+  rm.nwarps = a.hdr[3];
+  rm.ntail = 0;  // not needed to map blocks to ranges
+  const int32_t* cum = a.hdr + kHdrCum;
   const int nblk = cum[b + 1] - cum[b];
   const int skip = a.skip != nullptr ? a.skip[b] : 0;
   const int npc = skip > 0 ? (skip + a.pchunk - 1) / a.pchunk : 0;
@@ -633,14 +715,14 @@ __device__ __forceinline__ void combine_row(const DecodeArgs& a, int64_t bh, int
   const int hgi = h * a.head_groups + within / kHeadsPerGroup;
   const int hh = within % kHeadsPerGroup;
   const int64_t seg_start = static_cast<int64_t>(hgi) * tb + cum[b];
-  int64_t w_first = 0, nd = 0;
+  int64_t r_first = 0, nd = 0;
   if (nblk > 0) {
-    w_first = seg_start / P;
-    const int64_t w_last = (seg_start + nblk - 1) / P;
-    if (w_first == w_last) return;  // one warp: written by the decode kernel
-    nd = w_last - w_first + 1;
+    r_first = range_of(rm, seg_start);
+    const int64_t r_last = range_of(rm, seg_start + nblk - 1);
+    if (r_first == r_last) return;  // one range: written by the decode kernel
+    nd = r_last - r_first + 1;
   }
-  merge_pieces<QBF>(a, bh, hh, lane, w_first, nd, seg_start, P, npc);
+  merge_pieces<QBF>(a, bh, hh, lane, r_first, nd, seg_start, rm, npc);
 }
 
 template <bool QBF>
@@ -689,8 +771,8 @@ __device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target
 // tokens, spread over the whole grid; (2) the decode, as decode_kernel; (3)
 // the combine, one warp per (request, q head). The phases are separated by
 // grid barriers, so the step is one launch instead of four.
-template <int KV, bool QBF>
-__global__ void __launch_bounds__(kDecodeThreads, KvTraits<KV>::kQuant ? kMaxCtasPerSm : 3)
+template <int KV, bool QBF, bool TAIL>
+__global__ void __launch_bounds__(kDecodeThreads, KV == kI4 && !TAIL ? kMaxCtasPerSm : 3)
     step_kernel(const __grid_constant__ StepArgs s) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ int32_t warp_sum[kWarps];
@@ -714,21 +796,21 @@ __global__ void __launch_bounds__(kDecodeThreads, KvTraits<KV>::kQuant ? kMaxCta
   }
   if (!grid_sync(s.barrier, gridDim.x, s.d.dev_err)) return;
   // (2) decode
-  decode_body<KV, QBF>(s.d, dsmem, warp_sum, blockIdx.x, gridDim.x);
+  decode_body<KV, QBF, TAIL>(s.d, dsmem, warp_sum, blockIdx.x, gridDim.x);
   if (!grid_sync(s.barrier, 2 * gridDim.x, s.d.dev_err)) return;
   // (3) combine
   for (int64_t bh = gwarp; bh < static_cast<int64_t>(s.d.batch) * s.d.q_heads; bh += nwarps)
     combine_row<QBF>(s.d, bh, lane);
 }
 
-template <int KV, bool QBF>
+template <int KV, bool QBF, bool TAIL>
 cudaError_t launch_step_t(const StepArgs& a, int grid, cudaStream_t s) {
   static int opted_in_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (opted_in_device != dev) {
-    e = cudaFuncSetAttribute(step_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(step_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
@@ -743,20 +825,20 @@ cudaError_t launch_step_t(const StepArgs& a, int grid, cudaStream_t s) {
   attr.val.cooperative = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<KV, QBF>, a);
+  return cudaLaunchKernelEx(&cfg, step_kernel<KV, QBF, TAIL>, a);
 }
 
-template <int KV, bool QBF>
+template <int KV, bool QBF, bool TAIL>
 int step_occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   static int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
-  if (cudaFuncSetAttribute(step_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(step_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<KV, QBF>, kDecodeThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<KV, QBF, TAIL>, kDecodeThreads,
                                                     smem_bytes_for<KV>(batch)) != cudaSuccess)
     return 0;
   cached_dev = dev;
@@ -765,7 +847,7 @@ int step_occupancy_t(int batch) {
   return n;
 }
 
-template <int KV, bool QBF>
+template <int KV, bool QBF, bool TAIL>
 cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   // allow the largest dynamic shared memory the kernel can ask for, once
   // per device
@@ -774,26 +856,26 @@ cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (opted_in_device != dev) {
-    e = cudaFuncSetAttribute(decode_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
   }
-  decode_kernel<KV, QBF><<<grid, kDecodeThreads, smem_bytes_for<KV>(a.batch), s>>>(a);
+  decode_kernel<KV, QBF, TAIL><<<grid, kDecodeThreads, smem_bytes_for<KV>(a.batch), s>>>(a);
   return cudaGetLastError();
 }
 
-template <int KV, bool QBF>
+template <int KV, bool QBF, bool TAIL>
 int occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   static int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
-  if (cudaFuncSetAttribute(decode_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF>, kDecodeThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF, TAIL>, kDecodeThreads,
                                                     smem_bytes_for<KV>(batch)) != cudaSuccess)
     return 0;
   cached_dev = dev;
@@ -804,21 +886,68 @@ int occupancy_t(int batch) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid,
-                          cudaStream_t s) {
+namespace {
+
+// f.run<KV, QBF, TAIL>() for the runtime pool kind, Q type and tail flag;
+// f.fail() for a kind without a kernel.
+template <typename F>
+auto with_kinds(int kv_dtype, int q_dtype, bool tail, const F& f) -> decltype(f.fail()) {
   const bool qbf = q_dtype == kBF16;
   switch (kv_dtype) {
     case kF16:
-      return launch_t<kF16, false>(a, grid, s);
+      return tail ? f.template run<kF16, false, true>() : f.template run<kF16, false, false>();
     case kBF16:
-      return launch_t<kBF16, true>(a, grid, s);
+      return tail ? f.template run<kBF16, true, true>() : f.template run<kBF16, true, false>();
     case kI8:
-      return qbf ? launch_t<kI8, true>(a, grid, s) : launch_t<kI8, false>(a, grid, s);
+      if (qbf)
+        return tail ? f.template run<kI8, true, true>() : f.template run<kI8, true, false>();
+      return tail ? f.template run<kI8, false, true>() : f.template run<kI8, false, false>();
     case kI4:
-      return qbf ? launch_t<kI4, true>(a, grid, s) : launch_t<kI4, false>(a, grid, s);
+      if (qbf)
+        return tail ? f.template run<kI4, true, true>() : f.template run<kI4, true, false>();
+      return tail ? f.template run<kI4, false, true>() : f.template run<kI4, false, false>();
     default:
-      return cudaErrorInvalidValue;
+      return f.fail();
   }
+}
+
+struct LaunchDecode {
+  const DecodeArgs& a;
+  int grid;
+  cudaStream_t s;
+  template <int KV, bool QBF, bool TAIL>
+  cudaError_t run() const { return launch_t<KV, QBF, TAIL>(a, grid, s); }
+  cudaError_t fail() const { return cudaErrorInvalidValue; }
+};
+
+struct LaunchStep {
+  const StepArgs& a;
+  int grid;
+  cudaStream_t s;
+  template <int KV, bool QBF, bool TAIL>
+  cudaError_t run() const { return launch_step_t<KV, QBF, TAIL>(a, grid, s); }
+  cudaError_t fail() const { return cudaErrorInvalidValue; }
+};
+
+struct DecodeOccupancy {
+  int batch;
+  template <int KV, bool QBF, bool TAIL>
+  int run() const { return occupancy_t<KV, QBF, TAIL>(batch); }
+  int fail() const { return 0; }
+};
+
+struct StepOccupancy {
+  int batch;
+  template <int KV, bool QBF, bool TAIL>
+  int run() const { return step_occupancy_t<KV, QBF, TAIL>(batch); }
+  int fail() const { return 0; }
+};
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int grid,
+                          cudaStream_t s) {
+  return with_kinds(kv_dtype, q_dtype, a.tail_ctr != nullptr, LaunchDecode{a, grid, s});
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
@@ -834,41 +963,15 @@ cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
 
 cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid,
                         cudaStream_t s) {
-  const bool qbf = q_dtype == kBF16;
-  switch (kv_dtype) {
-    case kF16:
-      return launch_step_t<kF16, false>(a, grid, s);
-    case kBF16:
-      return launch_step_t<kBF16, true>(a, grid, s);
-    case kI8:
-      return qbf ? launch_step_t<kI8, true>(a, grid, s) : launch_step_t<kI8, false>(a, grid, s);
-    case kI4:
-      return qbf ? launch_step_t<kI4, true>(a, grid, s) : launch_step_t<kI4, false>(a, grid, s);
-    default:
-      return cudaErrorInvalidValue;
-  }
+  return with_kinds(kv_dtype, q_dtype, a.d.tail_ctr != nullptr, LaunchStep{a, grid, s});
 }
 
-int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch) {
-  const bool qbf = q_dtype == kBF16;
-  switch (kv_dtype) {
-    case kF16: return step_occupancy_t<kF16, false>(batch);
-    case kBF16: return step_occupancy_t<kBF16, true>(batch);
-    case kI8: return qbf ? step_occupancy_t<kI8, true>(batch) : step_occupancy_t<kI8, false>(batch);
-    case kI4: return qbf ? step_occupancy_t<kI4, true>(batch) : step_occupancy_t<kI4, false>(batch);
-    default: return 0;
-  }
+int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail) {
+  return with_kinds(kv_dtype, q_dtype, tail, StepOccupancy{batch});
 }
 
-int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch) {
-  const bool qbf = q_dtype == kBF16;
-  switch (kv_dtype) {
-    case kF16: return occupancy_t<kF16, false>(batch);
-    case kBF16: return occupancy_t<kBF16, true>(batch);
-    case kI8: return qbf ? occupancy_t<kI8, true>(batch) : occupancy_t<kI8, false>(batch);
-    case kI4: return qbf ? occupancy_t<kI4, true>(batch) : occupancy_t<kI4, false>(batch);
-    default: return 0;
-  }
+int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail) {
+  return with_kinds(kv_dtype, q_dtype, tail, DecodeOccupancy{batch});
 }
 
 }  // namespace kvq

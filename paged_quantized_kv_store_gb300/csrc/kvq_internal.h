@@ -65,9 +65,12 @@ struct DecodeArgs {
   int min_blocks_per_warp;
   int len_cap;           // lengths are clamped to this (tokens)
   float sm_scale_log2;   // sm_scale * log2(e): scores live in the exp2 domain
-  float* part;           // [warps][2][hpg][kPartStride]: o[128], max, sum
-  int32_t* hdr;          // [0] blocks per head group, [1] blocks per warp,
-                         // [2 .. 2 + batch] prefix sums of the blocks per request
+  float* part;           // [ranges][2][hpg][kPartStride]: o[128], max, sum
+  int64_t max_ranges;    // ranges the workspace holds records for
+  unsigned int* tail_ctr;  // tail chunks handed out (zero at launch); null: no tail
+  int32_t* hdr;          // [0] blocks per head group, [1] blocks per static range,
+                         // [2] blocks per tail chunk (0: none), [3] warps,
+                         // [kHdrCum .. kHdrCum + batch] prefix sums of the blocks per request
   int32_t* dev_err;
   // shared-prefix decode only (null / 0 otherwise): group G's members are
   // grp_mem[grp_off[G] .. grp_off[G + 1]) and share their first grp_shared[G]
@@ -145,7 +148,7 @@ cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
 // kv_dtype / q_dtype as for launch_decode (the new rows have Q's dtype)
 cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                         cudaStream_t s);
-int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
+int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail);
 cudaError_t launch_extend(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                           cudaStream_t s);
 int extend_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
@@ -165,7 +168,7 @@ cudaError_t launch_prefix(const DecodeArgs& a, int kv_dtype, int q_dtype, int gr
                           cudaStream_t s);
 
 // CTAs of the decode kernel resident per SM (occupancy) for a dtype pair and batch
-int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
+int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail);
 // the same for the shared-prefix kernel and a number of groups
 int prefix_ctas_per_sm(int kv_dtype, int q_dtype, int num_groups);
 
@@ -173,6 +176,9 @@ constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared 
 constexpr int kDecodeThreads = 128;
 constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many CTAs per SM
 constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)
+constexpr int kHdrCum = 4;                 // first prefix sum in the decode's header
+constexpr int kRangesPerWarp = 5;          // records the workspace holds: static + tail
+constexpr int kTailMinShare = 128;         // blocks per warp from which the decode has a tail
 constexpr int kMaxPrefixChunk = 32;    // shared blocks per prefix unit: one table window
 
 }  // namespace kvq

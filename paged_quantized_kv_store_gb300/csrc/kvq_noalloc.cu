@@ -56,8 +56,8 @@ extern "C" kvq_status paged_decode_attn_noalloc(
   const kvq_status st = paged_decode_attn_plan(batch, q_heads, pool->kv_heads, pool->head_dim,
                                                max_seq_len, num_splits, 0, &plan);
   if (st != KVQ_OK) return st;
-  if (plan.workspace_bytes > static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES))
-    return KVQ_ERR_WORKSPACE;  // these sizes need more scratch than the array holds
+  // sizes whose static ranges need more scratch than the array holds are
+  // refused by paged_decode_attn itself (KVQ_ERR_WORKSPACE, nothing launched)
   void* scratch = scratch_on_current_device();
   if (scratch == nullptr) return KVQ_ERR_CUDA;
   return paged_decode_attn(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens,

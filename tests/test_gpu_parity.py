@@ -327,3 +327,37 @@ def test_store_rounding_ties(gpu, kv_dtype, in_dtype):
     opool = oracle.Pool(4, Hkv, 128, kv_dtype)
     oracle.kv_store(opool, k, v, in_dtype, slots)
     _compare_pools(pool, opool)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kv_dtype", ["int8", "int4"])
+def test_balanced_tail_on_long_contexts(gpu, kv_dtype):
+    """Per-warp shares above 128 blocks: the decode hands the last tenth of
+    the stream out in chunks (tail). Same outputs as the oracle, and as the
+    static split (a workspace that holds one range per warp) and an explicit
+    split count, both of which run without the tail."""
+    wl = synthetic.custom(f"tail_{kv_dtype}", kv_dtype, [49152, 20000, 49152, 33333], 48, 48,
+                          seed=58)
+    pool = fill_pool(wl)
+    out, bt, dev_err = run_step(wl, pool)
+    assert gpu.kvq_check_error(dev_err) == 0
+    got = out_to_f64(out)
+    for b in range(wl.batch):
+        _, oout = oracle_request(wl, b)
+        assert_close(got[b], oout)
+    plan = gpu.paged_decode_attn_plan(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
+    static = (256 + -(-(wl.batch + 5) * 4 // 256) * 256
+              + plan["warps"] * 2 * plan["heads_per_group"] * 132 * 4)
+    assert static < plan["workspace_bytes"]
+    q = to_dev(wl.q(), wl.q_dtype)
+    for ws_bytes, splits in ((static, 0), (plan["workspace_bytes"], 3)):
+        out2 = torch.empty_like(q)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        gpu.paged_decode_attn(pool, q, out2, bt, i32(wl.seq_lens), wl.max_seq_len, wl.sm_scale,
+                              splits, ws, dev_err)
+        assert gpu.kvq_check_error(dev_err) == 0
+        assert_close(out_to_f64(out2), got)
+    small = torch.empty(static - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gpu.KvqError):
+        gpu.paged_decode_attn(pool, q, torch.empty_like(q), bt, i32(wl.seq_lens),
+                              wl.max_seq_len, wl.sm_scale, 0, small, dev_err)
