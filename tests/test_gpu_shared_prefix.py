@@ -215,3 +215,26 @@ def test_block_id_outside_the_pool_in_the_shared_part(gpu):
     out = _shared_call(pool, q, i32(bt), i32(lens), [([0, 1, 2], 3)], 64, dev_err)
     assert gpu.kvq_check_error(dev_err) & kvq.DEV_ERR_BITS["block_id"]
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.slow
+def test_cascade_with_the_balanced_tail(gpu):
+    """Long contexts behind a shared prefix: the members' own blocks give
+    per-warp shares above 128 blocks, so the decode hands out tail chunks and
+    the combine merges tail pieces with the prefix records. Same outputs as
+    the plain decode over whole block tables, and as the oracle on the
+    shortest request."""
+    wl = synthetic.shared_prefix("sp_tail", "int8", [49152, 40000, 49152, 33333], 48, 48,
+                                 prefix_blocks=512, seed=59)
+    pool = fill_pool(wl)
+    slots, k, v = wl.step_store()
+    _kvq().kv_store_quant(pool, to_dev(k, wl.in_dtype), to_dev(v, wl.in_dtype), i64(slots))
+    bt = i32(wl.block_tables)
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    plain = decode(wl, pool, bt, dev_err=dev_err)
+    out, dev_err = _run_shared(wl, pool, bt, _full_group(wl), dev_err=dev_err)
+    assert _kvq().kvq_check_error(dev_err) == 0
+    assert_close(out_to_f64(out), out_to_f64(plain))
+    b = int(np.argmin(wl.seq_lens))
+    _, oout = oracle_request(wl, b)
+    assert_close(out_to_f64(out)[b], oout)
