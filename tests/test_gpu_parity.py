@@ -361,3 +361,22 @@ def test_balanced_tail_on_long_contexts(gpu, kv_dtype):
     with pytest.raises(gpu.KvqError):
         gpu.paged_decode_attn(pool, q, torch.empty_like(q), bt, i32(wl.seq_lens),
                               wl.max_seq_len, wl.sm_scale, 0, small, dev_err)
+    # a chunk's result does not depend on the warp that takes it, and every
+    # call resets the chunk counter: repeated calls and CUDA-graph replays
+    # give the same bits
+    ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device="cuda")
+    sl = i32(wl.seq_lens)
+    first = torch.empty_like(q)
+    gpu.paged_decode_attn(pool, q, first, bt, sl, wl.max_seq_len, wl.sm_scale, 0, ws, dev_err)
+    assert torch.equal(first.view(torch.int16), out.view(torch.int16))
+    again = torch.empty_like(q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gpu.paged_decode_attn(pool, q, again, bt, sl, wl.max_seq_len, wl.sm_scale, 0, ws,
+                              dev_err)
+    for _ in range(3):
+        again.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+    assert gpu.kvq_check_error(dev_err) == 0
