@@ -20,6 +20,10 @@
 //   its range, a partial record (running max, sum, unnormalised output) that
 //   the combine kernel merges with a log-sum-exp. All q heads of a kv head's
 //   group are handled by the same warp, so every KV byte is read once.
+//   Long shares (RangeMap) keep about nine tenths of the stream in such
+//   static ranges and hand the rest out in short chunks from a counter, each
+//   chunk a range of its own, so that warps that ran slower are not waited
+//   for.
 //
 // Per-block arithmetic of one warp (16 tokens of one kv head):
 //   S^T = K Q^T  with mma.m16n8k16: M = 16 tokens, N = 8 q heads (padded),
@@ -631,12 +635,11 @@ __global__ void __launch_bounds__(kDecodeThreads, TAIL && KV != kI4 ? 3 : 1)
 }
 
 // The merge of one (request, q head) row that the decode did not finish
-// itself, by one warp: the split-K records of the warps its
-// blocks were split between (slot 1 for the first when the request starts
-// inside that warp's range), then its shared-prefix records, if any (a
-// request made of shared blocks only has nothing else). Log-sum-exp in the
-// exp2 domain; the pieces' maxima and sums are read in one round, one piece
-// per lane.
+// itself, by one warp: the split-K records of the ranges its blocks were
+// split between (slot 1 for the first when the request starts inside that
+// range), then its shared-prefix records, if any (a request made of shared
+// blocks only has nothing else). Log-sum-exp in the exp2 domain, 8 pieces
+// per round of loads.
 template <bool QBF>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t bh, int hh, int lane,
                                              int64_t r_first, int64_t nd, int64_t seg_start,
