@@ -330,7 +330,7 @@ def test_store_rounding_ties(gpu, kv_dtype, in_dtype):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kv_dtype", ["int8", "int4"])
+@pytest.mark.parametrize("kv_dtype", ["int8", "int4", "bf16", "f16"])
 def test_balanced_tail_on_long_contexts(gpu, kv_dtype):
     """Per-warp shares above 128 blocks: the decode hands the last tenth of
     the stream out in chunks (tail). Same outputs as the oracle, and as the
