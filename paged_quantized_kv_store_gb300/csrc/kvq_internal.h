@@ -70,6 +70,7 @@ struct DecodeArgs {
   unsigned int* tail_ctr;  // tail chunks handed out (zero at launch); null: no tail
   int32_t* hdr;          // [0] blocks per head group, [1] blocks per static range,
                          // [2] blocks per tail chunk (0: none), [3] warps,
+                         // [4] ranges per q-head group (0: one cut of the whole stream),
                          // [kHdrCum .. kHdrCum + batch] prefix sums of the blocks per request
   int32_t* dev_err;
   // shared-prefix decode only (null / 0 otherwise): group G's members are
@@ -176,7 +177,7 @@ constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared 
 constexpr int kDecodeThreads = 128;
 constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many CTAs per SM
 constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)
-constexpr int kHdrCum = 4;                 // first prefix sum in the decode's header
+constexpr int kHdrCum = 5;                 // first prefix sum in the decode's header
 constexpr int kRangesPerWarp = 5;          // records the workspace holds: static + tail
 constexpr int kTailMinShare = 128;         // blocks per warp from which the decode has a tail
 constexpr int kMaxPrefixChunk = 32;    // shared blocks per prefix unit: one table window
