@@ -199,7 +199,8 @@ size_t paged_decode_attn_workspace_size(int32_t batch, int32_t q_heads, int32_t 
  *  num_splits   : as in paged_decode_attn_plan.
  *  workspace    : device scratch of paged_decode_attn_workspace_size(...)
  *                 bytes, 16-byte aligned. A smaller one is accepted down to
- *                 one range per warp (256 + header + warps * 2 *
+ *                 one range per warp (256 bytes + the header, (batch + 6)
+ *                 int32 rounded up to 256 bytes, + warps * 2 *
  *                 heads_per_group * 132 floats) and then runs without the
  *                 tail; below that KVQ_ERR_WORKSPACE.
  * For request b and q head h (kv head h / (q_heads / kv_heads)):

@@ -111,6 +111,14 @@ def test_planner(lib):
     p4 = plan(64, 32, 8, 8192, num_sms=152)
     assert p4["heads_per_group"] == 4
     assert p4["workspace_bytes"] >= p4["warps"] * 2 * 4 * 132 * 4
+    # layout: 256 bytes of counters, the header ((batch + 6) int32, rounded
+    # up to 256 bytes), then 2 records of 132 floats per q head of the group
+    # slot for 5 ranges per warp
+    for b, hq, hkv in ((128, 32, 32), (64, 32, 8), (1, 64, 2)):
+        q = plan(b, hq, hkv, 4096, num_sms=152)
+        header = -(-(b + 6) * 4 // 256) * 256
+        assert q["workspace_bytes"] == (256 + header +
+                                        5 * q["warps"] * 2 * q["heads_per_group"] * 132 * 4)
     # the workspace does not grow with the context
     assert plan(64, 32, 8, 100, num_sms=152)["workspace_bytes"] == p4["workspace_bytes"]
     # explicit split counts bound the pieces of a request
