@@ -337,310 +337,310 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
   // the range [x0, x0 + n), its records filed under range id rid; false when a
   // copy timed out (the warp stops)
   auto run_range = [&](const int64_t x0, const int n, const int64_t rid) -> bool {
-  // issue side: cursor, a 32-entry window of the block table, validity bits
-  Cursor ic;
-  locate(ic, x0, cum, a.batch, tb);
-  Cursor cc = ic;  // compute side
-  int win_b = -1, win_j0 = 0;
-  int32_t win = -1;
-  uint32_t ok_mask = 0;  // stages holding a valid block in flight
-  int k_issue = 0;   // next block of the range to issue
-  int st_issue = 0;  // its stage
-  auto issue_next = [&]() {
-    if (k_issue < n) {
-      if (ic.b != win_b || ic.j >= win_j0 + 32) {
-        win_b = ic.b;
-        win_j0 = ic.j;
-        const int jj = win_j0 + lane;
-        win = jj < ic.nblk ? a.block_tables[static_cast<int64_t>(ic.b) * a.max_blocks +
-                                            skip_of(a, ic.b) + jj]
-                           : -1;
+    // issue side: cursor, a 32-entry window of the block table, validity bits
+    Cursor ic;
+    locate(ic, x0, cum, a.batch, tb);
+    Cursor cc = ic;  // compute side
+    int win_b = -1, win_j0 = 0;
+    int32_t win = -1;
+    uint32_t ok_mask = 0;  // stages holding a valid block in flight
+    int k_issue = 0;   // next block of the range to issue
+    int st_issue = 0;  // its stage
+    auto issue_next = [&]() {
+      if (k_issue < n) {
+        if (ic.b != win_b || ic.j >= win_j0 + 32) {
+          win_b = ic.b;
+          win_j0 = ic.j;
+          const int jj = win_j0 + lane;
+          win = jj < ic.nblk ? a.block_tables[static_cast<int64_t>(ic.b) * a.max_blocks +
+                                              skip_of(a, ic.b) + jj]
+                             : -1;
+        }
+        const int32_t phys = __shfl_sync(kFull, win, ic.j - win_j0);
+        const bool ok = phys >= 0 && phys < a.num_blocks;
+        const uint32_t bit = 1u << st_issue;
+        if (ok) {
+          issue_block<KV>(wr, st_issue, a, lm, phys, ic.hgi / a.head_groups, lane);
+          ok_mask |= bit;
+        } else {
+          ok_mask &= ~bit;
+          if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+        }
+        if (k_issue + 1 < n) advance(ic, cum, a.batch);
       }
-      const int32_t phys = __shfl_sync(kFull, win, ic.j - win_j0);
-      const bool ok = phys >= 0 && phys < a.num_blocks;
-      const uint32_t bit = 1u << st_issue;
-      if (ok) {
-        issue_block<KV>(wr, st_issue, a, lm, phys, ic.hgi / a.head_groups, lane);
-        ok_mask |= bit;
-      } else {
-        ok_mask &= ~bit;
-        if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
-      }
-      if (k_issue + 1 < n) advance(ic, cum, a.batch);
-    }
-    if constexpr (!S::kTma) cp_async_commit();
-    ++k_issue;
-    st_issue = st_issue == D - 1 ? 0 : st_issue + 1;
-  };
-#pragma unroll
-  for (int k = 0; k < D - 1; ++k) issue_next();
+      if constexpr (!S::kTma) cp_async_commit();
+      ++k_issue;
+      st_issue = st_issue == D - 1 ? 0 : st_issue + 1;
+    };
+  #pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue_next();
 
-  // ---- per-request state ---------------------------------------------------------
-  int seg_b = -1, seg_hgi = -1, hq0 = 0, nh = 0, L = 0, seg_nblk = 0, seg_skip = 0;
-  int64_t seg_start = 0;
-  uint32_t qb[8][2];
-  float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
-  bool hv0 = false, hv1 = false;
-  float o[8][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
-  float r0 = 0.f, r1 = 0.f;  // sums of the 16-bit P' values fed to the P.V product
+    // ---- per-request state ---------------------------------------------------------
+    int seg_b = -1, seg_hgi = -1, hq0 = 0, nh = 0, L = 0, seg_nblk = 0, seg_skip = 0;
+    int64_t seg_start = 0;
+    uint32_t qb[8][2];
+    float qs0 = 0.f, qs1 = 0.f;  // sum(q) of heads 2t and 2t+1
+    bool hv0 = false, hv1 = false;
+    float o[8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+    float r0 = 0.f, r1 = 0.f;  // sums of the 16-bit P' values fed to the P.V product
 
-  // writes the finished state of request seg_b: the output if this warp
-  // covered all of its blocks, else a partial record
-  auto flush = [&]() {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(kFull, l0, off);
-      l1 += __shfl_xor_sync(kFull, l1, off);
-      if constexpr (kQuant) {
-        z0 += __shfl_xor_sync(kFull, z0, off);
-        z1 += __shfl_xor_sync(kFull, z1, off);
-        if constexpr (kPCorr) {
-          r0 += __shfl_xor_sync(kFull, r0, off);
-          r1 += __shfl_xor_sync(kFull, r1, off);
+    // writes the finished state of request seg_b: the output if this warp
+    // covered all of its blocks, else a partial record
+    auto flush = [&]() {
+  #pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, off);
+        l1 += __shfl_xor_sync(kFull, l1, off);
+        if constexpr (kQuant) {
+          z0 += __shfl_xor_sync(kFull, z0, off);
+          z1 += __shfl_xor_sync(kFull, z1, off);
+          if constexpr (kPCorr) {
+            r0 += __shfl_xor_sync(kFull, r0, off);
+            r1 += __shfl_xor_sync(kFull, r1, off);
+          }
         }
       }
-    }
-    if constexpr (kPCorr) {
-      // o = sum P'(a + c) + sum p (Z + mid S) - (a + mid) sum P'
-      z0 -= (kAv + kMid) * r0;
-      z1 -= (kAv + kMid) * r1;
-    }
-    const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
-    const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int hh = 2 * t + u;
-      if (hh >= nh) continue;
-      const float z = u ? z1 : z0, l = u ? l1 : l0, m = u ? m1 : m0;
-      if (contained) {
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc[2 * i] = o[i][u] + z;
-          acc[2 * i + 1] = o[i][2 + u] + z;
-        }
-        float mm = m, ll = l;
-        if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
-        const float inv = ll > 0.f ? 1.f / ll : 0.f;
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = pack2<QBF>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                              (row0 + hh) * kHeadDim + 16 * g);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      } else {
-        const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
-        float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
-        float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
-#pragma unroll
-        for (int i = 0; i < 8; i += 2)
-          ov[i / 2] =
-              make_float4(o[i][u] + z, o[i][2 + u] + z, o[i + 1][u] + z, o[i + 1][2 + u] + z);
-        if (g == 0) {
-          rec[kHeadDim] = m;
-          rec[kHeadDim + 1] = l;
-        }
-      }
-    }
-  };
-
-  int st = 0;  // stage of block k
-  for (int k = 0; k < n; ++k) {
-    issue_next();  // refills the stage block k - 1 used
-    const bool blk_ok = (ok_mask >> st) & 1u;
-    if constexpr (S::kTma) {
-      if (blk_ok) {
-        if (!mbar_wait(wr + S::kBarOff + 8 * st, (phase >> st) & 1u)) {
-          // a copy did not land: report, wait (bounded) for the other copies
-          // this warp started, and stop
-          if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
-          const uint32_t rest = ok_mask & ~(1u << st);
-          for (int i = 0; i < D; ++i)
-            if ((rest >> i) & 1u) mbar_wait(wr + S::kBarOff + 8 * i, (phase >> i) & 1u);
-          return false;
-        }
-        phase ^= 1u << st;
-      }
-    } else {
-      cp_async_wait<D - 1>();  // this lane's copies of block k have landed
-      __syncwarp();            // ... and every other lane's
-    }
-
-    if (cc.b != seg_b || cc.hgi != seg_hgi) {
-      if (seg_b >= 0) flush();
-      // start request cc.b for q-head group cc.hgi
-      seg_b = cc.b;
-      seg_hgi = cc.hgi;
-      seg_nblk = cc.nblk;
-      seg_start = static_cast<int64_t>(cc.hgi) * tb + cum[cc.b];
-      const int h = cc.hgi / a.head_groups;
-      const int hg = cc.hgi - h * a.head_groups;
-      hq0 = h * a.group + hg * kHeadsPerGroup;
-      nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
-      seg_skip = skip_of(a, cc.b);
-      L = clamped_len(a, cc.b) - kBlock * seg_skip;  // tokens of this request's own blocks
-      // Q fragments (B operand of S^T = K Q^T), permuted like the K dims
-      uint32_t qw[16];
-      if (g < nh) {
-        const uint4* qp = reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(a.q) +
-            (static_cast<int64_t>(cc.b) * a.q_heads + hq0 + g) * kHeadDim + 32 * t);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = qp[i];
-          qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qw[i] = 0u;
-      }
-      if constexpr (KV == kI4) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int j = kk >> 1, u = kk & 1;
-          qb[kk][0] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x5410u);
-          qb[kk][1] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x7632u);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          qb[kk][0] = qw[2 * kk];
-          qb[kk][1] = qw[2 * kk + 1];
-        }
-      }
-      if constexpr (kQuant) {
-        float part = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) part += lo_to_float<QBF>(qw[i]) + hi_to_float<QBF>(qw[i]);
-        part += __shfl_xor_sync(kFull, part, 1);
-        part += __shfl_xor_sync(kFull, part, 2);
-        qs0 = __shfl_sync(kFull, part, (2 * t) * 4);  // lanes 4h hold sum(q) of head h
-        qs1 = __shfl_sync(kFull, part, (2 * t + 1) * 4);
-      }
-      hv0 = 2 * t < nh;
-      hv1 = 2 * t + 1 < nh;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = z0 = z1 = r0 = r1 = 0.f;
-    }
-
-    if (blk_ok) {
-      ok_mask &= ~(1u << st);
-      Frag<KV> cur;
-      read_frag<KV>(cur, wr, st, lm, g);
-      // S^T = K Q^T, even and odd k-steps in two accumulators
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 0; kk < 8; kk += 2) {
-        uint32_t ak[4];
-        k_operand<KV, QBF>(cur, kk, ak);
-        mma16816<QBF>(sa, ak, qb[kk]);
-        k_operand<KV, QBF>(cur, kk + 1, ak);
-        mma16816<QBF>(sb, ak, qb[kk + 1]);
-      }
-      const float sc0 = sa[0] + sb[0], sc1 = sa[1] + sb[1];
-      const float sc2 = sa[2] + sb[2], sc3 = sa[3] + sb[3];
-      // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
-      const int tok0 = cc.j * kBlock + g, tok1 = tok0 + 8;
-      float s00, s01, s10, s11;
-      if constexpr (kQuant) {
-        // q.k = S (q.(a + c)) + (Z - a S) sum(q)
-        const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) - kAk * S0;
-        const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) - kAk * S1;
-        s00 = (S0 * sc0 + Z0 * qs0) * a.sm_scale_log2;
-        s01 = (S0 * sc1 + Z0 * qs1) * a.sm_scale_log2;
-        s10 = (S1 * sc2 + Z1 * qs0) * a.sm_scale_log2;
-        s11 = (S1 * sc3 + Z1 * qs1) * a.sm_scale_log2;
-      } else {
-        s00 = sc0 * a.sm_scale_log2;
-        s01 = sc1 * a.sm_scale_log2;
-        s10 = sc2 * a.sm_scale_log2;
-        s11 = sc3 * a.sm_scale_log2;
-      }
-      if (tok0 >= L) s00 = s01 = -INFINITY;
-      if (tok1 >= L) s10 = s11 = -INFINITY;
-      if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
-      if (!hv1) s01 = s11 = 0.f;
-      // the running maximum moves only when some lane holds a larger score:
-      // then reduce the block maximum over the 16 tokens (lanes with equal t)
-      // and rescale the running state
-      float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
-      float mn0 = m0, mn1 = m1;
-      if (__any_sync(kFull, bm0 > m0 || bm1 > m1)) {
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-          bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-        }
-        mn0 = fmaxf(m0, bm0);
-        mn1 = fmaxf(m1, bm1);
-        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-        l0 *= al0;
-        l1 *= al1;
-        z0 *= al0;
-        z1 *= al1;
-        r0 *= al0;
-        r1 *= al1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i][0] *= al0; o[i][2] *= al0;
-          o[i][1] *= al1; o[i][3] *= al1;
-        }
-      }
-      m0 = mn0;
-      m1 = mn1;
-      const float p00 = ex2(s00 - mn0), p10 = ex2(s10 - mn0);
-      const float p01 = ex2(s01 - mn1), p11 = ex2(s11 - mn1);
-      l0 += p00 + p10;
-      l1 += p01 + p11;
-      float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
-      if constexpr (kQuant) {
-        // sum_t p_t v_t = sum_t P'_t (a + c_t) + sum_t p_t (Z_t + mid S_t)
-        //                 - (a + mid) sum_t P'_t,  with P'_t = p_t S_t in fp16:
-        // subtracting the rounded P' actually used leaves their rounding
-        // error multiplied by c - mid only, as if the codes were centred
-        const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
-        const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
-        z0 += p00 * Z0 + p10 * Z1;
-        z1 += p01 * Z0 + p11 * Z1;
-        q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
-      }
-      // P'^T as the B operand: transpose the (token x head) fragments
-      uint32_t bp[2], bp_lo[2];
-      const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
       if constexpr (kPCorr) {
-        r0 += lo_to_float<false>(h0) + lo_to_float<false>(h1);
-        r1 += hi_to_float<false>(h0) + hi_to_float<false>(h1);
+        // o = sum P'(a + c) + sum p (Z + mid S) - (a + mid) sum P'
+        z0 -= (kAv + kMid) * r0;
+        z1 -= (kAv + kMid) * r1;
       }
-      bp[0] = movmatrix_trans(h0);
-      bp[1] = movmatrix_trans(h1);
-      if constexpr (kPvBf) {
-        // bf16 keeps 8 bits of P: add the rounding residual in a second
-        // product so P carries ~16 bits (P = hi + lo)
-        bp_lo[0] = movmatrix_trans(pack2<true>(q00 - lo_to_float<true>(h0),
-                                               q01 - hi_to_float<true>(h0)));
-        bp_lo[1] = movmatrix_trans(pack2<true>(q10 - lo_to_float<true>(h1),
-                                               q11 - hi_to_float<true>(h1)));
+      const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
+      const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
+  #pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int hh = 2 * t + u;
+        if (hh >= nh) continue;
+        const float z = u ? z1 : z0, l = u ? l1 : l0, m = u ? m1 : m0;
+        if (contained) {
+          float acc[16];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[2 * i] = o[i][u] + z;
+            acc[2 * i + 1] = o[i][2 + u] + z;
+          }
+          float mm = m, ll = l;
+          if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
+          const float inv = ll > 0.f ? 1.f / ll : 0.f;
+          uint32_t w[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = pack2<QBF>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                                (row0 + hh) * kHeadDim + 16 * g);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+          const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
+          float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
+          float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
+  #pragma unroll
+          for (int i = 0; i < 8; i += 2)
+            ov[i / 2] =
+                make_float4(o[i][u] + z, o[i][2 + u] + z, o[i + 1][u] + z, o[i + 1][2 + u] + z);
+          if (g == 0) {
+            rec[kHeadDim] = m;
+            rec[kHeadDim + 1] = l;
+          }
+        }
       }
-      // O^T += V^T P'^T
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t av[4];
-        v_operand<KV>(cur, i, av);
-        mma16816<kPvBf>(o[i], av, bp);
-        if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
+    };
+
+    int st = 0;  // stage of block k
+    for (int k = 0; k < n; ++k) {
+      issue_next();  // refills the stage block k - 1 used
+      const bool blk_ok = (ok_mask >> st) & 1u;
+      if constexpr (S::kTma) {
+        if (blk_ok) {
+          if (!mbar_wait(wr + S::kBarOff + 8 * st, (phase >> st) & 1u)) {
+            // a copy did not land: report, wait (bounded) for the other copies
+            // this warp started, and stop
+            if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
+            const uint32_t rest = ok_mask & ~(1u << st);
+            for (int i = 0; i < D; ++i)
+              if ((rest >> i) & 1u) mbar_wait(wr + S::kBarOff + 8 * i, (phase >> i) & 1u);
+            return false;
+          }
+          phase ^= 1u << st;
+        }
+      } else {
+        cp_async_wait<D - 1>();  // this lane's copies of block k have landed
+        __syncwarp();            // ... and every other lane's
       }
+
+      if (cc.b != seg_b || cc.hgi != seg_hgi) {
+        if (seg_b >= 0) flush();
+        // start request cc.b for q-head group cc.hgi
+        seg_b = cc.b;
+        seg_hgi = cc.hgi;
+        seg_nblk = cc.nblk;
+        seg_start = static_cast<int64_t>(cc.hgi) * tb + cum[cc.b];
+        const int h = cc.hgi / a.head_groups;
+        const int hg = cc.hgi - h * a.head_groups;
+        hq0 = h * a.group + hg * kHeadsPerGroup;
+        nh = min(kHeadsPerGroup, a.group - hg * kHeadsPerGroup);
+        seg_skip = skip_of(a, cc.b);
+        L = clamped_len(a, cc.b) - kBlock * seg_skip;  // tokens of this request's own blocks
+        // Q fragments (B operand of S^T = K Q^T), permuted like the K dims
+        uint32_t qw[16];
+        if (g < nh) {
+          const uint4* qp = reinterpret_cast<const uint4*>(
+              static_cast<const uint16_t*>(a.q) +
+              (static_cast<int64_t>(cc.b) * a.q_heads + hq0 + g) * kHeadDim + 32 * t);
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = qp[i];
+            qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
+          }
+        } else {
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) qw[i] = 0u;
+        }
+        if constexpr (KV == kI4) {
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int j = kk >> 1, u = kk & 1;
+            qb[kk][0] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x5410u);
+            qb[kk][1] = prmt(qw[4 * j + u], qw[4 * j + u + 2], 0x7632u);
+          }
+        } else {
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            qb[kk][0] = qw[2 * kk];
+            qb[kk][1] = qw[2 * kk + 1];
+          }
+        }
+        if constexpr (kQuant) {
+          float part = 0.f;
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) part += lo_to_float<QBF>(qw[i]) + hi_to_float<QBF>(qw[i]);
+          part += __shfl_xor_sync(kFull, part, 1);
+          part += __shfl_xor_sync(kFull, part, 2);
+          qs0 = __shfl_sync(kFull, part, (2 * t) * 4);  // lanes 4h hold sum(q) of head h
+          qs1 = __shfl_sync(kFull, part, (2 * t + 1) * 4);
+        }
+        hv0 = 2 * t < nh;
+        hv1 = 2 * t + 1 < nh;
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = z0 = z1 = r0 = r1 = 0.f;
+      }
+
+      if (blk_ok) {
+        ok_mask &= ~(1u << st);
+        Frag<KV> cur;
+        read_frag<KV>(cur, wr, st, lm, g);
+        // S^T = K Q^T, even and odd k-steps in two accumulators
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int kk = 0; kk < 8; kk += 2) {
+          uint32_t ak[4];
+          k_operand<KV, QBF>(cur, kk, ak);
+          mma16816<QBF>(sa, ak, qb[kk]);
+          k_operand<KV, QBF>(cur, kk + 1, ak);
+          mma16816<QBF>(sb, ak, qb[kk + 1]);
+        }
+        const float sc0 = sa[0] + sb[0], sc1 = sa[1] + sb[1];
+        const float sc2 = sa[2] + sb[2], sc3 = sa[3] + sb[3];
+        // scores of tokens g, g+8 for heads 2t, 2t+1, in the exp2 domain
+        const int tok0 = cc.j * kBlock + g, tok1 = tok0 + 8;
+        float s00, s01, s10, s11;
+        if constexpr (kQuant) {
+          // q.k = S (q.(a + c)) + (Z - a S) sum(q)
+          const float S0 = half_lo(cur.ksz[0]), Z0 = half_hi(cur.ksz[0]) - kAk * S0;
+          const float S1 = half_lo(cur.ksz[1]), Z1 = half_hi(cur.ksz[1]) - kAk * S1;
+          s00 = (S0 * sc0 + Z0 * qs0) * a.sm_scale_log2;
+          s01 = (S0 * sc1 + Z0 * qs1) * a.sm_scale_log2;
+          s10 = (S1 * sc2 + Z1 * qs0) * a.sm_scale_log2;
+          s11 = (S1 * sc3 + Z1 * qs1) * a.sm_scale_log2;
+        } else {
+          s00 = sc0 * a.sm_scale_log2;
+          s01 = sc1 * a.sm_scale_log2;
+          s10 = sc2 * a.sm_scale_log2;
+          s11 = sc3 * a.sm_scale_log2;
+        }
+        if (tok0 >= L) s00 = s01 = -INFINITY;
+        if (tok1 >= L) s10 = s11 = -INFINITY;
+        if (!hv0) s00 = s10 = 0.f;  // padded heads: finite, never written
+        if (!hv1) s01 = s11 = 0.f;
+        // the running maximum moves only when some lane holds a larger score:
+        // then reduce the block maximum over the 16 tokens (lanes with equal t)
+        // and rescale the running state
+        float bm0 = fmaxf(s00, s10), bm1 = fmaxf(s01, s11);
+        float mn0 = m0, mn1 = m1;
+        if (__any_sync(kFull, bm0 > m0 || bm1 > m1)) {
+  #pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+          }
+          mn0 = fmaxf(m0, bm0);
+          mn1 = fmaxf(m1, bm1);
+          const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+          l0 *= al0;
+          l1 *= al1;
+          z0 *= al0;
+          z1 *= al1;
+          r0 *= al0;
+          r1 *= al1;
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[i][0] *= al0; o[i][2] *= al0;
+            o[i][1] *= al1; o[i][3] *= al1;
+          }
+        }
+        m0 = mn0;
+        m1 = mn1;
+        const float p00 = ex2(s00 - mn0), p10 = ex2(s10 - mn0);
+        const float p01 = ex2(s01 - mn1), p11 = ex2(s11 - mn1);
+        l0 += p00 + p10;
+        l1 += p01 + p11;
+        float q00 = p00, q01 = p01, q10 = p10, q11 = p11;
+        if constexpr (kQuant) {
+          // sum_t p_t v_t = sum_t P'_t (a + c_t) + sum_t p_t (Z_t + mid S_t)
+          //                 - (a + mid) sum_t P'_t,  with P'_t = p_t S_t in fp16:
+          // subtracting the rounded P' actually used leaves their rounding
+          // error multiplied by c - mid only, as if the codes were centred
+          const float S0 = half_lo(cur.vsz[0]), Z0 = half_hi(cur.vsz[0]) + kMid * S0;
+          const float S1 = half_lo(cur.vsz[1]), Z1 = half_hi(cur.vsz[1]) + kMid * S1;
+          z0 += p00 * Z0 + p10 * Z1;
+          z1 += p01 * Z0 + p11 * Z1;
+          q00 *= S0; q01 *= S0; q10 *= S1; q11 *= S1;
+        }
+        // P'^T as the B operand: transpose the (token x head) fragments
+        uint32_t bp[2], bp_lo[2];
+        const uint32_t h0 = pack2<kPvBf>(q00, q01), h1 = pack2<kPvBf>(q10, q11);
+        if constexpr (kPCorr) {
+          r0 += lo_to_float<false>(h0) + lo_to_float<false>(h1);
+          r1 += hi_to_float<false>(h0) + hi_to_float<false>(h1);
+        }
+        bp[0] = movmatrix_trans(h0);
+        bp[1] = movmatrix_trans(h1);
+        if constexpr (kPvBf) {
+          // bf16 keeps 8 bits of P: add the rounding residual in a second
+          // product so P carries ~16 bits (P = hi + lo)
+          bp_lo[0] = movmatrix_trans(pack2<true>(q00 - lo_to_float<true>(h0),
+                                                 q01 - hi_to_float<true>(h0)));
+          bp_lo[1] = movmatrix_trans(pack2<true>(q10 - lo_to_float<true>(h1),
+                                                 q11 - hi_to_float<true>(h1)));
+        }
+        // O^T += V^T P'^T
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t av[4];
+          v_operand<KV>(cur, i, av);
+          mma16816<kPvBf>(o[i], av, bp);
+          if constexpr (kPvBf) mma16816<true>(o[i], av, bp_lo);
+        }
+      }
+      __syncwarp();  // all lanes are done with this stage before it is refilled
+      st = st == D - 1 ? 0 : st + 1;
+      if (k + 1 < n) advance(cc, cum, a.batch);
     }
-    __syncwarp();  // all lanes are done with this stage before it is refilled
-    st = st == D - 1 ? 0 : st + 1;
-    if (k + 1 < n) advance(cc, cum, a.batch);
-  }
-  if constexpr (!S::kTma) cp_async_wait<0>();
-  flush();
-  return true;
+    if constexpr (!S::kTma) cp_async_wait<0>();
+    flush();
+    return true;
   };  // run_range
 
   // the static range (the whole share when there is no tail) ...
@@ -862,7 +862,8 @@ cudaError_t launch_step_t(const StepArgs& a, int grid, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (opted_in_device != dev) {
-    e = cudaFuncSetAttribute(step_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(step_kernel<KV, QBF, TAIL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
@@ -908,7 +909,8 @@ cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (opted_in_device != dev) {
-    e = cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes_for<KV>(kMaxBatch)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
@@ -923,11 +925,13 @@ int occupancy_t(int batch) {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   static int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
-  if (cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF, TAIL>, kDecodeThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KV, QBF, TAIL>,
+                                                    kDecodeThreads,
                                                     smem_bytes_for<KV>(batch)) != cudaSuccess)
     return 0;
   cached_dev = dev;
