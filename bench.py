@@ -200,7 +200,8 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh")) -> str:
+def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh",
+                             "kvq_ranges.h")) -> str:
     """Hash of the decode kernel's source with // comments and blank lines
     removed, so that editing a comment keeps a DRAM-traffic record valid."""
     src = hashlib.sha256()
@@ -213,8 +214,8 @@ def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh"))
     return src.hexdigest()[:16]
 
 
-STEP_SOURCES = ("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh", "kvq_store_row.cuh",
-                "kvq_tables_item.cuh")
+STEP_SOURCES = ("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh", "kvq_ranges.h",
+                "kvq_store_row.cuh", "kvq_tables_item.cuh")
 
 
 def traffic_from_profile(workload: str, kind: str = "decode"):

@@ -16,7 +16,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 SOURCES = ["kvq_api.cu", "kvq_store.cu", "kvq_tables.cu", "kvq_decode.cu", "kvq_prefix.cu",
            "kvq_extend.cu", "kvq_extend_tc.cu", "kvq_copy.cu", "kvq_noalloc.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_tile.cuh", "kvq_umma.cuh", "kvq_store_row.cuh",
-           "kvq_tables_item.cuh"]
+           "kvq_tables_item.cuh", "kvq_ranges.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

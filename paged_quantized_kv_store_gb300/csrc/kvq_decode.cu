@@ -152,88 +152,6 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch
   } while (c.nblk == 0);
 }
 
-// How the block stream is cut into ranges, each ending in at most two partial
-// records per q head. Static part: warp w owns blocks [w Pst, (w + 1) Pst) of
-// the first nwarps * Pst. Tail (C > 0): the rest in chunks of C blocks, taken
-// one at a time from a counter by whichever warp is free, so that warps whose
-// static part ran slower (the co-resident CTAs of an SM do not get equal
-// shares of it) are not waited for. Range ids: warps 0 .. nwarps - 1, then
-// nwarps + tail chunk.
-struct RangeMap {
-  int64_t nwarps;
-  int Pst;        // blocks per static range
-  int C;          // blocks per tail chunk; 0: no tail (static ranges cover all)
-  int64_t ntail;  // tail chunks
-  // k > 0: the static ranges are laid out per q-head group instead: group
-  // hgi's tb blocks are cut into k ranges of Pst (the last one shorter),
-  // ranges hgi k .. hgi k + k - 1, the same cut in every group (no tail)
-  int k;
-  int tb;
-};
-
-__host__ __device__ __forceinline__ int64_t range_of(const RangeMap& m, int64_t x) {
-  if (m.k > 0) {
-    const int64_t hgi = x / m.tb;
-    return hgi * m.k + (x - hgi * m.tb) / m.Pst;
-  }
-  if (m.C == 0) return x / m.Pst;
-  const int64_t ns = m.nwarps * m.Pst;
-  return x < ns ? x / m.Pst : m.nwarps + (x - ns) / m.C;
-}
-
-__host__ __device__ __forceinline__ int64_t range_start(const RangeMap& m, int64_t r) {
-  if (m.k > 0) return (r / m.k) * m.tb + (r % m.k) * m.Pst;
-  if (m.C == 0 || r < m.nwarps) return r * m.Pst;
-  return m.nwarps * m.Pst + (r - m.nwarps) * m.C;
-}
-
-// Static ranges cut the same way in every q-head group when the grid has at
-// least a warp per group: then the warps of different kv heads read the same
-// requests' blocks at the same time, and a block's token rows (the kv heads
-// side by side) leave DRAM together instead of as scattered 64-256-byte
-// pieces. Each group's tb blocks go to k = min(warps / groups, tb / P_min)
-// ranges; the rest of the warps stay idle. Measured per kind: INT8 GQA-4
-// (80 blocks per warp) 6 % faster, bf16 GQA-2 1 %, INT4 GQA-4 3 % slower
-// (its decode is bound by in-block latency, not DRAM), and nothing to gain
-// for shares under 16 blocks; `lockstep` says whether to use it.
-__device__ __forceinline__ RangeMap static_range_map(int64_t total, int tb, int groups,
-                                                     int64_t nwarps, int P, int min_blocks,
-                                                     bool lockstep) {
-  RangeMap m{nwarps, P, 0, 0, 0, tb};
-  if (!lockstep || P < 16 || tb <= 0 || groups > nwarps) return m;
-  const int64_t k = min(nwarps / groups,
-                        (static_cast<int64_t>(tb) + min_blocks - 1) / min_blocks);
-  m.k = static_cast<int>(k);
-  m.Pst = static_cast<int>((tb + k - 1) / k);
-  return m;
-}
-
-// The map for `total` blocks over `nwarps` warps with per-warp range length P
-// (the even share, at least the plan's minimum). A tail needs a counter (an
-// automatic split) and P >= kTailMinShare: only long ranges drift apart by
-// more than a short chunk, and a chunk pays a pipeline fill and its own
-// partial records. It takes about a tenth of the blocks, in at most 4 chunks
-// per warp of at least 8 blocks, and is dropped when the workspace holds
-// fewer than nwarps + ntail ranges.
-__device__ __forceinline__ RangeMap make_range_map(const DecodeArgs& a, int64_t total, int tb,
-                                                   int groups, int64_t nwarps, int P,
-                                                   bool lockstep) {
-  if (a.tail_ctr == nullptr || P < kTailMinShare)
-    return static_range_map(total, tb, groups, nwarps, P, a.min_blocks_per_warp, lockstep);
-  RangeMap m{nwarps, P, 0, 0, 0, tb};
-  constexpr int c0 = 8;
-  const int64_t per = (9 * total) / (10 * nwarps * c0);  // static chunks per warp
-  const int64_t rem = total - nwarps * per * c0;
-  const int64_t c = max(static_cast<int64_t>(c0), (rem + 4 * nwarps - 1) / (4 * nwarps));
-  const int64_t ntail = (rem + c - 1) / c;
-  if (nwarps + ntail > a.max_ranges)
-    return static_range_map(total, tb, groups, nwarps, P, a.min_blocks_per_warp, lockstep);
-  m.Pst = static_cast<int>(per * c0);
-  m.C = static_cast<int>(c);
-  m.ntail = ntail;
-  return m;
-}
-
 // The decode of CTA `cta` out of `ncta` (the persistent grid); dsmem is the
 // CTA's dynamic shared memory, warp_sum 4 ints of static shared memory.
 // TAIL: the instantiation that can hand out tail chunks (make_range_map);
@@ -292,7 +210,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
                                                                     : a.min_blocks_per_warp);
   constexpr bool kLockstep = KV != kI4;
   const RangeMap rm =
-      TAIL ? make_range_map(a, total, tb, groups, nwarps, P, kLockstep)
+      TAIL ? make_range_map(a.tail_ctr != nullptr, a.max_ranges, a.min_blocks_per_warp, total,
+                            tb, groups, nwarps, P, kLockstep)
            : static_range_map(total, tb, groups, nwarps, P, a.min_blocks_per_warp, kLockstep);
   if (cta == 0) {
     // what the combine kernel needs, and the all-zero rows of empty requests

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "kvq.h"
+#include "kvq_ranges.h"
 
 namespace kvq {
 
@@ -179,7 +180,6 @@ constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many 
 constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)
 constexpr int kHdrCum = 5;                 // first prefix sum in the decode's header
 constexpr int kRangesPerWarp = 5;          // records the workspace holds: static + tail
-constexpr int kTailMinShare = 128;         // blocks per warp from which the decode has a tail
 constexpr int kMaxPrefixChunk = 32;    // shared blocks per prefix unit: one table window
 
 }  // namespace kvq
