@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kDecodeThreads, KV == kI4 && !TAIL ? kMaxCtasP
 
 template <int KV, bool QBF, bool TAIL>
 cudaError_t launch_step_t(const StepArgs& a, int grid, cudaStream_t s) {
-  static int opted_in_device = -1;
+  thread_local int opted_in_device = -1;  // per host thread: no shared state
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -804,7 +804,7 @@ template <int KV, bool QBF, bool TAIL>
 int step_occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(step_kernel<KV, QBF, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes_for<KV>(kMaxBatch))) != cudaSuccess)
@@ -823,7 +823,7 @@ template <int KV, bool QBF, bool TAIL>
 cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   // allow the largest dynamic shared memory the kernel can ask for, once
   // per device
-  static int opted_in_device = -1;
+  thread_local int opted_in_device = -1;  // per host thread: no shared state
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -842,7 +842,7 @@ template <int KV, bool QBF, bool TAIL>
 int occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(decode_kernel<KV, QBF, TAIL>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,

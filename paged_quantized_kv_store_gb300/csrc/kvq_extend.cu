@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(128) extend_combine_kernel(const __grid_consta
 
 template <int KV, bool QBF>
 cudaError_t launch_t(const ExtendArgs& a, int grid, cudaStream_t s) {
-  static int opted_in_device = -1;
+  thread_local int opted_in_device = -1;  // per host thread: no shared state
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -529,7 +529,7 @@ template <int KV, bool QBF>
 int occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(extend_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(extend_smem_bytes<KV>(kMaxBatch))) != cudaSuccess)

@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int KV, bool QBF>
 cudaError_t launch_tc_t(const ExtendArgs& a, int grid, cudaStream_t s) {
-  static int opted_in_device = -1;
+  thread_local int opted_in_device = -1;  // per host thread: no shared state
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -602,7 +602,7 @@ template <int KV, bool QBF>
 int tc_occupancy_t(int batch) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  static int cached_dev = -1, cached_batch = -1, cached_n = 0;
+  thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(tc_smem_bytes(kMaxBatch))) != cudaSuccess ||

@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
 template <int KV, bool QBF>
 cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
-  static int opted_in_device = -1;
+  thread_local int opted_in_device = -1;  // per host thread: no shared state
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -483,7 +483,7 @@ int occupancy_t(int num_groups) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   // cached: a captured step (CUDA graph) repeats the call without new queries
-  static int cached_dev = -1, cached_groups = -1, cached_n = 0;
+  thread_local int cached_dev = -1, cached_groups = -1, cached_n = 0;
   if (dev == cached_dev && num_groups == cached_groups) return cached_n;
   if (cudaFuncSetAttribute(prefix_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(prefix_smem_bytes<KV>(kMaxBatch))) != cudaSuccess)
