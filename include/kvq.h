@@ -274,9 +274,12 @@ kvq_status paged_decode_attn_shared_prefix(
  * it until the process exits); nothing is allocated by the call. The caller
  * still passes inputs and outputs, with the meaning and layout of
  * paged_decode_attn.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *    in the current context, so a context made anew on the device (after
+ *    cudaDeviceReset, or one the caller makes current) is served at the
+ *    array's address there. The first call in a context may load the
+ *    library's device code into it: make that first call before any stream
+ *    capture; later calls only read a host-side table.
  *  - Sizes whose static ranges alone need more than KVQ_NOALLOC_SCRATCH_BYTES
  *    are rejected with KVQ_ERR_WORKSPACE before anything is launched; sizes
  *    whose full workspace does not fit run without the tail.

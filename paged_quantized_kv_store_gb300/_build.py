@@ -13,9 +13,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libkvq.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["kvq_api.cu", "kvq_store.cu", "kvq_tables.cu", "kvq_decode.cu", "kvq_prefix.cu",
+SOURCES = ["kvq_api.cu", "kvq_store.cu", "kvq_tables.cu", "kvq_decode.cu", "kvq_decode_gqa.cu",
+           "kvq_prefix.cu",
            "kvq_extend.cu", "kvq_extend_tc.cu", "kvq_copy.cu", "kvq_noalloc.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_tile.cuh", "kvq_umma.cuh", "kvq_store_row.cuh",
+           "kvq_decode_common.cuh",
            "kvq_tables_item.cuh", "kvq_ranges.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

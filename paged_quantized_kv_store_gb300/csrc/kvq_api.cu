@@ -184,9 +184,14 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
   kvq::DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (pool->kv_dtype == KVQ_INT8) {  // the INT8 kernel stages its tiles by TMA
-    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
-        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
+  // the INT8 kernels and the grouped-query kernel (INT8 and INT4) stage their
+  // tiles by TMA; the fused step keeps the general kernel
+  const bool gqa = pre == nullptr &&
+                   kvq::decode_gqa_supported(pool->kv_dtype, q_dtype, q_heads / pool->kv_heads);
+  if (pool->kv_dtype == KVQ_INT8 || gqa) {
+    const int row = pool->kv_dtype == KVQ_INT8 ? kHeadDim : kHeadDim / 2;
+    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, row) ||
+        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, row))
       return KVQ_ERR_CUDA;
   } else {
     std::memset(&a.k_map, 0, sizeof(a.k_map));
@@ -266,12 +271,15 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   }
   // persistent grid: as many CTAs as fit on the device at once (the
   // workspace has partial slots for kMaxCtasPerSm per SM)
-  const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
-                              kvq::kMaxCtasPerSm);
+  const int per_sm = std::min(
+      gqa ? kvq::decode_gqa_ctas_per_sm(pool->kv_dtype, batch, tail)
+          : kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
+      kvq::kMaxCtasPerSm);
   if (per_sm <= 0) return KVQ_ERR_CUDA;
   const int grid = plan.num_sms * per_sm;
-  if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s) != cudaSuccess)
-    return KVQ_ERR_CUDA;
+  const cudaError_t le = gqa ? kvq::launch_decode_gqa(a, pool->kv_dtype, grid, s)
+                             : kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s);
+  if (le != cudaSuccess) return KVQ_ERR_CUDA;
   if (kvq::launch_combine(a, q_dtype, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

@@ -55,6 +55,7 @@
 //   same way once per request).
 #include <cuda_runtime.h>
 
+#include "kvq_decode_common.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_store_row.cuh"
@@ -63,94 +64,6 @@
 
 namespace kvq {
 namespace {
-
-// Dynamic shared memory: [prefix sums of the blocks per request][slack to a
-// 1024-byte boundary][the stage regions of the 4 warps].
-template <int KV>
-__host__ __device__ constexpr size_t smem_bytes_for(int batch) {
-  return align128((batch + 1) * sizeof(int32_t)) + 1024 +
-         static_cast<size_t>(kWarps) * Stage<KV>::kWarpBytes;
-}
-
-// Clamped length of request b.
-__device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
-  return min(max(a.seq_lens[b], 0), a.len_cap);
-}
-
-// Leading blocks of request b attended by the shared-prefix kernel (0 in a
-// plain decode).
-__device__ __forceinline__ int skip_of(const DecodeArgs& a, int b) {
-  return a.skip != nullptr ? a.skip[b] : 0;
-}
-
-// Blocks of request b this kernel reads.
-__device__ __forceinline__ int own_blocks(const DecodeArgs& a, int b) {
-  return max((clamped_len(a, b) + kBlock - 1) / kBlock - skip_of(a, b), 0);
-}
-
-// Merges the shared-prefix records of (request, q head) `row` into a state
-// (max m, sum l, unnormalised output acc of the 16 dims [16 g, 16 g + 16)).
-__device__ __forceinline__ void merge_prefix(const DecodeArgs& a, int64_t row, int skip, int g,
-                                             float& m, float& l, float (&acc)[16]) {
-  const int npc = (skip + a.pchunk - 1) / a.pchunk;
-  const float* rec0 = a.ppart + row * a.pmax_chunks * kPartStride;
-  float M = m;
-  for (int c = 0; c < npc; ++c) M = fmaxf(M, rec0[c * kPartStride + kHeadDim]);
-  if (M == -INFINITY) return;
-  const float al = m == -INFINITY ? 0.f : ex2(m - M);
-  l *= al;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] *= al;
-  for (int c = 0; c < npc; ++c) {
-    const float* rec = rec0 + c * kPartStride;
-    const float mc = rec[kHeadDim];
-    const float e = mc == -INFINITY ? 0.f : ex2(mc - M);
-    l += e * rec[kHeadDim + 1];
-    const float4* v = reinterpret_cast<const float4*>(rec + 16 * g);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 x = v[q];
-      acc[4 * q] += e * x.x;
-      acc[4 * q + 1] += e * x.y;
-      acc[4 * q + 2] += e * x.z;
-      acc[4 * q + 3] += e * x.w;
-    }
-  }
-  m = M;
-}
-
-// Position in the block stream: q-head group hgi (kv head * head_groups +
-// group), request b, block j of nblk.
-struct Cursor {
-  int hgi, b, j, nblk;
-};
-
-__device__ __forceinline__ void locate(Cursor& c, int64_t x, const int32_t* cum, int batch,
-                                       int tb) {
-  c.hgi = static_cast<int>(x / tb);
-  const int r = static_cast<int>(x - static_cast<int64_t>(c.hgi) * tb);
-  int lo = 0, hi = batch - 1;  // largest b with cum[b] <= r: the non-empty request holding r
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= r) lo = mid; else hi = mid - 1;
-  }
-  c.b = lo;
-  c.j = r - cum[lo];
-  c.nblk = cum[lo + 1] - cum[lo];
-}
-
-// Next block of the stream (the caller knows there is one).
-__device__ __forceinline__ void advance(Cursor& c, const int32_t* cum, int batch) {
-  if (++c.j < c.nblk) return;
-  c.j = 0;
-  do {
-    if (++c.b == batch) {
-      c.b = 0;
-      ++c.hgi;
-    }
-    c.nblk = cum[c.b + 1] - cum[c.b];
-  } while (c.nblk == 0);
-}
 
 // The decode of CTA `cta` out of `ncta` (the persistent grid); dsmem is the
 // CTA's dynamic shared memory, warp_sum 4 ints of static shared memory.
@@ -168,74 +81,19 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
   constexpr bool kPCorr = CodeOffset<KV, QBF>::kPCorr;
   constexpr int D = S::kDepth;
 
-  int32_t* cum = reinterpret_cast<int32_t*>(dsmem);  // [batch + 1]: blocks before request b
-  unsigned char* stages = dsmem + align128((a.batch + 1) * sizeof(int32_t));
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
 
-  // ---- blocks per request, prefix-summed (every CTA) --------------------------
-  {
-    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
-    const int b0 = min(tid * per, a.batch), b1 = min(b0 + per, a.batch);
-    int sum = 0;
-    for (int b = b0; b < b1; ++b) {
-      sum += own_blocks(a, b);
-      if (cta == 0 && a.seq_lens[b] > a.len_cap) report(a.dev_err, KVQ_DEV_ERR_LENGTH);
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_sum[w];
-    int run = base + incl - sum;
-    for (int b = b0; b < b1; ++b) {
-      cum[b] = run;
-      run += own_blocks(a, b);
-    }
-    if (tid == kDecodeThreads - 1) cum[a.batch] = base + incl;
-    __syncthreads();
-  }
-  const int tb = cum[a.batch];  // blocks of one q-head group over all requests
-  const int groups = a.kv_heads * a.head_groups;
-  const int64_t total = static_cast<int64_t>(tb) * groups;
-  const int64_t nwarps = static_cast<int64_t>(ncta) * kWarps;
-  const int64_t even_share = (total + nwarps - 1) / nwarps;
-  const int P = static_cast<int>(even_share > a.min_blocks_per_warp ? even_share
-                                                                    : a.min_blocks_per_warp);
+  // ---- blocks per request, prefix-summed (every CTA); the cut into ranges ------
   constexpr bool kLockstep = KV != kI4;
-  const RangeMap rm =
-      TAIL ? make_range_map(a.tail_ctr != nullptr, a.max_ranges, a.min_blocks_per_warp, total,
-                            tb, groups, nwarps, P, kLockstep)
-           : static_range_map(total, tb, groups, nwarps, P, a.min_blocks_per_warp, kLockstep);
-  if (cta == 0) {
-    // what the combine kernel needs, and the all-zero rows of empty requests
-    // (a request whose only blocks are shared ones is written by the combine
-    // kernel)
-    if (tid == 0) {
-      a.hdr[0] = tb;
-      a.hdr[1] = rm.Pst;
-      a.hdr[2] = rm.C;
-      a.hdr[3] = static_cast<int32_t>(nwarps);
-      a.hdr[4] = rm.k;
-    }
-    for (int b = tid; b <= a.batch; b += kDecodeThreads) a.hdr[kHdrCum + b] = cum[b];
-    for (int b = 0; b < a.batch; ++b) {
-      if (cum[b + 1] != cum[b] || skip_of(a, b) > 0) continue;
-      for (int e = tid; e < a.q_heads * kHeadDim; e += kDecodeThreads)
-        store_out<QBF>(a.out, static_cast<int64_t>(b) * a.q_heads * kHeadDim + e, 0.f);
-    }
-  }
+  const StreamPlan sp = plan_stream<QBF, TAIL>(a, dsmem, warp_sum, cta, ncta, kLockstep);
+  const int32_t* cum = sp.cum;
+  unsigned char* stages = sp.stages;
+  const int tb = sp.tb;
 
   // ---- this warp's ranges: its static range, then tail chunks ----------------------
   // (no block barrier follows: warps are independent from here)
   const int64_t gw = static_cast<int64_t>(cta) * kWarps + warp;
-  const int64_t static_end = rm.C == 0 ? total : nwarps * rm.Pst;
   // this warp's stage region, 1024-byte aligned (the 128-byte swizzle repeats
   // every 1024 bytes)
   const uint32_t region0 =
@@ -562,34 +420,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, unsigned char* 
     return true;
   };  // run_range
 
-  // the static range (the whole share when there is no tail) ...
-  if (rm.k > 0) {  // the same cut in every q-head group
-    if (gw >= static_cast<int64_t>(groups) * rm.k) return;
-    const int64_t hgi = gw / rm.k, i = gw - hgi * rm.k;
-    const int64_t lo = i * rm.Pst;
-    if (lo < tb) run_range(hgi * tb + lo, static_cast<int>(min(tb - lo,
-                                                                static_cast<int64_t>(rm.Pst))),
-                           gw);
-    return;
-  }
-  const int64_t xs = gw * rm.Pst;
-  if (xs < static_end &&
-      !run_range(xs, static_cast<int>(min(static_end - xs, static_cast<int64_t>(rm.Pst))), gw))
-    return;
-  if constexpr (TAIL) {
-    if (rm.C == 0) return;
-    // ... then tail chunks while there are any
-    for (;;) {
-      unsigned int c = 0;
-      if (lane == 0) c = atomicAdd(a.tail_ctr, 1u);
-      c = __shfl_sync(kFull, c, 0);
-      if (c >= rm.ntail) return;
-      const int64_t x0 = static_end + static_cast<int64_t>(c) * rm.C;
-      if (!run_range(x0, static_cast<int>(min(total - x0, static_cast<int64_t>(rm.C))),
-                     nwarps + c))
-        return;
-    }
-  }
+  for_each_range<TAIL>(a, sp, gw, lane, run_range);
 }
 
 template <int KV, bool QBF, bool TAIL>
@@ -597,6 +428,8 @@ __global__ void __launch_bounds__(kDecodeThreads, TAIL && KV != kI4 ? 3 : 1)
     decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ int32_t warp_sum[kWarps];
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;");
   decode_body<KV, QBF, TAIL>(a, dsmem, warp_sum, blockIdx.x, gridDim.x);
 }
 
@@ -696,8 +529,12 @@ __device__ __forceinline__ void combine_row(const DecodeArgs& a, int64_t bh, int
   merge_pieces<QBF>(a, bh, hh, lane, r_first, nd, seg_start, rm, npc);
 }
 
+// Launched as a programmatic dependent of the decode kernel: its CTAs may
+// start while the decode runs and wait here until the decode grid has
+// finished and its records are visible.
 template <bool QBF>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   combine_row<QBF>(a, static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5),
                    threadIdx.x & 31);
 }
@@ -928,12 +765,17 @@ cudaError_t launch_decode(const DecodeArgs& a, int kv_dtype, int q_dtype, int gr
 cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.batch) * a.q_heads;
   if (rows == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
-  if (q_dtype == kBF16)
-    combine_kernel<true><<<grid, 128, 0, s>>>(a);
-  else
-    combine_kernel<false><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the decode's tail
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return q_dtype == kBF16 ? cudaLaunchKernelEx(&cfg, combine_kernel<true>, a)
+                          : cudaLaunchKernelEx(&cfg, combine_kernel<false>, a);
 }
 
 cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid,

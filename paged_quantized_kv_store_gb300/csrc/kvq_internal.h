@@ -171,6 +171,11 @@ cudaError_t launch_prefix(const DecodeArgs& a, int kv_dtype, int q_dtype, int gr
 
 // CTAs of the decode kernel resident per SM (occupancy) for a dtype pair and batch
 int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail);
+// The grouped-query decode kernel (kvq_decode_gqa.cu): INT8 / INT4 pools, fp16
+// queries, 4 q heads per kv head; same workspace, records and combine.
+bool decode_gqa_supported(int kv_dtype, int q_dtype, int group);
+cudaError_t launch_decode_gqa(const DecodeArgs& a, int kv_dtype, int grid, cudaStream_t s);
+int decode_gqa_ctas_per_sm(int kv_dtype, int batch, bool tail);
 // the same for the shared-prefix kernel and a number of groups
 int prefix_ctas_per_sm(int kv_dtype, int q_dtype, int num_groups);
 

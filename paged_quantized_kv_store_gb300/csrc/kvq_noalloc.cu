@@ -14,11 +14,13 @@
 // library holds KVQ_NOALLOC_SCRATCH_BYTES of it until the process exits. Host
 // code cannot use the array's name as a device address (on the host it names
 // a shadow variable), so the device address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current, on the
-// first call made on it.
+// cudaGetSymbolAddress, with the caller's device current, on every call. The
+// address is not cached: it belongs to the module as loaded in the current
+// context, and a context made anew on the same device (after
+// cudaDeviceReset, or another context the caller makes current) loads the
+// module again, possibly elsewhere. Once the module is loaded in a context
+// the lookup is a host-side table read.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "kvq.h"
 
@@ -26,22 +28,11 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device (looked up on
-// the first call for each device). Returns nullptr on failure.
-void* scratch_on_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+// Device address of the scratch array in the current context, or nullptr.
+void* scratch_in_current_context() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
@@ -58,7 +49,7 @@ extern "C" kvq_status paged_decode_attn_noalloc(
   if (st != KVQ_OK) return st;
   // sizes whose static ranges need more scratch than the array holds are
   // refused by paged_decode_attn itself (KVQ_ERR_WORKSPACE, nothing launched)
-  void* scratch = scratch_on_current_device();
+  void* scratch = scratch_in_current_context();
   if (scratch == nullptr) return KVQ_ERR_CUDA;
   return paged_decode_attn(pool, q, q_dtype, out, block_tables, max_blocks_per_seq, seq_lens,
                            batch, q_heads, max_seq_len, sm_scale, num_splits, scratch,

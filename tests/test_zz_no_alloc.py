@@ -20,6 +20,16 @@ pytestmark = pytest.mark.gpu
 from gpu_harness import assert_close, decode, fill_pool, i32, out_to_f64, run_step, to_dev  # noqa: E402
 
 SCRATCH_BYTES = 16 * 1024 * 1024
+PART_STRIDE = 132  # floats per partial record (128 outputs, max, sum, padding)
+HDR_CUM = 5        # ints before the per-request prefix sums in the header
+
+
+def _static_bytes(kvq, batch, q_heads, kv_heads, max_len, splits=0):
+    """Scratch the static ranges alone need: counters, the length header and
+    one record slot (2 rows per q head of a group slot) per warp of the plan."""
+    plan = kvq.paged_decode_attn_plan(batch, q_heads, kv_heads, max_len, splits)
+    records_off = 256 + ((batch + HDR_CUM + 1) * 4 + 255) // 256 * 256
+    return records_off + plan["warps"] * 2 * plan["heads_per_group"] * PART_STRIDE * 4
 
 
 def _noalloc(kvq, wl, pool, bt, num_splits=0):
@@ -52,13 +62,31 @@ def test_two_calls_match_the_workspace_entry_point(gpu):
         assert torch.equal(got.view(torch.int16), again.view(torch.int16))
 
 
+def test_long_gqa_contexts_run_without_the_tail(gpu):
+    # 4 q heads per kv head over long contexts: the array holds the static
+    # ranges but not the balanced tail's records, so this entry point runs
+    # the static cut while paged_decode_attn (full workspace) uses the tail
+    lens = [8192 + 64 * i for i in range(64)]
+    wl = synthetic.custom("noalloc_gqa_long", "int4", lens, 32, 8, seed=92)
+    full = gpu.paged_decode_attn_workspace_size(wl.batch, wl.q_heads, wl.kv_heads,
+                                                wl.max_seq_len, 0)
+    static = _static_bytes(gpu, wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
+    assert static <= SCRATCH_BYTES < full
+    pool = fill_pool(wl)
+    ref, bt, dev_err = run_step(wl, pool)
+    assert gpu.kvq_check_error(dev_err) == 0
+    for _ in range(2):
+        got = _noalloc(gpu, wl, pool, bt)
+        assert_close(out_to_f64(got), out_to_f64(ref))
+
+
 def test_sizes_beyond_the_scratch_are_rejected(gpu):
     # 8 q heads per kv head need 8 partial rows per warp slot: more than the array holds
     wl = synthetic.custom("noalloc_big", "int8", [16], 64, 8, seed=91)
     pool = gpu.KVPool.allocate(wl.num_blocks, wl.kv_heads, "int8")
     batch, q_heads, max_len = 8, 64, 4096
-    need = gpu.paged_decode_attn_workspace_size(batch, q_heads, 8, max_len, 0)
-    assert need > SCRATCH_BYTES
+    # the entry point refuses a size when the static ranges alone do not fit
+    assert _static_bytes(gpu, batch, q_heads, 8, max_len) > SCRATCH_BYTES
     q = torch.zeros((batch, q_heads, 128), dtype=torch.float16, device="cuda")
     out = torch.zeros_like(q)
     bt = torch.zeros((batch, max_len // 16), dtype=torch.int32, device="cuda")
