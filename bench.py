@@ -200,8 +200,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh",
-                             "kvq_ranges.h")) -> str:
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_common.cuh", "kvq_tile.cuh", "kvq_device.cuh",
+                  "kvq_ranges.h")
+GQA_SOURCES = ("kvq_decode_gqa.cu", "kvq_decode_common.cuh", "kvq_tile.cuh", "kvq_device.cuh",
+               "kvq_ranges.h")
+STEP_SOURCES = DECODE_SOURCES + ("kvq_store_row.cuh", "kvq_tables_item.cuh")
+SPEC_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (~8 TB/s)
+
+
+def uses_gqa_kernel(wl, fused: bool = False) -> bool:
+    """Whether the decode call runs the grouped-query kernel (INT8/INT4 pool,
+    fp16 queries, 4 q heads per kv head; not inside the fused step)."""
+    return (not fused and wl.kv_dtype in ("int8", "int4") and wl.q_dtype == "f16"
+            and wl.q_heads == 4 * wl.kv_heads)
+
+
+def kernel_source_sha(files=DECODE_SOURCES) -> str:
     """Hash of the decode kernel's source with // comments and blank lines
     removed, so that editing a comment keeps a DRAM-traffic record valid."""
     src = hashlib.sha256()
@@ -214,15 +228,14 @@ def kernel_source_sha(files=("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh",
     return src.hexdigest()[:16]
 
 
-STEP_SOURCES = ("kvq_decode.cu", "kvq_tile.cuh", "kvq_device.cuh", "kvq_ranges.h",
-                "kvq_store_row.cuh", "kvq_tables_item.cuh")
-
-
 def traffic_from_profile(workload: str, kind: str = "decode"):
-    """DRAM bytes per launch of the decode kernel (kind "decode") or of the
-    fused step kernel (kind "step") from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    sha = kernel_source_sha() if kind == "decode" else kernel_source_sha(STEP_SOURCES)
+    """DRAM bytes per launch of the decode kernel (kind "decode": the general
+    kernel, "gqa": the grouped-query kernel) or of the fused step kernel (kind
+    "step") from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    sha = kernel_source_sha({"decode": DECODE_SOURCES, "gqa": GQA_SOURCES,
+                             "step": STEP_SOURCES}[kind])
+    kind = "decode" if kind == "gqa" else kind
     path = os.path.join(ROOT, "profiles", f"{kind}_{workload}_traffic.txt")
     try:
         text = open(path).read()
@@ -443,6 +456,157 @@ def measure_extend(kvq, dev, reps: int = 10) -> dict:
     except Exception as e:  # noqa: BLE001 - context only
         res["torch_sdpa_fp16"] = f"not measured: {e}"
     del pool, ws
+    return res
+
+
+def store_bytes(wl, n_tokens: int) -> int:
+    """HBM bytes of kv_store_quant for n_tokens: the new K and V rows read
+    (16-bit), the pool rows and scale/zero pairs written, the slot mapping."""
+    row_out = wl.kv_row_bytes() + (4 if wl.quantized else 0)
+    return n_tokens * (2 * wl.kv_heads * (2 * wl.head_dim + row_out) + 8)
+
+
+def time_store(kvq, pool, wl, d_k, d_v, d_slots, dev, peak: float, reps: int = 100) -> dict:
+    """kv_store_quant of the given rows alone (graph-replayed), L2 flushed by
+    a write of twice its size before every call, outside the CUDA events."""
+    import torch
+
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kvq.kv_store_quant(pool, d_k, d_v, d_slots, err)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kvq.kv_store_quant(pool, d_k, d_v, d_slots, err)
+    ms = []
+    for i in range(reps + 3):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ms.append(e0.elapsed_time(e1))
+    if kvq.kvq_check_error(err):
+        raise RuntimeError("device error word set by the store measurement")
+    n = int(d_slots.numel())
+    sb = store_bytes(wl, n)
+    m = float(np.mean(ms))
+    del flush, g
+    return {"tokens": n, "bytes": sb, "ms_mean": round(m, 5),
+            "ms_median": round(float(np.median(ms)), 5),
+            "gbs": round(sb / (m / 1e3) / 1e9, 1), "frac": round(sb / (m / 1e3) / 1e9 / peak, 4),
+            "l2": "flushed before every call", "cuda_graph": True, "reps": reps}
+
+
+def measure_workload(kvq, name: str, dev, peak: float, reps: int = 100) -> dict:
+    """One workload's decode call (paged_decode_attn: decode + combine kernels,
+    graph-replayed, CUDA events on the launching stream) and its store
+    (kv_store_quant of the step's tokens: each request's new token and, for
+    the mixed step, the 4096-token prefill chunk).
+
+    The decode is timed with a cold L2: a pool larger than L2 is read anew by
+    every call; a pool that fits is replicated R times (R x bytes >= 3 x L2)
+    and the calls rotate over the replicas, as the layers of a model would.
+    The warm-L2 time (one pool, back to back) is reported beside it. The
+    store is timed with L2 flushed (a write larger than L2) before every
+    call, outside the timed events."""
+    import torch
+
+    wl = synthetic.by_name(name)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+    def to_dev(bits, dt):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt[dt]).to(dev)
+
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    pool = kvq.KVPool.allocate(wl.num_blocks, wl.kv_heads, wl.kv_dtype, device=dev)
+    for slots, k, v in wl.setup_chunks(max_tokens=1 << 17):
+        kvq.kv_store_quant(pool, to_dev(k, wl.in_dtype), to_dev(v, wl.in_dtype),
+                           torch.from_numpy(slots).to(dev))
+    slots, k_new, v_new = wl.step_store()
+    d_slots = torch.from_numpy(slots).to(dev)
+    d_k, d_v = to_dev(k_new, wl.in_dtype), to_dev(v_new, wl.in_dtype)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvq.kv_store_quant(pool, d_k, d_v, d_slots, err)
+    bt = torch.empty((wl.batch, wl.max_blocks_per_seq), dtype=torch.int32, device=dev)
+    kvq.kvq_block_tables_from_req_to_token(i32(wl.req_to_token), i32(wl.req_pool_indices),
+                                           i32(wl.seq_lens), bt, err)
+    q = to_dev(wl.q(), wl.q_dtype)
+    sl = i32(wl.seq_lens)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(16, kvq.paged_decode_attn_workspace_size(
+        wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, 0)), dtype=torch.uint8, device=dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    alg, logical = decode_algorithmic_bytes(wl), decode_logical_bytes(wl)
+    pool_bytes = pool.nbytes()
+    R = 1 if pool_bytes > 3 * l2 else -(-3 * l2 // pool_bytes)
+    pools = [pool]
+    for _ in range(R - 1):
+        pools.append(kvq.KVPool(pool.k.clone(), pool.v.clone(),
+                                None if pool.k_sz is None else pool.k_sz.clone(),
+                                None if pool.v_sz is None else pool.v_sz.clone(),
+                                pool.num_blocks, pool.kv_heads, pool.kv_dtype))
+    graphs = []
+    for pl in pools:
+        call = (lambda pl=pl: kvq.paged_decode_attn(pl, q, out, bt, sl, wl.max_seq_len,
+                                                    wl.sm_scale, 0, ws, err))
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        graphs.append(g)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(order):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in order]
+        for i in range(min(len(order), 3 * R)):  # warm-up in the same rotation
+            graphs[order[i]].replay()
+        torch.cuda.synchronize()
+        for (e0, e1), r in zip(ev, order):
+            e0.record(stream)
+            graphs[r].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+    cold = timed([i % R for i in range(reps)])
+    warm = timed([0] * reps)
+    if kvq.kvq_check_error(err):
+        raise RuntimeError(f"device error word set by the {name} decode measurement")
+
+    store = time_store(kvq, pool, wl, d_k, d_v, d_slots, dev, peak, reps)
+    mc, mw = float(np.mean(cold)), float(np.mean(warm))
+    res = {
+        "workload": f"{wl.name}: {wl.description}",
+        "kernel": ("grouped-query decode kernel + combine" if uses_gqa_kernel(wl)
+                   else "decode kernel + combine"),
+        "decode_ms_mean": round(mc, 5), "decode_ms_median": round(float(np.median(cold)), 5),
+        "decode_ms_min": round(float(np.min(cold)), 5),
+        "decode_ms_max": round(float(np.max(cold)), 5),
+        "decode_tokens_per_s": round(wl.batch / (mc / 1e3), 1),
+        "algorithmic_bytes": alg, "logical_bytes": logical,
+        "decode_gbs": round(alg / (mc / 1e3) / 1e9, 1),
+        "frac": round(alg / (mc / 1e3) / 1e9 / peak, 4),
+        "frac_of_spec_8tbs": round(alg / (mc / 1e3) / 1e9 / SPEC_HBM_GBS, 4),
+        "logical_gbs": round(logical / (mc / 1e3) / 1e9, 1),
+        "l2": (f"cold: {R} replica pools rotated ({R} x {pool_bytes / 1e6:.1f} MB >= 3 x L2 of "
+               f"{l2 / 1e6:.0f} MB)" if R > 1 else
+               f"cold: the pool ({pool_bytes / 1e6:.0f} MB) is more than 3 x L2"),
+        "warm_l2": {"decode_ms_mean": round(mw, 5),
+                    "decode_gbs": round(alg / (mw / 1e3) / 1e9, 1),
+                    "frac": round(alg / (mw / 1e3) / 1e9 / peak, 4)},
+        "store": store,
+        "cuda_graph": True, "reps": reps,
+    }
+    del graphs, pools, pool, ws
+    torch.cuda.empty_cache()
     return res
 
 
@@ -673,12 +837,16 @@ def run_ours(args, rank: int, world: int, dist):
     peak, peak_kind = measured_peak()
     achieved = alg / (mean_decode_ms / 1e3) / 1e9
     single = args.fused_step and launches_per_step == 1
-    traffic, sha = traffic_from_profile(wl.name, "step" if single else "decode")
+    gqa = uses_gqa_kernel(wl, fused=bool(args.fused_step))
+    traffic, sha = traffic_from_profile(wl.name, "step" if single else ("gqa" if gqa else "decode"))
+    if gqa and groups is None and not args.fused_step:
+        decode_kernels = "paged_decode_attn (decode_gqa_kernel + combine_kernel)"
     roofline = {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "traffic": traffic,
         "kernel": decode_kernels,
         "peak_kind": f"{peak_kind} (hbm_gbs)",
+        "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
         "algorithmic_bytes_per_launch": alg, "logical_bytes_per_launch": logical,
         "decode_ms_mean": round(mean_decode_ms, 5),
         "decode_ms_median": round(float(np.median(decode_ms)), 5),
@@ -690,10 +858,26 @@ def run_ours(args, rank: int, world: int, dist):
         "frac_of_this_gpu_copy": round(achieved / box_copy, 4),
     }
 
+    # the step's store (each request's new token, and a prefill chunk if the
+    # step has one) alone, L2 flushed before each call
+    store = time_store(kvq, pool, wl, d_in["k_new"], d_in["v_new"], d_in["slot_mapping"], dev,
+                       peak, reps=50)
+    l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    pool_bytes = pool.nbytes()
+    l2_note = (f"no flush: the pool ({pool_bytes / 1e6:.0f} MB) is more than 3 x L2 "
+               f"({l2_bytes / 1e6:.0f} MB); every step reads it anew" if pool_bytes > 3 * l2_bytes
+               else f"warm L2: the pool ({pool_bytes / 1e6:.0f} MB) fits in L2 "
+                    f"({l2_bytes / 1e6:.0f} MB); the cold-L2 figure of this workload is in "
+                    f"extras.workloads")
+
     extras = None
     if not args.no_extras:
-        extras = {"kvq_copy_blocks": measure_block_copy(kvq, pool, wl, dev, peak),
-                  "paged_extend_attn": measure_extend(kvq, dev)}
+        extras = {"workloads": {}}
+        for name in ("cfg2", "cfg4", "cfg5"):
+            if name != wl.name:
+                extras["workloads"][name] = measure_workload(kvq, name, dev, peak)
+        extras["kvq_copy_blocks"] = measure_block_copy(kvq, pool, wl, dev, peak)
+        extras["paged_extend_attn"] = measure_extend(kvq, dev)
         if fstep is not None:
             sep = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq,
                                  wl.max_seq_len, tdt[wl.q_dtype], num_splits=args.num_splits,
@@ -719,12 +903,12 @@ def run_ours(args, rank: int, world: int, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"int8": "u8", "int4": "u4", "f16": "f16", "bf16": "bf16"}[wl.kv_dtype],
         "data": "synthetic (seeded counter-based generator; no dataset)",
-        "config": {**workload_desc(wl), "l2": "no flush: the pool is larger than L2",
+        "config": {**workload_desc(wl), "l2": l2_note,
                    "cuda_graph": use_graph, "fused_step": bool(args.fused_step),
                    "shared_prefix": None if groups is None else
                    {"groups": 1, "members": len(groups[0]), "shared_blocks": groups[1]},
                    "plan": plan, "parallelism": f"replicas x{world} (no data-path collective)"},
-        "roofline": roofline, "clocks": clocks, "e2e": e2e,
+        "roofline": roofline, "store": store, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "decode_hbm_gbs": round(achieved, 1),
         "extras": extras,
@@ -770,7 +954,53 @@ def _oracle_step(wl, reqs, q, k_new, v_new):
     return outs
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip().lower() == "model name":
+                return f"{line.split(':', 1)[1].strip()} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_store_rate(wl, budget_s: float) -> dict:
+    """The oracle's quantizing store of the step's tokens (each request's new
+    token, and the prefill chunk if the step has one), one host core, on as
+    many of them as fit the time budget."""
+    import oracle
+    slots, k, v = wl.step_store()
+    n = len(slots)
+    pool = oracle.Pool(wl.num_blocks, wl.kv_heads, wl.head_dim, wl.kv_dtype)
+    t = time.perf_counter()
+    oracle.kv_store(pool, k[:1], v[:1], wl.in_dtype, slots[:1])
+    per_tok = max(time.perf_counter() - t, 1e-7)
+    m = int(max(1, min(n, budget_s / per_tok)))
+    t = time.perf_counter()
+    oracle.kv_store(pool, k[:m], v[:m], wl.in_dtype, slots[:m])
+    dt = time.perf_counter() - t
+    sb = store_bytes(wl, m)
+    return {"tokens": m, "of_tokens": n, "s": round(dt, 4),
+            "tokens_per_s": round(m / dt, 1), "gbs": round(sb / dt / 1e9, 4)}
+
+
 def cpu_baseline(wl, budget_s: float = 20.0, n_req: int = 0) -> dict:
+    """The oracle, single-threaded, on a bounded sample of the workload: the
+    decode of a sample of requests (block table, store of the new token, fp64
+    attention of every q head) gives the line's value; the store of the
+    step's tokens is timed on its own beside it."""
     q = wl.q()
     k_new, v_new = wl.new_rows("k"), wl.new_rows("v")
     if n_req <= 0:
@@ -783,10 +1013,14 @@ def cpu_baseline(wl, budget_s: float = 20.0, n_req: int = 0) -> dict:
     t = time.perf_counter()
     _oracle_step(wl, reqs, q, k_new, v_new)
     dt = time.perf_counter() - t
+    store = _oracle_store_rate(wl, budget_s=min(5.0, budget_s / 4))
     return {"value": round(n_req / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n_req} of the {wl.batch} requests of one step (block table, store of "
                       f"the new token, fp64 decode of all {wl.q_heads} q heads), "
-                      f"{dt:.1f} s on one host core"}
+                      f"{dt:.1f} s on one host core",
+            "decode": {"requests": n_req, "s": round(dt, 3),
+                       "requests_per_s": round(n_req / dt, 3)},
+            "store": store, "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank: int):
@@ -821,7 +1055,7 @@ def run_reference(args, rank: int):
         "config": {**workload_desc(wl), "reference": "CPU oracle (oracle/kvq_oracle.cpp), "
                    "single-threaded; the pages ship no code to install"},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "nproc": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -386,6 +386,19 @@ kvq_status kvq_decode_step(const kvq_pool* pool, const int32_t* req_to_token,
                            int32_t* dev_err, void* stream);
 
 /*
+ * kvq_selftest_step_barrier -- a self-test of the bounded grid barrier that
+ * kvq_decode_step's single launch waits at (the pages have no counterpart:
+ * it checks this library's failure handling). One cooperative launch of
+ * `grid_ctas` CTAs (0: one per SM) meets at that barrier, made to wait for
+ * one CTA more than the grid has, with a limit of limit_us microseconds: the
+ * wait runs out, sets KVQ_DEV_ERR_TIMEOUT in *dev_err and every CTA returns,
+ * leaving the context usable. counter: a device word, zero at the call (it
+ * counts the arrivals). Asynchronous on `stream`; allocates nothing.
+ */
+kvq_status kvq_selftest_step_barrier(uint32_t* counter, int32_t grid_ctas, int32_t limit_us,
+                                     int32_t* dev_err, void* stream);
+
+/*
  * kvq_copy_blocks -- copy whole blocks from one pool to another (LMDeploy
  * article §4.4: the cache engine swaps blocks between the GPU and the CPU
  * cache by a {dst: src} map, K and V alike; inside one pool the same copy

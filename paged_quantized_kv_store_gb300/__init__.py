@@ -116,6 +116,8 @@ def load(build_if_missing: bool = False):
     lib.kvq_decode_step.restype = ctypes.c_int
     lib.kvq_decode_step_fused.argtypes = [I32, I64]
     lib.kvq_decode_step_fused.restype = I32
+    lib.kvq_selftest_step_barrier.argtypes = [P, I32, I32, P, P]
+    lib.kvq_selftest_step_barrier.restype = ctypes.c_int
     lib.kvq_copy_blocks.argtypes = [ctypes.POINTER(_Pool), ctypes.POINTER(_Pool), P, P, I64, P, P]
     lib.kvq_copy_blocks.restype = ctypes.c_int
     lib.kvq_check_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -458,6 +460,15 @@ def kvq_check_error(dev_err, stream=None) -> int:
     if st not in (0, 4):
         _check(st, "kvq_check_error")
     return int(bits.value)
+
+
+def kvq_selftest_step_barrier(counter, dev_err, grid_ctas=0, limit_us=5000, stream=None):
+    """The fused step's bounded grid barrier made to wait for one CTA more
+    than the grid has (a self-test of its timeout); see kvq.h."""
+    lib = load()
+    st = lib.kvq_selftest_step_barrier(_ptr(counter), int(grid_ctas), int(limit_us),
+                                       _ptr(dev_err), _stream(stream))
+    _check(st, "kvq_selftest_step_barrier")
 
 
 def kvq_status_string(status: int) -> str:

@@ -184,14 +184,13 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   if (!aligned16(out)) return KVQ_ERR_INVALID_ARG;
   kvq::DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
-  // the INT8 kernels and the grouped-query kernel (INT8 and INT4) stage their
-  // tiles by TMA; the fused step keeps the general kernel
+  // the grouped-query kernel (INT8 / INT4 pools, fp16 queries, 4 q heads per
+  // kv head) serves the plain decode; the fused step keeps the general kernel
   const bool gqa = pre == nullptr &&
                    kvq::decode_gqa_supported(pool->kv_dtype, q_dtype, q_heads / pool->kv_heads);
-  if (pool->kv_dtype == KVQ_INT8 || gqa) {
-    const int row = pool->kv_dtype == KVQ_INT8 ? kHeadDim : kHeadDim / 2;
-    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, row) ||
-        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, row))
+  if (pool->kv_dtype == KVQ_INT8) {  // the general INT8 kernels stage their tiles by TMA
+    if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
+        !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
       return KVQ_ERR_CUDA;
   } else {
     std::memset(&a.k_map, 0, sizeof(a.k_map));
@@ -578,6 +577,20 @@ kvq_status kvq_decode_step_workspace_size(int32_t batch, int32_t q_heads, int32_
   if (st != KVQ_OK) return st;
   *bytes = step_workspace(plan);
   return KVQ_OK;
+}
+
+kvq_status kvq_selftest_step_barrier(uint32_t* counter, int32_t grid_ctas, int32_t limit_us,
+                                     int32_t* dev_err, void* stream) {
+  if (counter == nullptr || dev_err == nullptr || grid_ctas < 0 || limit_us <= 0 ||
+      limit_us > 1000000)
+    return KVQ_ERR_INVALID_ARG;
+  const int grid = grid_ctas > 0 ? grid_ctas : current_sm_count();
+  if (grid <= 0) return KVQ_ERR_CUDA;
+  return kvq::launch_barrier_selftest(counter, dev_err, grid,
+                                      static_cast<uint64_t>(limit_us) * 1000ull,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
 
 int32_t kvq_decode_step_fused(int32_t batch, int64_t num_tokens) {

@@ -545,9 +545,11 @@ constexpr int kStepUnroll = 4;  // table entries / pool rows a half-warp has in 
 
 // Grid-wide barrier of a cooperative launch: thread 0 of every CTA counts in
 // and waits, with acquire loads, until `target` CTAs have; the wait gives up
-// after 2 s (KVQ_DEV_ERR_TIMEOUT, false: the caller stops).
+// after limit_ns (2 s in the step; KVQ_DEV_ERR_TIMEOUT, false: the caller
+// stops).
 __device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target,
-                                          int32_t* dev_err) {
+                                          int32_t* dev_err,
+                                          uint64_t limit_ns = 2000000000ull) {
   __shared__ int ok_s;
   asm volatile("fence.proxy.async.global;" ::: "memory");  // global writes before TMA reads
   __syncthreads();
@@ -560,7 +562,7 @@ __device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target
       unsigned int v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if (global_ns() - t0 > 2000000000ull) {
+      if (global_ns() - t0 > limit_ns) {
         ok = 0;
         report(dev_err, KVQ_DEV_ERR_TIMEOUT);
         break;
@@ -609,6 +611,15 @@ __global__ void __launch_bounds__(kDecodeThreads, KV == kI4 && !TAIL ? kMaxCtasP
   // (3) combine
   for (int64_t bh = gwarp; bh < static_cast<int64_t>(s.d.batch) * s.d.q_heads; bh += nwarps)
     combine_row<QBF>(s.d, bh, lane);
+}
+
+// Self-test of the step's barrier: the grid's CTAs meet at one barrier that
+// waits for one CTA more than the grid has, with a limit of limit_ns, so the
+// wait runs out, reports KVQ_DEV_ERR_TIMEOUT and every CTA returns.
+__global__ void __launch_bounds__(kDecodeThreads) barrier_selftest_kernel(unsigned int* ctr,
+                                                                         int32_t* dev_err,
+                                                                         uint64_t limit_ns) {
+  grid_sync(ctr, gridDim.x + 1, dev_err, limit_ns);
 }
 
 template <int KV, bool QBF, bool TAIL>
@@ -781,6 +792,20 @@ cudaError_t launch_combine(const DecodeArgs& a, int q_dtype, cudaStream_t s) {
 cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid,
                         cudaStream_t s) {
   return with_kinds(kv_dtype, q_dtype, a.d.tail_ctr != nullptr, LaunchStep{a, grid, s});
+}
+
+cudaError_t launch_barrier_selftest(unsigned int* ctr, int32_t* dev_err, int grid,
+                                    uint64_t limit_ns, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;  // as the step: every CTA resident
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, barrier_selftest_kernel, ctr, dev_err, limit_ns);
 }
 
 int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail) {

@@ -13,11 +13,13 @@
 // the instructions spent per unit, not DRAM, set the pace; everything below
 // is arranged to spend few.
 //
-// Staging. Every warp keeps a ring of kDepth stages. Lane 0 stages a unit
-// with two TMA tensor copies (the 16 K and the 16 V rows of one kv head, the
-// pool's 64- or 128-byte swizzle) and two 64-byte bulk copies (their scale /
-// zero pairs), completing on the stage's mbarrier, and leaves the unit's
-// position (kv head, request, block) in the stage for the compute side.
+// Staging. Every warp keeps a ring of kDepth stages. All 32 lanes stage a
+// unit with 16-byte cp.async copies (the 16 K and the 16 V rows of one kv
+// head, each row's chunks XOR-swizzled so that the fragment reads hit
+// distinct banks, and the 64-byte scale/zero runs), and lane 0 leaves the
+// unit's position (kv head, request, block) in the stage for the compute
+// side. A tensor copy issued by one lane would move only 1-2 KB here, and
+// measured costlier per unit: its operands must first be made warp-uniform.
 // Physical block ids and positions come 32 units at a time: lane i of the
 // warp locates unit k0 + i of its range (binary search over the per-request
 // block offsets in shared memory) and loads its block id, one window ahead of
@@ -54,9 +56,6 @@
 // same softmax: the maximum only bounds the exponents.
 #include <cuda_runtime.h>
 
-#include <type_traits>
-#include <utility>
-
 #include "kvq_decode_common.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -74,8 +73,8 @@ constexpr float kSlack = 8.f;             // the running maximum may lag the sco
 constexpr float kSlackMaxScale = 240.f;   // ... while V scales stay below this (2^8 S_v < 2^16)
 
 // Per-warp ring of stages: [K tiles][V tiles][scale/zero runs][unit
-// positions][mbarriers], 1024-byte aligned (the tiles take the pool's TMA
-// swizzle, whose pattern repeats every 512 / 1024 bytes).
+// positions], 1024-byte aligned (the swizzle pattern repeats every 512 /
+// 1024 bytes).
 template <int KV>
 struct GqaStage {
   static constexpr int kRow = KvTraits<KV>::kRowBytes;  // 64 (INT4) or 128 (INT8)
@@ -84,11 +83,11 @@ struct GqaStage {
   static constexpr int kVOff = kDepth * kTile;
   static constexpr int kSzOff = 2 * kDepth * kTile;
   static constexpr int kInfoOff = kSzOff + kDepth * 128;
-  static constexpr int kBarOff = kInfoOff + kDepth * 8;
-  static constexpr int kWarpBytes = (kBarOff + kDepth * 8 + 1023) / 1024 * 1024;
-  static constexpr uint32_t kTxBytes = 2 * kTile + 128;  // bytes one stage receives
-  // chunk c of row r sits at chunk c ^ swz(r): the TMA 128-byte swizzle for
-  // 128-byte rows, the 64-byte swizzle for 64-byte rows
+  static constexpr int kWarpBytes = (kInfoOff + kDepth * 8 + 1023) / 1024 * 1024;
+  static constexpr int kChunks = kRow / 16;                // 16-byte chunks per row
+  static constexpr int kCopies = kBlock * kChunks / 32;    // per lane per tile
+  // chunk c of row r sits at chunk c ^ swz(r): the 128-byte pattern (r mod 8)
+  // for 128-byte rows, the 64-byte pattern ((r / 2) mod 4) for 64-byte rows
   __host__ __device__ static constexpr int at(int r, int c) {
     return r * kRow + (c ^ (kRow == 64 ? ((r >> 1) & 3) : (r & 7))) * 16;
   }
@@ -114,16 +113,6 @@ __device__ __forceinline__ void sts64(uint32_t addr, uint32_t x, uint32_t y) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
 }
 
-// f(integral_constant<int, 0>) ... f(integral_constant<int, N - 1>), in order
-template <class F, int... I>
-__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
-  (f(std::integral_constant<int, I>{}), ...);
-}
-template <int N, class F>
-__device__ __forceinline__ void static_for(F&& f) {
-  static_for_impl(f, std::make_integer_sequence<int, N>{});
-}
-
 template <int KV, bool TAIL>
 __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsmem,
                                          int32_t* warp_sum, int cta, int ncta) {
@@ -144,15 +133,20 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
   const int32_t* lown = sp.cum + a.batch + 1;  // tokens of request b's own blocks
   const int tb = sp.tb;
   const int64_t gw = static_cast<int64_t>(cta) * kWarps + warp;
+
   const uint32_t region0 =
       (static_cast<uint32_t>(__cvta_generic_to_shared(sp.stages)) + 1023u) & ~1023u;
   const uint32_t wr = region0 + static_cast<uint32_t>(warp * S::kWarpBytes);
-  if (lane == 0) {
+  // this lane's copies: chunk n = lane + 32 i of a tile (row n / kChunks)
+  uint32_t csrc[S::kCopies], cdst[S::kCopies];
 #pragma unroll
-    for (int i = 0; i < D; ++i) mbar_init(wr + S::kBarOff + 8 * i);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  for (int i = 0; i < S::kCopies; ++i) {
+    const int n = lane + 32 * i, r = n / S::kChunks, c = n % S::kChunks;
+    csrc[i] = static_cast<uint32_t>(r * a.kv_heads * S::kRow + c * 16);
+    cdst[i] = S::at(r, c);
   }
-  __syncwarp();
+  // lanes 0-3 copy the 64 bytes of K scale/zero pairs, lanes 4-7 those of V
+  const uint32_t* const sz_src = (lane < 4 ? a.k_sz : a.v_sz) + 4 * (lane & 3);
 
   // fragment offsets of this lane in a stage's K and V tiles
   uint32_t kro[2][S::kRow / 64];  // rows g, g + 8: dims [32t, 32t + 32)
@@ -170,7 +164,6 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
   }
   const float kq = a.sm_scale_log2;
 
-  uint32_t phase = 0;  // parity to wait for, per stage, across ranges
   auto run_range = [&](const int64_t x0, const int n, const int64_t rid) -> bool {
     // ---- issue side: windows of 32 units located lane-parallel ---------------------
     // lane i of window w holds unit 32 w + i of the range: its block id and its
@@ -199,12 +192,8 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
     int32_t wblk, nblk_;
     locate_window(0, wphys, wkey, wblk);
     locate_window(1, nphys, nkey, nblk_);
-    const uint32_t nb32 = static_cast<uint32_t>(a.num_blocks);  // block ids are TMA coordinates
-    uint32_t ok_mask = 0;  // stages holding a valid unit in flight
-    // stage ST receives unit kq of the range (nothing past its end)
-    auto issue = [&](auto st_c, const int kq) {
-      constexpr int ST = decltype(st_c)::value;
-      if (kq >= n) return;
+    const uint32_t nb32 = static_cast<uint32_t>(a.num_blocks);  // valid ids are below this
+    auto issue_unit = [&](const int ST, const int kq) {
       const int kk = kq & 31;
       if (kk == 0 && kq > 0) {  // next window; locate the one after it
         wphys = nphys; wkey = nkey; wblk = nblk_;
@@ -214,26 +203,34 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
       const uint32_t key = __shfl_sync(kFull, wkey, kk);
       const int32_t blk = __shfl_sync(kFull, wblk, kk);
       const bool ok = static_cast<uint32_t>(phys) < nb32;
-      ok_mask = ok ? (ok_mask | (1u << ST)) : (ok_mask & ~(1u << ST));
       if (lane == 0) {
-        sts64(wr + S::kInfoOff + 8 * ST, key, static_cast<uint32_t>(blk));
-        if (ok) {
-          const int h = static_cast<int>(key >> 16);
-          const uint32_t bar = wr + S::kBarOff + 8 * ST;
-          const uint32_t sz = wr + S::kSzOff + 128 * ST;
-          const int64_t szi = (static_cast<int64_t>(phys) * a.kv_heads + h) * kBlock;
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arm(bar, S::kTxBytes);
-          tma_tile_4d(wr + ST * S::kTile, &a.k_map, 0, h, 0, phys, bar);
-          tma_tile_4d(wr + S::kVOff + ST * S::kTile, &a.v_map, 0, h, 0, phys, bar);
-          bulk_copy(sz, a.k_sz + szi, 64, bar);
-          bulk_copy(sz + 64, a.v_sz + szi, 64, bar);
-        } else {
-          report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+        sts64(wr + S::kInfoOff + 8 * ST, key, ok ? static_cast<uint32_t>(blk) : 0xFFFFFFFFu);
+        if (!ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+      }
+      if (ok) {
+        // row r of the (block, head) tile: ((phys * 16 + r) * kv_heads + h) * kRow
+        const int h = static_cast<int>(key >> 16);
+        const int64_t ph = static_cast<int64_t>(phys) * a.kv_heads + h;
+        const int64_t base = (static_cast<int64_t>(phys) * kBlock * a.kv_heads + h) * S::kRow;
+        const uint8_t* kb = a.k + base;
+        const uint8_t* vb = a.v + base;
+        const uint32_t kd = wr + ST * S::kTile, vd = wr + S::kVOff + ST * S::kTile;
+#pragma unroll
+        for (int i = 0; i < S::kCopies; ++i) {
+          cp_async16(kd + cdst[i], kb + csrc[i]);
+          cp_async16(vd + cdst[i], vb + csrc[i]);
         }
+        if (lane < 8) cp_async16(wr + S::kSzOff + 128 * ST + 16 * lane, sz_src + ph * kBlock);
       }
     };
-    static_for<D - 1>([&](auto st_c) { issue(st_c, decltype(st_c)::value); });
+    // stage ST receives unit kq of the range (nothing past its end); every call
+    // commits one cp.async group, so that the wait below always counts kDepth - 1
+    auto issue = [&](const int ST, const int kq) {
+      if (kq < n) issue_unit(ST, kq);
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue(k, k);
 
     // ---- per-request state -----------------------------------------------------------
     uint32_t seg_key = 0xFFFFFFFFu;
@@ -263,69 +260,58 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         for (int c = 0; c < 4; ++c) o[i][c] += __shfl_xor_sync(kFull, o[i][c], 2);
       R[0] += __shfl_xor_sync(kFull, R[0], 2);
       R[1] += __shfl_xor_sync(kFull, R[1], 2);
-      if (tsel != 0) return;  // lanes t = 2, 3 now hold copies
       const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
       const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
+      if (tsel == 0) {  // lanes t = 2, 3 hold copies
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int hh = 2 * t + u;
-        const float l = u ? l1 : l0, m = u ? m1 : m0;
-        const float corr = (u ? z1 : z0) - kMid * R[u];
-        float acc[16];
+        for (int u = 0; u < 2; ++u) {
+          const int hh = 2 * t + u;
+          const float l = u ? l1 : l0, m = u ? m1 : m0;
+          const float corr = (u ? z1 : z0) - kMid * R[u];
+          float acc[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          // INT4 output rows fed by a nibble at bits 4-7 (odd i) carry 16 c
-          const float sc = (KV == kI4 && (i & 1)) ? kTwo24 / 16.f : kTwo24;
-          acc[i] = fmaf(o[i][u], sc, corr);
-          acc[8 + i] = fmaf(o[i][2 + u], sc, corr);
-        }
-        if (contained) {
-          float mm = m, ll = l;
-          if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
-          const float inv = ll > 0.f ? 1.f / ll : 0.f;
-          uint32_t w[8];
+          for (int i = 0; i < 8; ++i) {
+            // INT4 output rows fed by a nibble at bits 4-7 (odd i) carry 16 c
+            const float sc = (KV == kI4 && (i & 1)) ? kTwo24 / 16.f : kTwo24;
+            acc[i] = fmaf(o[i][u], sc, corr);
+            acc[8 + i] = fmaf(o[i][2 + u], sc, corr);
+          }
+          if (contained) {
+            float mm = m, ll = l;
+            if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
+            const float inv = ll > 0.f ? 1.f / ll : 0.f;
+            uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = pack2<false>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                                (row0 + hh) * kHeadDim + 16 * g);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
-          const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
-          float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
-          float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack2<false>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                                  (row0 + hh) * kHeadDim + 16 * g);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last
+            float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
+            float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            ov[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-          if (g == 0) {
-            rec[kHeadDim] = m;
-            rec[kHeadDim + 1] = l;
+            for (int i = 0; i < 4; ++i)
+              ov[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            if (g == 0) {
+              rec[kHeadDim] = m;
+              rec[kHeadDim + 1] = l;
+            }
           }
         }
       }
     };
 
-    bool failed = false;
-    // unit k of the range in stage ST; false when the range is done (or failed)
-    auto step = [&](auto st_c, const int k) -> bool {
-      constexpr int ST = decltype(st_c)::value;
-      if (k >= n) return false;
-      issue(std::integral_constant<int, (ST + D - 1) % D>{}, k + D - 1);  // the stage k - 1 used
-      const bool blk_ok = (ok_mask >> ST) & 1u;
-      if (blk_ok) {
-        if (!mbar_wait(wr + S::kBarOff + 8 * ST, (phase >> ST) & 1u)) {
-          // a copy did not land: report, wait (bounded) for the other copies this
-          // warp started, and stop
-          if (lane == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
-          const uint32_t rest = ok_mask & ~(1u << ST);
-          for (int i = 0; i < D; ++i)
-            if ((rest >> i) & 1u) mbar_wait(wr + S::kBarOff + 8 * i, (phase >> i) & 1u);
-          failed = true;
-          return false;
-        }
-        phase ^= 1u << ST;
-      }
-      const uint2 info = lds64u(wr + S::kInfoOff + 8 * ST);  // (kv head << 16 | request, block)
+    // unit k of the range in stage ST
+    auto step = [&](const int ST, const int k) {
+      issue(ST == 0 ? D - 1 : ST - 1, k + D - 1);  // the stage unit k - 1 used
+      cp_async_wait<D - 1>();  // this lane's copies of unit k have landed
+      __syncwarp();            // ... and every other lane's
+      // (kv head << 16 | request, block; all ones for a block id outside the pool)
+      const uint2 info = lds64u(wr + S::kInfoOff + 8 * ST);
+      const bool blk_ok = info.y != 0xFFFFFFFFu;
       const int j = static_cast<int>(info.y);
 
       if (info.x != seg_key) {
@@ -380,7 +366,7 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
       }
 
       if (blk_ok) {
-        constexpr uint32_t kKt = ST * S::kTile, kVt = S::kVOff + ST * S::kTile;
+        const uint32_t kKt = ST * S::kTile, kVt = S::kVOff + ST * S::kTile;
         const uint32_t szp = wr + S::kSzOff + 128 * ST + 4 * tau;
         const uint32_t ksz = lds32(szp), vsz = lds32(szp + 64);
         // ---- S^T = K Q^T: class-A k-steps into sa, class-B into sb -------------------
@@ -523,17 +509,10 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         }
       }
       __syncwarp();  // all lanes are done with this stage before it is refilled
-      return true;
     };
 
-    for (int kb = 0; kb < n; kb += D) {
-      bool more = true;
-      static_for<D>([&](auto st_c) {
-        if (more) more = step(st_c, kb + decltype(st_c)::value);
-      });
-      if (!more) break;
-    }
-    if (failed) return false;
+    for (int k = 0, st = 0; k < n; ++k, st = st == D - 1 ? 0 : st + 1) step(st, k);
+    cp_async_wait<0>();
     if (seg_key != 0xFFFFFFFFu) flush();
     return true;
   };

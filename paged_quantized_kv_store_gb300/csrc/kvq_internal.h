@@ -151,6 +151,9 @@ cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
 cudaError_t launch_step(const StepArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                         cudaStream_t s);
 int step_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail);
+// the step's grid barrier made to wait for one CTA more than the grid has
+cudaError_t launch_barrier_selftest(unsigned int* ctr, int32_t* dev_err, int grid,
+                                    uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_extend(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                           cudaStream_t s);
 int extend_ctas_per_sm(int kv_dtype, int q_dtype, int batch);

@@ -83,14 +83,18 @@ def out_to_f64(out):
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL):
+    """Element-wise: |got - ref| <= atol or <= rtol |ref|. Returns the largest
+    absolute and relative errors (both are reported on failure)."""
     err = np.abs(got - ref)
+    rel = err / np.maximum(np.abs(ref), 1e-30)
     ok = (err <= atol) | (err <= rtol * np.abs(ref))
     if not ok.all():
         idx = np.unravel_index(np.argmax(np.where(ok, 0, err)), err.shape)
         raise AssertionError(
             f"{(~ok).sum()} of {ok.size} elements out of tolerance; worst at {idx}: "
-            f"got {got[idx]!r} ref {ref[idx]!r}; max abs err {err.max():.3e}")
-    return float(err.max()), float((err / np.maximum(np.abs(ref), 1e-30)).max())
+            f"got {got[idx]!r} ref {ref[idx]!r}; max abs err {err.max():.3e}, "
+            f"max rel err {rel.max():.3e}")
+    return float(err.max()), float(rel.max())
 
 
 def oracle_request(wl, b):

@@ -56,6 +56,27 @@ SMALL = {
 }
 
 
+def test_step_barrier_timeout_is_reported_and_context_survives(gpu):
+    # the step's grid barrier waiting for one CTA more than the grid has: the
+    # bounded wait runs out after 5 ms, sets the timeout bit and every CTA
+    # returns (no fault, no hang)
+    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu.kvq_selftest_step_barrier(counter, dev_err, grid_ctas=0, limit_us=5000)
+    bits = gpu.kvq_check_error(dev_err)
+    assert bits == 64, bits  # KVQ_DEV_ERR_TIMEOUT alone
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert int(counter.item()) == n_sm  # every CTA arrived, none was waited for in vain
+    # the context is still usable: a fused step right after matches the oracle
+    wl = SMALL["cfg3"]()
+    pool = fill_pool(wl)
+    out, bt, err = fused_step(gpu, wl, pool)
+    assert gpu.kvq_check_error(err) == 0
+    opool, oout = oracle.run_workload(wl)
+    _compare_pools(pool, opool)
+    assert_close(out_to_f64(out), oout)
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_workloads_match_oracle_and_separate_calls(gpu, name):
     wl = SMALL[name]()
