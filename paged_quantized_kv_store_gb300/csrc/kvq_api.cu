@@ -104,6 +104,33 @@ bool encode_pool_map(CUtensorMap* map, void* base, int64_t num_blocks, int kv_he
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same pool as a 4-D view ordered [block][kv head][token][row] (token
+// and head strides swapped), one box = the 16 rows of heads kv heads of one
+// block, laid out head after head, each tile with the swizzle above: the
+// grouped-query decode kernel stages a block for all heads of its CTA with
+// one copy.
+bool encode_pool_map_heads(CUtensorMap* map, void* base, int64_t num_blocks, int kv_heads,
+                           int row_bytes, int heads) {
+  std::memset(map, 0, sizeof(*map));
+  if (num_blocks <= 0) return true;
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), 16,
+                              static_cast<cuuint64_t>(kv_heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kv_heads) * row_bytes,
+                                 static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(16) * kv_heads * row_bytes};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(row_bytes), 16,
+                             static_cast<cuuint32_t>(heads), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Shared-prefix groups as the caller describes them.
 struct PrefixDesc {
   const int32_t* offsets;
@@ -186,9 +213,20 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   std::memset(&a, 0, sizeof(a));
   // the grouped-query kernel (INT8 / INT4 pools, fp16 queries, 4 q heads per
   // kv head) serves the plain decode; the fused step keeps the general kernel
-  const bool gqa = pre == nullptr &&
-                   kvq::decode_gqa_supported(pool->kv_dtype, q_dtype, q_heads / pool->kv_heads);
-  if (pool->kv_dtype == KVQ_INT8) {  // the general INT8 kernels stage their tiles by TMA
+  const bool gqa = pre == nullptr && kvq::decode_gqa_supported(pool->kv_dtype, q_dtype,
+                                                                q_heads / pool->kv_heads,
+                                                                pool->kv_heads);
+  const int cta_heads = gqa ? kvq::decode_gqa_cta_heads(pool->kv_heads) : 0;
+  if (gqa) {  // one copy stages a block for the CTA's kv heads
+    const int row = pool->kv_dtype == KVQ_INT8 ? kHeadDim : kHeadDim / 2;
+    if (!encode_pool_map_heads(&a.kh_map, pool->k, pool->num_blocks, pool->kv_heads, row,
+                               cta_heads) ||
+        !encode_pool_map_heads(&a.vh_map, pool->v, pool->num_blocks, pool->kv_heads, row,
+                               cta_heads))
+      return KVQ_ERR_CUDA;
+  }
+  // the general INT8 kernels (decode, shared prefix, step) stage one tile per copy
+  if (pool->kv_dtype == KVQ_INT8) {
     if (!encode_pool_map(&a.k_map, pool->k, pool->num_blocks, pool->kv_heads, kHeadDim) ||
         !encode_pool_map(&a.v_map, pool->v, pool->num_blocks, pool->kv_heads, kHeadDim))
       return KVQ_ERR_CUDA;
@@ -223,11 +261,31 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
       static_cast<int64_t>((decode_bytes - decode_records_offset(batch)) / rec),
       static_cast<int64_t>(kvq::kRangesPerWarp) * plan.warps);
   // a tail needs an automatic split (an explicit count keeps every request to
-  // num_splits + 1 pieces) and sizes whose per-warp share can reach
+  // num_splits + 1 pieces) and sizes whose per-range share can reach
   // kTailMinShare blocks
-  const int64_t max_total = static_cast<int64_t>(batch) * pool->kv_heads * plan.head_groups *
-                            (a.len_cap / kBlock);
-  const bool tail = num_splits == 0 && max_total >= int64_t{kvq::kTailMinShare} * plan.warps;
+  int64_t max_total = static_cast<int64_t>(batch) * pool->kv_heads * plan.head_groups *
+                      (a.len_cap / kBlock);
+  int64_t ranges = plan.warps;
+  int gqa_grid = 0;
+  if (gqa) {
+    // a CTA per group of cta_heads kv heads, one range each; at most
+    // kMaxCtasPerSm * 4 warps per SM, as the workspace's records assume
+    const int occ = kvq::decode_gqa_ctas_per_sm(pool->kv_dtype, batch, cta_heads, false);
+    const int per_sm =
+        std::min(occ, kvq::kMaxCtasPerSm * (kvq::kDecodeThreads / 32) / cta_heads);
+    if (per_sm <= 0) return KVQ_ERR_CUDA;
+    gqa_grid = plan.num_sms * per_sm;
+    a.cta_heads = cta_heads;
+    a.hpg = cta_heads * a.group;
+    a.head_groups = 1;
+    const size_t rec_g = static_cast<size_t>(2) * a.hpg * kvq::kPartStride * sizeof(float);
+    a.max_ranges = std::min<int64_t>(
+        static_cast<int64_t>((decode_bytes - decode_records_offset(batch)) / rec_g),
+        static_cast<int64_t>(kvq::kRangesPerWarp) * gqa_grid);
+    max_total = static_cast<int64_t>(batch) * (pool->kv_heads / cta_heads) * (a.len_cap / kBlock);
+    ranges = gqa_grid;
+  }
+  const bool tail = num_splits == 0 && max_total >= int64_t{kvq::kTailMinShare} * ranges;
   a.tail_ctr = tail ? static_cast<unsigned int*>(workspace) : nullptr;
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -270,15 +328,17 @@ kvq_status decode_impl(const kvq_pool* pool, const void* q, int32_t q_dtype, voi
   }
   // persistent grid: as many CTAs as fit on the device at once (the
   // workspace has partial slots for kMaxCtasPerSm per SM)
-  const int per_sm = std::min(
-      gqa ? kvq::decode_gqa_ctas_per_sm(pool->kv_dtype, batch, tail)
-          : kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
-      kvq::kMaxCtasPerSm);
-  if (per_sm <= 0) return KVQ_ERR_CUDA;
-  const int grid = plan.num_sms * per_sm;
-  const cudaError_t le = gqa ? kvq::launch_decode_gqa(a, pool->kv_dtype, grid, s)
-                             : kvq::launch_decode(a, pool->kv_dtype, q_dtype, grid, s);
-  if (le != cudaSuccess) return KVQ_ERR_CUDA;
+  if (gqa) {
+    if (kvq::launch_decode_gqa(a, pool->kv_dtype, gqa_grid, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  } else {
+    const int per_sm = std::min(kvq::decode_ctas_per_sm(pool->kv_dtype, q_dtype, batch, tail),
+                                kvq::kMaxCtasPerSm);
+    if (per_sm <= 0) return KVQ_ERR_CUDA;
+    if (kvq::launch_decode(a, pool->kv_dtype, q_dtype, plan.num_sms * per_sm, s) !=
+        cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
   if (kvq::launch_combine(a, q_dtype, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

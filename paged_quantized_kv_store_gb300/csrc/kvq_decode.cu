@@ -515,9 +515,16 @@ __device__ __forceinline__ void combine_row(const DecodeArgs& a, int64_t bh, int
   const int skip = a.skip != nullptr ? a.skip[b] : 0;
   const int npc = skip > 0 ? (skip + a.pchunk - 1) / a.pchunk : 0;
   if (nblk == 0 && npc == 0) return;  // zeroed by the decode kernel
-  const int h = hq / a.group, within = hq - h * a.group;
-  const int hgi = h * a.head_groups + within / kHeadsPerGroup;
-  const int hh = within % kHeadsPerGroup;
+  int hgi, hh;  // the row's q-head group in the stream, and its record row in the group
+  if (a.cta_heads > 0) {  // grouped-query kernel: groups of cta_heads kv heads
+    const int qpg = a.cta_heads * a.group;
+    hgi = hq / qpg;
+    hh = hq - hgi * qpg;
+  } else {
+    const int h = hq / a.group, within = hq - h * a.group;
+    hgi = h * a.head_groups + within / kHeadsPerGroup;
+    hh = within % kHeadsPerGroup;
+  }
   const int64_t seg_start = static_cast<int64_t>(hgi) * tb + cum[b];
   int64_t r_first = 0, nd = 0;
   if (nblk > 0) {

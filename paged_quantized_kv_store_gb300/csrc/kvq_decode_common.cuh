@@ -114,7 +114,7 @@ struct StreamPlan {
   int tb;                  // blocks of one q-head group over all requests
   int groups;              // q-head groups (kv heads x head groups)
   int64_t total;           // blocks in the stream
-  int64_t nwarps;          // warps of the grid
+  int64_t nwarps;          // ranges of the static cut (warps, or CTAs, of the grid)
   int64_t static_end;      // end of the static ranges (the tail follows)
   RangeMap rm;
 };
@@ -126,15 +126,19 @@ struct StreamPlan {
 // cut per q-head group where that pays), and, by CTA 0, the header the
 // combine kernel reads and the all-zero rows of empty requests (a request
 // whose only blocks are shared ones is written by the combine kernel).
+// The CTA has blockDim.x threads (at most 8 warps: warp_sum holds one int per
+// warp) and owns ranges_per_cta ranges of the stream (one per warp, or one).
 template <bool QBF, bool TAIL>
 __device__ __forceinline__ StreamPlan plan_stream(const DecodeArgs& a, unsigned char* dsmem,
                                                   int32_t* warp_sum, int cta, int ncta,
-                                                  bool lockstep, bool own_lens = false) {
+                                                  bool lockstep, bool own_lens = false,
+                                                  int ranges_per_cta = kWarps) {
   int32_t* cum = reinterpret_cast<int32_t*>(dsmem);
   int32_t* lown = cum + a.batch + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nt = blockDim.x;
   {
-    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
+    const int per = (a.batch + nt - 1) / nt;
     const int b0 = min(tid * per, a.batch), b1 = min(b0 + per, a.batch);
     int sum = 0;
     for (int b = b0; b < b1; ++b) {
@@ -157,16 +161,16 @@ __device__ __forceinline__ StreamPlan plan_stream(const DecodeArgs& a, unsigned 
       run += own_blocks(a, b);
       if (own_lens) lown[b] = clamped_len(a, b) - kBlock * skip_of(a, b);
     }
-    if (tid == kDecodeThreads - 1) cum[a.batch] = base + incl;
+    if (tid == nt - 1) cum[a.batch] = base + incl;
     __syncthreads();
   }
   StreamPlan sp;
   sp.cum = cum;
   sp.stages = dsmem + align128(((own_lens ? 2 : 1) * a.batch + 1) * sizeof(int32_t));
   sp.tb = cum[a.batch];
-  sp.groups = a.kv_heads * a.head_groups;
+  sp.groups = a.cta_heads > 0 ? a.kv_heads / a.cta_heads : a.kv_heads * a.head_groups;
   sp.total = static_cast<int64_t>(sp.tb) * sp.groups;
-  sp.nwarps = static_cast<int64_t>(ncta) * kWarps;
+  sp.nwarps = static_cast<int64_t>(ncta) * ranges_per_cta;  // ranges of the static cut
   const int64_t even_share = (sp.total + sp.nwarps - 1) / sp.nwarps;
   const int P = static_cast<int>(even_share > a.min_blocks_per_warp ? even_share
                                                                     : a.min_blocks_per_warp);
@@ -183,10 +187,10 @@ __device__ __forceinline__ StreamPlan plan_stream(const DecodeArgs& a, unsigned 
       a.hdr[3] = static_cast<int32_t>(sp.nwarps);
       a.hdr[4] = sp.rm.k;
     }
-    for (int b = tid; b <= a.batch; b += kDecodeThreads) a.hdr[kHdrCum + b] = cum[b];
+    for (int b = tid; b <= a.batch; b += nt) a.hdr[kHdrCum + b] = cum[b];
     for (int b = 0; b < a.batch; ++b) {
       if (cum[b + 1] != cum[b] || skip_of(a, b) > 0) continue;
-      for (int e = tid; e < a.q_heads * kHeadDim; e += kDecodeThreads)
+      for (int e = tid; e < a.q_heads * kHeadDim; e += nt)
         store_out<QBF>(a.out, static_cast<int64_t>(b) * a.q_heads * kHeadDim + e, 0.f);
     }
   }

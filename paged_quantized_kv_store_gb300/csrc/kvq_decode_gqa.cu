@@ -6,24 +6,31 @@
 // §3.2 item 3 and §4.2: generation attention reads the paged KV through
 // indirect block pointers in its own hand-written kernel.
 //
-// The work split is the general decode kernel's (kvq_decode_common.cuh: one
-// stream of (kv head, request, block) units, a persistent grid, equal ranges
-// per warp, partial records merged by the combine kernel). With 4 q heads per
-// kv head a unit carries 4-8 times fewer bytes per query than with one, and
-// the instructions spent per unit, not DRAM, set the pace; everything below
-// is arranged to spend few.
+// With 4 q heads per kv head a (block, kv head) unit carries 4-8 times fewer
+// bytes per query than with one, and the instructions spent per unit, not
+// DRAM, set the pace; the kernel is laid out to spend few.
 //
-// Staging. Every warp keeps a ring of kDepth stages. All 32 lanes stage a
-// unit with 16-byte cp.async copies (the 16 K and the 16 V rows of one kv
-// head, each row's chunks XOR-swizzled so that the fragment reads hit
-// distinct banks, and the 64-byte scale/zero runs), and lane 0 leaves the
-// unit's position (kv head, request, block) in the stage for the compute
-// side. A tensor copy issued by one lane would move only 1-2 KB here, and
-// measured costlier per unit: its operands must first be made warp-uniform.
-// Physical block ids and positions come 32 units at a time: lane i of the
-// warp locates unit k0 + i of its range (binary search over the per-request
-// block offsets in shared memory) and loads its block id, one window ahead of
-// the unit being issued.
+// Work split. A CTA has one warp per kv head of a group of W kv heads (W = the
+// pool's kv heads, or 8 of them). The work is one stream of (head group,
+// request, block) units, and a persistent grid gives every CTA one contiguous
+// range of it (kvq_decode_common.cuh: equal static ranges, tail chunks from a
+// counter for long shares); partial records of requests a range does not
+// hold whole are merged by the combine kernel. Every warp of a CTA attends the
+// same blocks, each for its own kv head.
+//
+// Staging. One thread (warp 0, lane 0) stages a block for all W kv heads with
+// two TMA tensor copies (K and V: a 4-D view of the pool ordered [block][kv
+// head][token][row], so the W tiles of 16 rows land one after the other, each
+// with the pool's 64- or 128-byte swizzle) and two bulk copies of the W
+// heads' scale/zero runs, into a ring of kDepth stages. A stage's full
+// mbarrier completes when its bytes have landed; its empty mbarrier when all W
+// warps have read it, after which the next block may be staged there. The
+// stage also carries the block's position (head group, request, block) for
+// the consumers. Block ids come from a window of 32 located lane-parallel by
+// warp 0 (binary search over the per-request block offsets in shared memory),
+// one window ahead. All waits are bounded (2 s): on expiry the thread reports
+// KVQ_DEV_ERR_TIMEOUT, the CTA stops staging and waits (bounded again) for
+// its copies in flight before it returns.
 //
 // Codes as fp16 subnormals. A code c written into the low mantissa bits of an
 // fp16 whose exponent field is zero is the exact value c * 2^-24 (tensor
@@ -45,8 +52,9 @@
 // mma layout holds tokens g and g + 8 for columns 2t, 2t + 1: lanes t = 0, 1
 // keep token g and lanes t = 2, 3 keep token g + 8, each for heads
 // 2 (t mod 2) and 2 (t mod 2) + 1, so every lane runs the softmax of two
-// scores instead of four. One shuffle brings token g + 8's weights back to
-// the lanes that feed them to the P.V product, whose columns 4-7 are zero.
+// scores instead of four. In the P.V product columns 0-3 take tokens 0-7 and
+// columns 4-7 tokens 8-15 of the same heads, so no weight changes lanes; the
+// two halves are added when a request's rows are written.
 //
 // Running maximum. Scores live in the exp2 domain. The running maximum m of
 // a q head is raised (and the state rescaled) only when a score exceeds it
@@ -65,40 +73,48 @@ namespace kvq {
 namespace {
 
 constexpr int kGqaGroup = 4;              // q heads per kv head served by this kernel
+constexpr int kMaxCtaHeads = 8;           // warps (kv heads) per CTA
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibble at bits 0-3 of each half: c
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibble at bits 4-7 of each half: 16 c
 constexpr float kTwo24 = 16777216.f;      // 2^24: one code unit of the subnormal encoding
 constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 pair (1, 1)
 constexpr float kSlack = 8.f;             // the running maximum may lag the scores by this
 constexpr float kSlackMaxScale = 240.f;   // ... while V scales stay below this (2^8 S_v < 2^16)
+constexpr uint64_t kWaitNs = 2000000000ull;
 
-// Per-warp ring of stages: [K tiles][V tiles][scale/zero runs][unit
-// positions], 1024-byte aligned (the swizzle pattern repeats every 512 /
-// 1024 bytes).
+// A stage holds one block for W kv heads: [K tiles W][V tiles W][K scale/zero
+// runs W][V scale/zero runs W][position]; stages are 1024-byte aligned (the
+// swizzle pattern of a tile repeats every 512 / 1024 bytes, and every tile
+// starts on such a boundary).
 template <int KV>
-struct GqaStage {
+struct CtaStage {
   static constexpr int kRow = KvTraits<KV>::kRowBytes;  // 64 (INT4) or 128 (INT8)
-  static constexpr int kTile = kBlock * kRow;
-  static constexpr int kDepth = 4;
-  static constexpr int kVOff = kDepth * kTile;
-  static constexpr int kSzOff = 2 * kDepth * kTile;
-  static constexpr int kInfoOff = kSzOff + kDepth * 128;
-  static constexpr int kWarpBytes = (kInfoOff + kDepth * 8 + 1023) / 1024 * 1024;
-  static constexpr int kChunks = kRow / 16;                // 16-byte chunks per row
-  static constexpr int kCopies = kBlock * kChunks / 32;    // per lane per tile
-  // chunk c of row r sits at chunk c ^ swz(r): the 128-byte pattern (r mod 8)
-  // for 128-byte rows, the 64-byte pattern ((r / 2) mod 4) for 64-byte rows
+  static constexpr int kTile = kBlock * kRow;           // one (block, kv head) tile
+  static constexpr int kDepth = KV == kI4 ? 4 : 3;
+  __host__ __device__ static constexpr int v_off(int w) { return w * kTile; }
+  __host__ __device__ static constexpr int sz_off(int w) { return 2 * w * kTile; }
+  __host__ __device__ static constexpr int info_off(int w) { return 2 * w * kTile + 2 * w * 64; }
+  __host__ __device__ static constexpr int bytes(int w) {
+    return (info_off(w) + 16 + 1023) / 1024 * 1024;
+  }
+  __host__ __device__ static constexpr uint32_t tx_bytes(int w) {
+    return static_cast<uint32_t>(2 * w * kTile + 2 * w * 64);
+  }
+  // chunk c of row r sits at chunk c ^ swz(r): the TMA 128-byte swizzle for
+  // 128-byte rows, the 64-byte swizzle for 64-byte rows
   __host__ __device__ static constexpr int at(int r, int c) {
     return r * kRow + (c ^ (kRow == 64 ? ((r >> 1) & 3) : (r & 7))) * 16;
   }
 };
 
 // Dynamic shared memory: [blocks before request b, batch + 1][own tokens of
-// request b, batch][slack to 1024 bytes][the warps' stage rings].
+// request b, batch][slack to 1024 bytes][kDepth stages][full and empty
+// mbarriers, kDepth each].
 template <int KV>
-__host__ __device__ constexpr size_t gqa_smem_bytes(int batch) {
+__host__ __device__ constexpr size_t gqa_smem_bytes(int batch, int w) {
   return align128((2 * batch + 1) * sizeof(int32_t)) + 1024 +
-         static_cast<size_t>(kWarps) * GqaStage<KV>::kWarpBytes;
+         static_cast<size_t>(CtaStage<KV>::kDepth) * CtaStage<KV>::bytes(w) +
+         2 * CtaStage<KV>::kDepth * 8;
 }
 
 // Two codes as the fp16 subnormal pair selected by sel from word w's bytes
@@ -107,67 +123,92 @@ __device__ __forceinline__ uint32_t bytes_sub(uint32_t w, uint32_t sel) {
   return prmt(w, 0u, sel);
 }
 
-__device__ __forceinline__ uint2 lds64u(uint32_t addr) { return lds64(addr); }
-
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t x, uint32_t y) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
 }
 
+__device__ __forceinline__ void mbar_init_n(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Waits for the phase of parity `parity`; gives up after kWaitNs or as soon as
+// *abort is set by another thread of the CTA (false either way).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort != 0 || global_ns() - t0 > kWaitNs) return false;
+  }
+  return true;
+}
+
 template <int KV, bool TAIL>
 __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsmem,
-                                         int32_t* warp_sum, int cta, int ncta) {
-  using S = GqaStage<KV>;
+                                         int32_t* warp_sum, volatile int* abort_s,
+                                         int32_t* chunk_s, int cta, int ncta) {
+  using S = CtaStage<KV>;
   constexpr int D = S::kDepth;
   constexpr float kMid = KV == kI8 ? 128.f : 8.f;
   constexpr bool kLockstep = KV != kI4;
 
+  const int W = a.cta_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int tsel = t >> 1;       // 0: this lane scores token g, 1: token g + 8
   const int hp = t & 1;          // ... for q heads 2 hp and 2 hp + 1 of the group
   const int tau = g + 8 * tsel;  // that token's row in the block
+  const bool producer = warp == 0;
 
   const StreamPlan sp = plan_stream<false, TAIL>(a, dsmem, warp_sum, cta, ncta, kLockstep,
-                                                 /*own_lens=*/true);
+                                                 /*own_lens=*/true, /*ranges_per_cta=*/1);
   const int32_t* cum = sp.cum;
   const int32_t* lown = sp.cum + a.batch + 1;  // tokens of request b's own blocks
   const int tb = sp.tb;
-  const int64_t gw = static_cast<int64_t>(cta) * kWarps + warp;
-
-  const uint32_t region0 =
+  const uint32_t stage0 =
       (static_cast<uint32_t>(__cvta_generic_to_shared(sp.stages)) + 1023u) & ~1023u;
-  const uint32_t wr = region0 + static_cast<uint32_t>(warp * S::kWarpBytes);
-  // this lane's copies: chunk n = lane + 32 i of a tile (row n / kChunks)
-  uint32_t csrc[S::kCopies], cdst[S::kCopies];
-#pragma unroll
-  for (int i = 0; i < S::kCopies; ++i) {
-    const int n = lane + 32 * i, r = n / S::kChunks, c = n % S::kChunks;
-    csrc[i] = static_cast<uint32_t>(r * a.kv_heads * S::kRow + c * 16);
-    cdst[i] = S::at(r, c);
+  const uint32_t SB = static_cast<uint32_t>(S::bytes(W));
+  const uint32_t full0 = stage0 + D * SB, empty0 = full0 + 8 * D;
+  if (tid == 0) {
+    for (int i = 0; i < D; ++i) {
+      mbar_init_n(full0 + 8 * i, 1);
+      mbar_init_n(empty0 + 8 * i, static_cast<uint32_t>(W));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *abort_s = 0;
   }
-  // lanes 0-3 copy the 64 bytes of K scale/zero pairs, lanes 4-7 those of V
-  const uint32_t* const sz_src = (lane < 4 ? a.k_sz : a.v_sz) + 4 * (lane & 3);
+  __syncthreads();
 
-  // fragment offsets of this lane in a stage's K and V tiles
+  // fragment offsets of this lane in its kv head's K and V tiles
   uint32_t kro[2][S::kRow / 64];  // rows g, g + 8: dims [32t, 32t + 32)
   uint32_t vro[4];                // rows 2t, 2t+1, 2t+8, 2t+9: dims [16g, 16g + 16)
 #pragma unroll
   for (int i = 0; i < S::kRow / 64; ++i) {
-    kro[0][i] = S::at(g, (S::kRow / 64) * t + i);
-    kro[1][i] = S::at(g + 8, (S::kRow / 64) * t + i);
+    kro[0][i] = warp * S::kTile + S::at(g, (S::kRow / 64) * t + i);
+    kro[1][i] = warp * S::kTile + S::at(g + 8, (S::kRow / 64) * t + i);
   }
   {
     const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
     for (int r = 0; r < 4; ++r)
-      vro[r] = KV == kI4 ? S::at(rows[r], g >> 1) + 8 * (g & 1) : S::at(rows[r], g);
+      vro[r] = S::v_off(W) + warp * S::kTile +
+               (KV == kI4 ? S::at(rows[r], g >> 1) + 8 * (g & 1) : S::at(rows[r], g));
   }
-  const float kq = a.sm_scale_log2;
+  const uint32_t szo = S::sz_off(W) + 64 * warp + 4 * tau;  // this lane's K (V: + 64 W) pair
+  const float lsc = a.sm_scale_log2;  // softmax scale x log2(e)
+  const uint32_t nb32 = static_cast<uint32_t>(a.num_blocks);  // valid ids are below this
+  const uint32_t tx = S::tx_bytes(W);
+
+  // blocks staged (warp 0) and consumed (every warp) by this CTA, across its
+  // ranges: stage i % D, phase parity (i / D) & 1
+  uint32_t n_staged = 0, n_used = 0;
 
   auto run_range = [&](const int64_t x0, const int n, const int64_t rid) -> bool {
-    // ---- issue side: windows of 32 units located lane-parallel ---------------------
-    // lane i of window w holds unit 32 w + i of the range: its block id and its
-    // position packed as (kv head << 16 | request, block)
+    // ---- producer: windows of 32 blocks located lane-parallel by warp 0 -------------
     auto locate_window = [&](int w, int32_t& phys, uint32_t& key, int32_t& blk) {
       const int kk = 32 * w + lane;
       phys = -1;
@@ -187,13 +228,15 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         phys = a.block_tables[static_cast<int64_t>(lo) * a.max_blocks + skip_of(a, lo) + blk];
       }
     };
-    int32_t wphys, nphys;
-    uint32_t wkey, nkey;
-    int32_t wblk, nblk_;
-    locate_window(0, wphys, wkey, wblk);
-    locate_window(1, nphys, nkey, nblk_);
-    const uint32_t nb32 = static_cast<uint32_t>(a.num_blocks);  // valid ids are below this
-    auto issue_unit = [&](const int ST, const int kq) {
+    int32_t wphys = -1, nphys = -1, wblk = 0, nblk_ = 0;
+    uint32_t wkey = 0, nkey = 0;
+    if (producer) {
+      locate_window(0, wphys, wkey, wblk);
+      locate_window(1, nphys, nkey, nblk_);
+    }
+    // warp 0 stages block kq of the range into the next stage; false when the
+    // CTA stops (a wait ran out)
+    auto stage_block = [&](const int kq) -> bool {
       const int kk = kq & 31;
       if (kk == 0 && kq > 0) {  // next window; locate the one after it
         wphys = nphys; wkey = nkey; wblk = nblk_;
@@ -202,39 +245,45 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
       const int32_t phys = __shfl_sync(kFull, wphys, kk);
       const uint32_t key = __shfl_sync(kFull, wkey, kk);
       const int32_t blk = __shfl_sync(kFull, wblk, kk);
-      const bool ok = static_cast<uint32_t>(phys) < nb32;
+      const uint32_t s = n_staged % D;
+      bool go = true;
       if (lane == 0) {
-        sts64(wr + S::kInfoOff + 8 * ST, key, ok ? static_cast<uint32_t>(blk) : 0xFFFFFFFFu);
-        if (!ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
-      }
-      if (ok) {
-        // row r of the (block, head) tile: ((phys * 16 + r) * kv_heads + h) * kRow
-        const int h = static_cast<int>(key >> 16);
-        const int64_t ph = static_cast<int64_t>(phys) * a.kv_heads + h;
-        const int64_t base = (static_cast<int64_t>(phys) * kBlock * a.kv_heads + h) * S::kRow;
-        const uint8_t* kb = a.k + base;
-        const uint8_t* vb = a.v + base;
-        const uint32_t kd = wr + ST * S::kTile, vd = wr + S::kVOff + ST * S::kTile;
-#pragma unroll
-        for (int i = 0; i < S::kCopies; ++i) {
-          cp_async16(kd + cdst[i], kb + csrc[i]);
-          cp_async16(vd + cdst[i], vb + csrc[i]);
+        const uint32_t st = stage0 + s * SB, full = full0 + 8 * s;
+        // the stage's previous block must have been read by every warp
+        if (n_staged >= D && !mbar_wait_or_abort(empty0 + 8 * s, ((n_staged / D) - 1) & 1u,
+                                                 abort_s)) {
+          if (*abort_s == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
+          *abort_s = 1;
+          go = false;
+        } else {
+          const bool ok = static_cast<uint32_t>(phys) < nb32;
+          sts64(st + S::info_off(W), key, ok ? static_cast<uint32_t>(blk) : 0xFFFFFFFFu);
+          if (ok) {
+            const int h0 = static_cast<int>(key >> 16) * W;  // first kv head of the group
+            const int64_t szi = (static_cast<int64_t>(phys) * a.kv_heads + h0) * kBlock;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arm(full, tx);
+            tma_tile_4d(st, &a.kh_map, 0, 0, h0, phys, full);
+            tma_tile_4d(st + S::v_off(W), &a.vh_map, 0, 0, h0, phys, full);
+            bulk_copy(st + S::sz_off(W), a.k_sz + szi, 64 * W, full);
+            bulk_copy(st + S::sz_off(W) + 64 * W, a.v_sz + szi, 64 * W, full);
+          } else {
+            report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+            mbar_arrive(full);  // nothing to copy: the phase completes now
+          }
         }
-        if (lane < 8) cp_async16(wr + S::kSzOff + 128 * ST + 16 * lane, sz_src + ph * kBlock);
       }
+      const bool cont = __shfl_sync(kFull, go ? 1 : 0, 0) != 0;
+      if (cont) ++n_staged;
+      return cont;
     };
-    // stage ST receives unit kq of the range (nothing past its end); every call
-    // commits one cp.async group, so that the wait below always counts kDepth - 1
-    auto issue = [&](const int ST, const int kq) {
-      if (kq < n) issue_unit(ST, kq);
-      cp_async_commit();
-    };
-#pragma unroll
-    for (int k = 0; k < D - 1; ++k) issue(k, k);
+    bool staging = producer;
+    for (int k = 0; staging && k < D - 1 && k < n; ++k) staging = stage_block(k);
 
-    // ---- per-request state -----------------------------------------------------------
+    // ---- per-request state of this warp's kv head -------------------------------------
     uint32_t seg_key = 0xFFFFFFFFu;
     int L = 0, seg_nblk = 0, seg_skip = 0, hq0 = 0, seg_b = 0;
+    const int hh0 = warp * kGqaGroup;  // this warp's first record row in the group
     int64_t seg_start = 0;
     uint32_t qb[8][2];           // Q as the B operand of S^T = K Q^T (dims permuted like K)
     float qz0 = 0.f, qz1 = 0.f;  // sm_scale log2(e) sum(q) of this lane's two heads
@@ -260,57 +309,62 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         for (int c = 0; c < 4; ++c) o[i][c] += __shfl_xor_sync(kFull, o[i][c], 2);
       R[0] += __shfl_xor_sync(kFull, R[0], 2);
       R[1] += __shfl_xor_sync(kFull, R[1], 2);
+      if (tsel != 0) return;  // lanes t = 2, 3 now hold copies
       const bool contained = seg_start >= x0 && seg_start + seg_nblk <= x0 + n;
       const int64_t row0 = static_cast<int64_t>(seg_b) * a.q_heads + hq0;
-      if (tsel == 0) {  // lanes t = 2, 3 hold copies
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int hh = 2 * t + u;
-          const float l = u ? l1 : l0, m = u ? m1 : m0;
-          const float corr = (u ? z1 : z0) - kMid * R[u];
-          float acc[16];
+      for (int u = 0; u < 2; ++u) {
+        const int hh = 2 * t + u;
+        const float l = u ? l1 : l0, m = u ? m1 : m0;
+        const float corr = (u ? z1 : z0) - kMid * R[u];
+        float acc[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            // INT4 output rows fed by a nibble at bits 4-7 (odd i) carry 16 c
-            const float sc = (KV == kI4 && (i & 1)) ? kTwo24 / 16.f : kTwo24;
-            acc[i] = fmaf(o[i][u], sc, corr);
-            acc[8 + i] = fmaf(o[i][2 + u], sc, corr);
-          }
-          if (contained) {
-            float mm = m, ll = l;
-            if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
-            const float inv = ll > 0.f ? 1.f / ll : 0.f;
-            uint32_t w[8];
+        for (int i = 0; i < 8; ++i) {
+          // INT4 output rows fed by a nibble at bits 4-7 (odd i) carry 16 c
+          const float sc = (KV == kI4 && (i & 1)) ? kTwo24 / 16.f : kTwo24;
+          acc[i] = fmaf(o[i][u], sc, corr);
+          acc[8 + i] = fmaf(o[i][2 + u], sc, corr);
+        }
+        if (contained) {
+          float mm = m, ll = l;
+          if (seg_skip > 0) merge_prefix(a, row0 + hh, seg_skip, g, mm, ll, acc);
+          const float inv = ll > 0.f ? 1.f / ll : 0.f;
+          uint32_t w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              w[i] = pack2<false>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                                  (row0 + hh) * kHeadDim + 16 * g);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last
-            float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh) * kPartStride;
-            float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
+          for (int i = 0; i < 8; ++i) w[i] = pack2<false>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                                (row0 + hh) * kHeadDim + 16 * g);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+          const int slot = seg_start <= x0 ? 0 : 1;  // the request holding x0, else the last one
+          float* rec = a.part + ((rid * 2 + slot) * a.hpg + hh0 + hh) * kPartStride;
+          float4* ov = reinterpret_cast<float4*>(rec + 16 * g);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ov[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-            if (g == 0) {
-              rec[kHeadDim] = m;
-              rec[kHeadDim + 1] = l;
-            }
+          for (int i = 0; i < 4; ++i)
+            ov[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+          if (g == 0) {
+            rec[kHeadDim] = m;
+            rec[kHeadDim + 1] = l;
           }
         }
       }
     };
 
-    // unit k of the range in stage ST
-    auto step = [&](const int ST, const int k) {
-      issue(ST == 0 ? D - 1 : ST - 1, k + D - 1);  // the stage unit k - 1 used
-      cp_async_wait<D - 1>();  // this lane's copies of unit k have landed
-      __syncwarp();            // ... and every other lane's
-      // (kv head << 16 | request, block; all ones for a block id outside the pool)
-      const uint2 info = lds64u(wr + S::kInfoOff + 8 * ST);
+    for (int k = 0; k < n; ++k) {
+      if (staging && k + D - 1 < n) staging = stage_block(k + D - 1);
+      const uint32_t s = n_used % D;
+      const uint32_t st = stage0 + s * SB;
+      if (!mbar_wait_or_abort(full0 + 8 * s, (n_used / D) & 1u, abort_s)) {
+        if (lane == 0 && *abort_s == 0) {
+          report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
+          *abort_s = 1;
+        }
+        return false;
+      }
+      ++n_used;
+      // (head group << 16 | request, block; all ones for a block id outside the pool)
+      const uint2 info = lds64(st + S::info_off(W));
       const bool blk_ok = info.y != 0xFFFFFFFFu;
       const int j = static_cast<int>(info.y);
 
@@ -323,7 +377,7 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         seg_nblk = cum[seg_b + 1] - cum[seg_b];
         L = lown[seg_b];
         seg_skip = skip_of(a, seg_b);
-        hq0 = hgi * kGqaGroup;
+        hq0 = (hgi * W + warp) * kGqaGroup;
         // Q of head hq0 + (g mod 4) (columns 4-7 repeat 0-3), dims [32t, 32t + 32)
         uint32_t qw[16];
         const uint4* qp = reinterpret_cast<const uint4*>(
@@ -356,8 +410,8 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         for (int i = 0; i < 16; ++i) part += half_lo(qw[i]) + half_hi(qw[i]);
         part += __shfl_xor_sync(kFull, part, 1);
         part += __shfl_xor_sync(kFull, part, 2);  // lanes 4h hold sum(q) of head h
-        qz0 = kq * __shfl_sync(kFull, part, (2 * hp) * 4);
-        qz1 = kq * __shfl_sync(kFull, part, (2 * hp + 1) * 4);
+        qz0 = lsc * __shfl_sync(kFull, part, (2 * hp) * 4);
+        qz1 = lsc * __shfl_sync(kFull, part, (2 * hp + 1) * 4);
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         R[0] = R[1] = R[2] = R[3] = 0.f;
@@ -366,13 +420,11 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
       }
 
       if (blk_ok) {
-        const uint32_t kKt = ST * S::kTile, kVt = S::kVOff + ST * S::kTile;
-        const uint32_t szp = wr + S::kSzOff + 128 * ST + 4 * tau;
-        const uint32_t ksz = lds32(szp), vsz = lds32(szp + 64);
+        const uint32_t ksz = lds32(st + szo), vsz = lds32(st + szo + 64 * W);
         // ---- S^T = K Q^T: class-A k-steps into sa, class-B into sb -------------------
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (KV == kI4) {
-          const uint4 k0 = lds128(wr + kKt + kro[0][0]), k1 = lds128(wr + kKt + kro[1][0]);
+          const uint4 k0 = lds128(st + kro[0][0]), k1 = lds128(st + kro[1][0]);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const uint32_t w0 = w4(k0, jj), w1 = w4(k1, jj);  // rows g, g + 8
@@ -385,8 +437,7 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         } else {
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            const uint4 k0 = lds128(wr + kKt + kro[0][half]);
-            const uint4 k1 = lds128(wr + kKt + kro[1][half]);
+            const uint4 k0 = lds128(st + kro[0][half]), k1 = lds128(st + kro[1][half]);
 #pragma unroll
             for (int q2 = 0; q2 < 4; q2 += 2) {
               const int kk = 4 * half + q2;
@@ -402,13 +453,14 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
           }
         }
         // this lane's token (row g or g + 8) and heads (2 hp, 2 hp + 1)
-        const float xa0 = tsel ? sa[2] : sa[0], xa1 = tsel ? sa[3] : sa[1];
-        const float xb0 = tsel ? sb[2] : sb[0], xb1 = tsel ? sb[3] : sb[1];
-        const float d0 = KV == kI4 ? fmaf(xb0, 1.f / 16.f, xa0) : xa0 + xb0;
-        const float d1 = KV == kI4 ? fmaf(xb1, 1.f / 16.f, xa1) : xa1 + xb1;
-        const float sk = half_lo(ksz) * (kTwo24 * kq), zk = half_hi(ksz);
+        const float d0a = KV == kI4 ? fmaf(sb[0], 1.f / 16.f, sa[0]) : sa[0] + sb[0];
+        const float d1a = KV == kI4 ? fmaf(sb[1], 1.f / 16.f, sa[1]) : sa[1] + sb[1];
+        const float d0b = KV == kI4 ? fmaf(sb[2], 1.f / 16.f, sa[2]) : sa[2] + sb[2];
+        const float d1b = KV == kI4 ? fmaf(sb[3], 1.f / 16.f, sa[3]) : sa[3] + sb[3];
+        const float d0 = tsel ? d0b : d0a, d1 = tsel ? d1b : d1a;
+        const float sk = half_lo(ksz) * (kTwo24 * lsc), zk = half_hi(ksz);
         float s0 = fmaf(sk, d0, zk * qz0), s1 = fmaf(sk, d1, zk * qz1);
-        if (j * kBlock + tau >= L) s0 = s1 = -INFINITY;
+        if ((j + 1) * kBlock > L && j * kBlock + tau >= L) s0 = s1 = -INFINITY;
         const float sv = half_lo(vsz);
         // ---- online softmax: the running maximum moves when a score passes it by
         // more than the slack (by anything, for a token with a large V scale) ------
@@ -446,8 +498,8 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
         bp[1] = movmatrix_trans(tsel ? hpk : 0u);
         // ---- O^T += V^T P'^T over 8 tiles of 16 dims, and sum(P') ---------------------
         if constexpr (KV == kI4) {
-          const uint2 v0 = lds64(wr + kVt + vro[0]), v1 = lds64(wr + kVt + vro[1]);
-          const uint2 v2 = lds64(wr + kVt + vro[2]), v3 = lds64(wr + kVt + vro[3]);
+          const uint2 v0 = lds64(st + vro[0]), v1 = lds64(st + vro[1]);  // rows 2t, 2t+1
+          const uint2 v2 = lds64(st + vro[2]), v3 = lds64(st + vro[3]);  // rows 2t+8, 2t+9
           // two rows side by side: lo halves = the first row's 4 dims, hi halves
           // = the second row's
 #pragma unroll
@@ -475,8 +527,8 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
             }
           }
         } else {
-          const uint4 v0 = lds128(wr + kVt + vro[0]), v1 = lds128(wr + kVt + vro[1]);
-          const uint4 v2 = lds128(wr + kVt + vro[2]), v3 = lds128(wr + kVt + vro[3]);
+          const uint4 v0 = lds128(st + vro[0]), v1 = lds128(st + vro[1]);
+          const uint4 v2 = lds128(st + vro[2]), v3 = lds128(st + vro[3]);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             // words hf (dims 16g + 4hf + 0..3) and 2 + hf (dims 16g + 8 + 4hf + 0..3)
@@ -508,26 +560,63 @@ __device__ __forceinline__ void gqa_body(const DecodeArgs& a, unsigned char* dsm
           mma16816<false>(R, ones, bp);
         }
       }
-      __syncwarp();  // all lanes are done with this stage before it is refilled
-    };
-
-    for (int k = 0, st = 0; k < n; ++k, st = st == D - 1 ? 0 : st + 1) step(st, k);
-    cp_async_wait<0>();
+      __syncwarp();  // every lane is done with the stage
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
     if (seg_key != 0xFFFFFFFFu) flush();
     return true;
   };
 
-  for_each_range<TAIL>(a, sp, gw, lane, run_range);
+  // ---- this CTA's ranges: its static range, then tail chunks ---------------------------
+  const RangeMap& rm = sp.rm;
+  bool alive = true;
+  if (rm.k > 0) {  // the same cut in every head group
+    if (cta < static_cast<int64_t>(sp.groups) * rm.k) {
+      const int64_t hgi = cta / rm.k, i = cta - hgi * rm.k;
+      const int64_t lo = i * rm.Pst;
+      if (lo < tb)
+        alive = run_range(hgi * tb + lo,
+                          static_cast<int>(min(tb - lo, static_cast<int64_t>(rm.Pst))), cta);
+    }
+  } else {
+    const int64_t xs = static_cast<int64_t>(cta) * rm.Pst;
+    if (xs < sp.static_end)
+      alive = run_range(
+          xs, static_cast<int>(min(sp.static_end - xs, static_cast<int64_t>(rm.Pst))), cta);
+    if constexpr (TAIL) {
+      while (rm.C > 0) {
+        __syncthreads();  // every warp is done with the previous range
+        if (tid == 0) *chunk_s = *abort_s ? -1 : static_cast<int32_t>(atomicAdd(a.tail_ctr, 1u));
+        __syncthreads();
+        const int32_t c = *chunk_s;
+        if (c < 0 || static_cast<int64_t>(c) >= rm.ntail) break;
+        const int64_t x0 = sp.static_end + static_cast<int64_t>(c) * rm.C;
+        alive = run_range(x0, static_cast<int>(min(sp.total - x0, static_cast<int64_t>(rm.C))),
+                          sp.nwarps + c) && alive;
+      }
+    }
+  }
+  (void)alive;
+  // nothing may still be copied into shared memory when the CTA exits: after a
+  // timeout, the stages staged but not read are waited for (bounded)
+  __syncthreads();
+  if (tid == 0) {
+    const int zero = 0;
+    for (uint32_t i = n_used; i < n_staged; ++i)
+      mbar_wait_or_abort(full0 + 8 * (i % D), (i / D) & 1u, &zero);
+  }
 }
 
 template <int KV, bool TAIL>
-__global__ void __launch_bounds__(kDecodeThreads, 4)
+__global__ void __launch_bounds__(kMaxCtaHeads * 32, 2)
     decode_gqa_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ __align__(128) unsigned char dsmem[];
-  __shared__ int32_t warp_sum[kWarps];
+  extern __shared__ __align__(1024) unsigned char dsmem[];
+  __shared__ int32_t warp_sum[kMaxCtaHeads];
+  __shared__ int abort_s;
+  __shared__ int32_t chunk_s;
   // the combine kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;");
-  gqa_body<KV, TAIL>(a, dsmem, warp_sum, blockIdx.x, gridDim.x);
+  gqa_body<KV, TAIL>(a, dsmem, warp_sum, &abort_s, &chunk_s, blockIdx.x, gridDim.x);
 }
 
 template <int KV, bool TAIL>
@@ -539,39 +628,47 @@ cudaError_t launch_gqa_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   if (opted_in_device != dev) {
     e = cudaFuncSetAttribute(decode_gqa_kernel<KV, TAIL>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gqa_smem_bytes<KV>(kMaxBatch)));
+                             static_cast<int>(gqa_smem_bytes<KV>(kMaxBatch, kMaxCtaHeads)));
     if (e != cudaSuccess) return e;
     opted_in_device = dev;
   }
-  decode_gqa_kernel<KV, TAIL><<<grid, kDecodeThreads, gqa_smem_bytes<KV>(a.batch), s>>>(a);
+  decode_gqa_kernel<KV, TAIL>
+      <<<grid, a.cta_heads * 32, gqa_smem_bytes<KV>(a.batch, a.cta_heads), s>>>(a);
   return cudaGetLastError();
 }
 
 template <int KV, bool TAIL>
-int gqa_occupancy_t(int batch) {
+int gqa_occupancy_t(int batch, int w) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
-  if (dev == cached_dev && batch == cached_batch) return cached_n;
+  thread_local int cached_dev = -1, cached_batch = -1, cached_w = -1, cached_n = 0;
+  if (dev == cached_dev && batch == cached_batch && w == cached_w) return cached_n;
   if (cudaFuncSetAttribute(decode_gqa_kernel<KV, TAIL>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(gqa_smem_bytes<KV>(kMaxBatch))) != cudaSuccess)
+                           static_cast<int>(gqa_smem_bytes<KV>(kMaxBatch, kMaxCtaHeads))) !=
+      cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gqa_kernel<KV, TAIL>,
-                                                    kDecodeThreads,
-                                                    gqa_smem_bytes<KV>(batch)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gqa_kernel<KV, TAIL>, w * 32,
+                                                    gqa_smem_bytes<KV>(batch, w)) != cudaSuccess)
     return 0;
   cached_dev = dev;
   cached_batch = batch;
+  cached_w = w;
   cached_n = n;
   return n;
 }
 
 }  // namespace
 
-bool decode_gqa_supported(int kv_dtype, int q_dtype, int group) {
-  return (kv_dtype == kI8 || kv_dtype == kI4) && q_dtype == kF16 && group == kGqaGroup;
+int decode_gqa_cta_heads(int kv_heads) {
+  if (kv_heads <= kMaxCtaHeads) return kv_heads;
+  return kv_heads % kMaxCtaHeads == 0 ? kMaxCtaHeads : 0;
+}
+
+bool decode_gqa_supported(int kv_dtype, int q_dtype, int group, int kv_heads) {
+  return (kv_dtype == kI8 || kv_dtype == kI4) && q_dtype == kF16 && group == kGqaGroup &&
+         decode_gqa_cta_heads(kv_heads) > 0;
 }
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, int kv_dtype, int grid, cudaStream_t s) {
@@ -583,11 +680,11 @@ cudaError_t launch_decode_gqa(const DecodeArgs& a, int kv_dtype, int grid, cudaS
   return cudaErrorInvalidValue;
 }
 
-int decode_gqa_ctas_per_sm(int kv_dtype, int batch, bool tail) {
+int decode_gqa_ctas_per_sm(int kv_dtype, int batch, int w, bool tail) {
   if (kv_dtype == kI8)
-    return tail ? gqa_occupancy_t<kI8, true>(batch) : gqa_occupancy_t<kI8, false>(batch);
+    return tail ? gqa_occupancy_t<kI8, true>(batch, w) : gqa_occupancy_t<kI8, false>(batch, w);
   if (kv_dtype == kI4)
-    return tail ? gqa_occupancy_t<kI4, true>(batch) : gqa_occupancy_t<kI4, false>(batch);
+    return tail ? gqa_occupancy_t<kI4, true>(batch, w) : gqa_occupancy_t<kI4, false>(batch, w);
   return 0;
 }
 

@@ -89,6 +89,15 @@ struct DecodeArgs {
   int pmax_chunks;            // ceil(max_shared / pchunk): records per (request, q head)
   int32_t* skip;              // [batch] shared blocks of request b (0: none)
   float* ppart;               // [batch][q_heads][pmax_chunks][kPartStride]
+  // grouped-query kernel: kv heads per CTA (one warp each; 0 for the other
+  // kernels); its stream runs over (group of cta_heads kv heads, request,
+  // block) and its records hold the group's cta_heads * group q heads
+  int cta_heads;
+  // ... and its TMA views of the K and V pools, ordered [block][kv head][token]
+  // [row], one box = the 16 rows of cta_heads kv heads (k_map / v_map keep the
+  // one-tile view the other INT8 kernels use)
+  CUtensorMap kh_map;
+  CUtensorMap vh_map;
 };
 
 struct CopyArgs {
@@ -175,10 +184,14 @@ cudaError_t launch_prefix(const DecodeArgs& a, int kv_dtype, int q_dtype, int gr
 // CTAs of the decode kernel resident per SM (occupancy) for a dtype pair and batch
 int decode_ctas_per_sm(int kv_dtype, int q_dtype, int batch, bool tail);
 // The grouped-query decode kernel (kvq_decode_gqa.cu): INT8 / INT4 pools, fp16
-// queries, 4 q heads per kv head; same workspace, records and combine.
-bool decode_gqa_supported(int kv_dtype, int q_dtype, int group);
+// queries, 4 q heads per kv head, a CTA per group of cta_heads kv heads (one
+// warp each); same workspace and combine, records of cta_heads * 4 q heads.
+// Its kh_map / vh_map are the [block][kv head][token][row] views
+// (encode_pool_map_heads).
+bool decode_gqa_supported(int kv_dtype, int q_dtype, int group, int kv_heads);
+int decode_gqa_cta_heads(int kv_heads);  // kv heads per CTA (0: unsupported)
 cudaError_t launch_decode_gqa(const DecodeArgs& a, int kv_dtype, int grid, cudaStream_t s);
-int decode_gqa_ctas_per_sm(int kv_dtype, int batch, bool tail);
+int decode_gqa_ctas_per_sm(int kv_dtype, int batch, int cta_heads, bool tail);
 // the same for the shared-prefix kernel and a number of groups
 int prefix_ctas_per_sm(int kv_dtype, int q_dtype, int num_groups);
 
