@@ -405,6 +405,9 @@ kvq_status kv_store_quant(const kvq_pool* pool, const void* k_new, const void* v
   if (!is_float16(in_dtype)) return KVQ_ERR_UNSUPPORTED;
   if (is_float16(pool->kv_dtype) && in_dtype != pool->kv_dtype) return KVQ_ERR_UNSUPPORTED;
   if (num_tokens == 0) return KVQ_OK;
+  // the store numbers its (token, K or V, kv head) rows in 32 bits
+  if (num_tokens > static_cast<int64_t>(kvq::kMaxStoreRows / (2 * pool->kv_heads)))
+    return KVQ_ERR_UNSUPPORTED;
   if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
   kvq::StoreArgs a;

@@ -196,6 +196,7 @@ int decode_gqa_ctas_per_sm(int kv_dtype, int batch, int cta_heads, bool tail);
 int prefix_ctas_per_sm(int kv_dtype, int q_dtype, int num_groups);
 
 constexpr int kMaxBatch = 8192;        // request lengths are scanned in shared memory
+constexpr uint32_t kMaxStoreRows = 0xFFFFFFFFu;  // store rows (tokens x 2 x kv heads) per call
 constexpr int kDecodeThreads = 128;
 constexpr int kMaxCtasPerSm = 4;       // the workspace has slots for this many CTAs per SM
 constexpr int kPartStride = kHeadDim + 4;  // floats per partial record (16-byte multiple)

@@ -44,11 +44,14 @@ __device__ __forceinline__ RowIn load_row(const StoreArgs& a, int64_t row, int l
   const int64_t rows = a.num_tokens * 2 * a.kv_heads;
   RowIn in;
   in.in_range = row < rows;
-  // row = (token * 2 + which) * kv_heads + head
-  const int64_t r = in.in_range ? row : 0;
-  in.h = static_cast<int>(r % a.kv_heads);
-  in.which = static_cast<int>((r / a.kv_heads) & 1);
-  const int64_t t = r / (2 * a.kv_heads);
+  // row = (token * 2 + which) * kv_heads + head, below 2^32 (kv_store_quant
+  // refuses larger stores): one 32-bit division
+  const uint32_t r = in.in_range ? static_cast<uint32_t>(row) : 0u;
+  const uint32_t kvh = static_cast<uint32_t>(a.kv_heads);
+  const uint32_t q = r / kvh;
+  in.h = static_cast<int>(r - q * kvh);
+  in.which = static_cast<int>(q & 1u);
+  const int64_t t = static_cast<int64_t>(q >> 1);
   in.slot = in.in_range ? a.slot_mapping[t] : -1;
   const uint16_t* src = static_cast<const uint16_t*>(in.which ? a.v_new : a.k_new) +
                         (t * a.kv_heads + in.h) * kHeadDim + lane16 * 8;
@@ -105,18 +108,24 @@ __device__ __forceinline__ void write_row(const StoreArgs& a, const RowIn& in, i
     // unless fl(d * inv) lies within that distance of a tie k + 1/2; there
     // (tested with the wider margin 2^-20 |q|) the correctly rounded division
     // decides. The codes are those of the division, bit for bit.
-    const float inv = __frcp_rn(S);
+    // A degenerate row takes inv = 0: every quotient is 0 (or NaN when Z is not
+    // finite), which converts to code 0 and never looks like a tie.
+    const float inv = degenerate ? 0.f : __frcp_rn(S);
     uint32_t c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float d = __fsub_rn(x[i], Z);
       float qf = __fmul_rn(d, inv);
-      const float frac = __fsub_rn(qf, floorf(qf));
-      if (fabsf(__fsub_rn(frac, 0.5f)) <= fabsf(qf) * 0x1p-20f + 0x1p-30f)
-        qf = __fdiv_rn(d, S);
-      int q = degenerate ? 0 : __float2int_rn(qf);
-      q = min(max(q, 0), kQmax);
-      c[i] = static_cast<uint32_t>(q);
+      // |qf - rint(qf)| is qf's distance to the nearest integer; qf lies within
+      // 2^-20 |qf| (+ 2^-30) of a tie k + 1/2 exactly when that distance plus
+      // the margin reaches 1/2
+      const float r = rintf(qf);
+      if (fmaf(fabsf(qf), 0x1p-20f, fabsf(__fsub_rn(qf, r))) >= 0.5f - 0x1p-30f)
+        qf = rintf(__fdiv_rn(d, S));
+      else
+        qf = r;
+      // round-half-even already done; negative codes saturate to 0
+      c[i] = min(__float2uint_rn(qf), static_cast<unsigned>(kQmax));
     }
     if constexpr (KV == kI8) {
       uint2 o;
