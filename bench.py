@@ -605,6 +605,10 @@ def measure_workload(kvq, name: str, dev, peak: float, reps: int = 100) -> dict:
         "store": store,
         "cuda_graph": True, "reps": reps,
     }
+    traffic, sha = traffic_from_profile(wl.name, "gqa" if uses_gqa_kernel(wl) else "decode")
+    res["traffic"] = traffic  # ncu DRAM bytes per decode launch, null when taken on other source
+    res["traffic_over_algorithmic"] = None if traffic is None else round(traffic / alg, 4)
+    res["kernel_source_sha"] = sha
     del graphs, pools, pool, ws
     torch.cuda.empty_cache()
     return res
