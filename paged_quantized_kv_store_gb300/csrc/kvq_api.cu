@@ -604,21 +604,18 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   a.dev_err = dev_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.counter, 0, sizeof(int32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
-  // tcgen05 (128-row tiles) when the pool kind allows it and the batch has at
-  // least one tile per SM; else 16-row tiles on mma.sync (which can also cut
+  // tcgen05 (256-row units) when the pool kind allows it and the batch has at
+  // least one unit per SM; else 16-row tiles on mma.sync (which can also cut
   // the context of a short chunk into parts)
-  const int64_t tc_tiles = static_cast<int64_t>(pool->kv_heads) *
-                           ((static_cast<int64_t>(total_q) * a.group + 127) / 128);
+  const int64_t tc_units = static_cast<int64_t>(pool->kv_heads) *
+                           ((static_cast<int64_t>(total_q) * a.group + 255) / 256);
   const bool use_tc = variant == KVQ_EXTEND_TCGEN05 ||
                       (variant == KVQ_EXTEND_AUTO &&
-                       kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_tiles >= sms);
+                       kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_units >= sms);
   if (use_tc) {
-    // persistent CTAs: two per SM (each holds 256 of the SM's 512 TMEM
-    // columns) while their shared memory fits, else one
+    // persistent CTAs, one per SM (each holds all 512 TMEM columns)
     if (kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch) <= 0) return KVQ_ERR_CUDA;
-    const size_t per_cta = kvq::extend_tc_smem_bytes(batch) + 2048;  // + static + reserved
-    const int per_sm = per_cta * 2 <= 228 * 1024 ? 2 : 1;
-    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms * per_sm, s) == cudaSuccess
+    return kvq::launch_extend_tc(a, pool->kv_dtype, q_dtype, sms, s) == cudaSuccess
                ? KVQ_OK
                : KVQ_ERR_CUDA;
   }

@@ -1,30 +1,34 @@
 // kvq_extend_tc: extend (chunked prefill) attention on the 5th-generation
-// tensor cores (tcgen05, accumulators in tensor memory).
+// tensor cores (tcgen05, accumulators in tensor memory), warp-specialised.
 //
 // Same computation as kvq_extend.cu ("pymllm Runtime Design", forward stage:
 // extend / prefill; LMDeploy article §2.3: prefills split into chunks; §2.4:
-// per-token, per-head INT8/INT4 scale and zero). A CTA takes 128 rows (query,
-// q head) of one kv head = the 128 TMEM lanes, one thread per row, and walks
-// the request's context in tiles of 64 tokens (4 blocks):
-//   1. the 128 threads stage the tile: K codes become centred 16-bit values
-//      c - mid (exact; Q's type) in a K-major 128-byte-swizzled tile, V codes
-//      become c - mid in fp16 written transposed (dims as rows, tokens as the
-//      reduction axis), so both products read K-major operands; the
-//      per-token scale S and shifted zero Z + mid S go to a small table;
-//   2. one thread issues S = Q K^T (M 128, N 64, K 128: 8 MMAs) into TMEM;
-//   3. every thread reads its row of S (tcgen05.ld), applies
-//      s = S_k (q.(c - mid)) + (Z_k + mid S_k) sum(q), the causal mask and the
-//      online softmax (no shuffles: a thread owns its row); when its running
-//      maximum moves by more than a threshold, the warp rescales its rows of
-//      O in TMEM (a stale maximum only scales every term alike); P' = p S_v goes
-//      to shared memory in fp16 and sum p (Z_v + mid S_v) stays in a register;
-//   4. one thread issues O += P' V (M 128, N 128, K 64: 4 MMAs) into TMEM.
-// At the end each thread reads its row of O, adds the zero term, divides by
-// the softmax sum and writes the output row. Every mbarrier wait is bounded
-// (2 s; then the CTA reports KVQ_DEV_ERR_TIMEOUT, frees its TMEM and stops).
-// Work units (request, kv head, 128-row tile) come from an atomic counter,
-// longest tiles first. Staging is not overlapped with the products in this
-// version.
+// per-token, per-head INT8/INT4 scale and zero). A work unit is 256 rows
+// (query, q head) of one kv head; the request's context is walked in tiles
+// of 64 tokens (4 blocks). One CTA per SM, thirteen warps in four roles:
+//   * staging warpgroup (warps 8-11): reads each tile's codes from the pool
+//     and writes K as centred 16-bit values c - mid (exact; Q's type) in a
+//     K-major 128-byte-swizzled tile and V as c - mid in fp16, transposed
+//     (dims as rows), into a two-stage ring, with the per-token scale S and
+//     shifted zero Z + mid S in four small arrays; it also hands out the work
+//     units (an atomic counter, longest tiles first);
+//   * MMA thread (warp 12, lane 0): for each tile issues S_g = Q_g K^T
+//     (M 128, N 64, K 128) for both softmax warpgroups into their own TMEM
+//     columns, and O_g += P'_g V (M 128, N 128, K 64) as soon as warpgroup
+//     g's P' is ready, so the tensor core works on one warpgroup's products
+//     while the other runs its softmax (ping-pong);
+//   * two softmax warpgroups (warps 0-3, 4-7), one thread per row: read the
+//     row of S (tcgen05.ld), apply s = S_k (q.(c - mid)) + (Z_k + mid S_k)
+//     sum(q), the causal mask and the online softmax; when the running
+//     maximum moves by more than a threshold, rescale the warp's rows of O in
+//     TMEM (a stale maximum only scales every term alike); write
+//     P' = p S_v to shared memory in fp16 and keep sum p (Z_v + mid S_v) in
+//     registers. At the end of the unit: (O + z) / l.
+// The per-token arithmetic runs on paired fp32 instructions (two tokens per
+// instruction). Roles meet only at mbarriers (no CTA-wide barrier inside the
+// work loop); every wait is bounded (2 s, then KVQ_DEV_ERR_TIMEOUT and every
+// role leaves its loop), and the MMA thread waits for its products in flight
+// before the CTA frees its TMEM.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -35,22 +39,43 @@
 namespace kvq {
 namespace {
 
-constexpr int kTcRows = 128;   // rows per CTA (M, TMEM lanes)
-constexpr int kTcTok = 64;     // tokens per context tile (N of S, K of P V)
-constexpr int kTcThreads = 128;
-constexpr uint32_t kTmemCols = 256;  // S: columns 0..63, O: 64..191
+constexpr int kWgRows = 128;              // rows per softmax warpgroup (M, TMEM lanes)
+constexpr int kUnitRows = 2 * kWgRows;    // rows per work unit
+constexpr int kTcTok = 64;                // tokens per context tile (N of S, K of P V)
+constexpr int kStageThreads = 128;        // staging warpgroup
+constexpr int kSoftWarps = 8;             // warps 0-7: softmax warpgroups 0 and 1
+constexpr int kMmaWarp = 12;              // warps 8-11 stage, warp 12 issues the MMAs
+constexpr int kTcThreads = 13 * 32;
+constexpr uint32_t kTmemCols = 512;       // S_g: columns 64 g .. 64 g + 63; O_g: 128 + 128 g ..
 
 // shared memory, offsets from a 1024-byte aligned base
-constexpr uint32_t kQOff = 0;                       // 2 x 128 rows x 128 B
-constexpr uint32_t kKOff = kQOff + 2 * 128 * 128;   // 2 x 64 rows x 128 B
-constexpr uint32_t kVOff = kKOff + 2 * 64 * 128;    // 1 x 128 rows x 128 B (V^T)
-constexpr uint32_t kPOff = kVOff + 128 * 128;       // 1 x 128 rows x 128 B
-constexpr uint32_t kSzOff = kPOff + 128 * 128;      // 64 tokens x 4 floats
-constexpr uint32_t kOkOff = kSzOff + kTcTok * 16;   // 64 token flags
-constexpr uint32_t kBarOff = kOkOff + kTcTok * 4;   // 2 mbarriers
-constexpr uint32_t kSlotOff = kBarOff + 16;         // TMEM base address
-constexpr uint32_t kSvMaxOff = kSlotOff + 8;        // largest V scale of the tile (2 halves)
-constexpr uint32_t kFixedBytes = kSlotOff + 16;
+constexpr uint32_t kQBytes = kWgRows * 256;         // 2 column blocks of 128 rows x 128 B
+constexpr uint32_t kKBytes = kTcTok * 256;          // 2 column blocks of 64 rows x 128 B
+constexpr uint32_t kVBytes = 128 * kTcTok * 2;      // 128 dims x 64 tokens
+constexpr uint32_t kPBytes = kWgRows * kTcTok * 2;  // 128 rows x 64 tokens
+constexpr uint32_t kSzBytes = 4 * kTcTok * 4;       // S_k'[64] Z_k'[64] S_v[64] Z_v'[64]
+constexpr uint32_t kQOff = 0;                       // Q of warpgroup g at g * kQBytes
+constexpr uint32_t kKOff = kQOff + 2 * kQBytes;     // K tile of stage s at s * kKBytes
+constexpr uint32_t kVOff = kKOff + 2 * kKBytes;
+constexpr uint32_t kPOff = kVOff + 2 * kVBytes;     // P' of warpgroup g
+constexpr uint32_t kSzOff = kPOff + 2 * kPBytes;
+constexpr uint32_t kInfoOff = kSzOff + 2 * kSzBytes;  // per stage: max S_v (2 halves), missing masks
+constexpr uint32_t kBarOff = kInfoOff + 2 * 16;
+// mbarriers (index: pairs by stage or warpgroup)
+constexpr uint32_t kBarKvFull = 0;     // staging -> MMA, softmax (128 arrivals)
+constexpr uint32_t kBarKvEmpty = 2;    // MMA commit: the stage's products are done
+constexpr uint32_t kBarSFull = 4;      // MMA commit: S_g is in TMEM
+constexpr uint32_t kBarPFull = 6;      // softmax g -> MMA (128 arrivals)
+constexpr uint32_t kBarODone = 8;      // MMA commit: O_g += P'_g V done
+constexpr uint32_t kBarQFull = 10;     // softmax g -> MMA: the unit's Q rows (128 arrivals)
+constexpr uint32_t kBarUnitFull = 12;  // unit slot written
+constexpr uint32_t kBarUnitEmpty = 14; // unit slot read by all 13 warps
+constexpr uint32_t kBarDrain = 16;     // MMA commit before TMEM is freed
+constexpr uint32_t kNumBars = 17;
+constexpr uint32_t kSlotOff = kBarOff + 8 * kNumBars;  // TMEM base address
+constexpr uint32_t kUnitOff = kSlotOff + 4;            // 2 unit slots
+constexpr uint32_t kAbortOff = kUnitOff + 8;
+constexpr uint32_t kFixedBytes = kAbortOff + 4;
 
 __host__ __device__ constexpr size_t tc_smem_bytes(int batch) {
   return 1024 + kFixedBytes + align128((batch + 1) * sizeof(int32_t));
@@ -69,7 +94,7 @@ __device__ __forceinline__ TcReq tc_req(const ExtendArgs& a, int b) {
   s.L = a.kv_lens[b];
   s.ok = s.q0 >= 0 && s.C >= 0 && q1 <= a.total_q && s.L >= s.C && s.L <= a.len_cap;
   if (!s.ok) s.C = s.L = 0;
-  s.tiles = (s.C * a.group + kTcRows - 1) / kTcRows;
+  s.tiles = (s.C * a.group + kUnitRows - 1) / kUnitRows;
   return s;
 }
 
@@ -81,21 +106,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
-}
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
 }
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
@@ -111,23 +121,19 @@ __device__ __forceinline__ uint32_t centred_pair(int c0, int c1, int mid) {
   return pack2<BF>(static_cast<float>(c0 - mid), static_cast<float>(c1 - mid));
 }
 
-// 16-bit pair (two consecutive tokens of one dim) for the transposed V tile.
-__device__ __forceinline__ uint32_t lo_hi(uint32_t x, uint32_t y, bool hi) {
-  return hi ? ((x >> 16) | (y & 0xFFFF0000u)) : ((x & 0xFFFFu) | (y << 16));
-}
-
-// Raw bytes of one 64-token context tile that this thread stages: K chunks
-// (16 bytes of one token row each), V pieces (8 dims of 8 consecutive tokens),
-// and, for threads < 64, the scale/zero words and validity of token tid.
+// Raw bytes of one 64-token context tile that staging thread `tid` (0..127)
+// holds: K chunks (16 bytes of one token row each), V pieces (8 dims of 8
+// consecutive tokens), and, for threads < 64, the scale/zero words of token
+// tid and whether its block is missing.
 template <int KV>
 struct RawTile {
   static constexpr int kRow = KvTraits<KV>::kRowBytes;
-  static constexpr int kKChunks = kTcTok * (kRow / 16) / kTcThreads;  // 4 / 2 / 8
+  static constexpr int kKChunks = kTcTok * (kRow / 16) / kStageThreads;  // 4 / 2 / 8
   static constexpr int kVWords = kRow / 64;  // 32-bit words per token of an 8-dim piece: 2 / 1 / 4
   uint4 k[kKChunks];
   uint32_t v[8][kVWords];
   uint32_t ksz, vsz;
-  bool ok;
+  bool miss;  // token `tid` of the tile is in the context but its block id is outside the pool
 };
 
 // Global row (token t of the tile, kv head h) of a pool, or null when the
@@ -149,7 +155,7 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int32_t* bt
   constexpr int kChunks = R::kRow / 16;
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
-    const int e = tid + kTcThreads * i;
+    const int e = tid + kStageThreads * i;
     const uint8_t* src = tc_row<KV>(a, bt, a.k, tok0 + e / kChunks, L, h);
     r.k[i] = src ? __ldg(reinterpret_cast<const uint4*>(src) + e % kChunks)
                  : make_uint4(0u, 0u, 0u, 0u);
@@ -179,19 +185,20 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int32_t* bt
       r.v[t][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
     }
   }
-  r.ok = false;
+  r.miss = false;
   r.ksz = r.vsz = 0u;
   if (tid < kTcTok) {
     const int tt = tok0 + tid;
     if (tt < L) {
       const int32_t blk = bt[tt / kBlock];
-      r.ok = blk >= 0 && blk < a.num_blocks;
-      if (r.ok && KvTraits<KV>::kQuant) {
+      const bool ok = blk >= 0 && blk < a.num_blocks;
+      if (ok && KvTraits<KV>::kQuant) {
         const int64_t i = (static_cast<int64_t>(blk) * a.kv_heads + h) * kBlock + tt % kBlock;
         r.ksz = __ldg(a.k_sz + i);
         r.vsz = __ldg(a.v_sz + i);
       }
-      if (!r.ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+      r.miss = !ok;
+      if (!ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
     }
   }
 }
@@ -215,17 +222,18 @@ __device__ __forceinline__ void piece_pairs(const uint32_t (&w)[RawTile<KV>::kVW
   }
 }
 
-// Registers -> shared memory: the K tile (K-major, Q's type), V transposed
-// (fp16), per-token (S_k', Z_k', S_v, Z_v') with the softmax scale folded
-// into the K pair, and validity flags. Returns (for the whole CTA) whether
-// any token of the tile is missing.
+// Registers -> one stage of the ring: the K tile at `kt` (K-major, Q's type),
+// V transposed at `vt` (fp16), the per-token S_k', Z_k', S_v, Z_v' arrays at
+// `sz` (softmax scale folded into the K pair), and at `info` the largest S_v
+// of each half-tile and the two 32-token masks of missing tokens. `tid` is
+// the staging thread (0..127).
 template <int KV, bool QBF>
-__device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV>& r,
-                                           uint32_t base, int tid) {
+__device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV>& r, uint32_t kt,
+                                           uint32_t vt, uint32_t sz, uint32_t info, int tid) {
   using R = RawTile<KV>;
   constexpr int kMid = KV == kI8 ? 128 : 8;
   constexpr int kChunks = R::kRow / 16;
-  if (tid < kTcTok) {
+  if (tid < kTcTok) {  // whole warps: the first two of the staging group
     float Sk = a.sm_scale_log2, Zk = 0.f, Sv = 1.f, Zv = 0.f;
     if constexpr (KvTraits<KV>::kQuant) {
       const float s_k = half_lo(r.ksz), s_v = half_lo(r.vsz);
@@ -234,22 +242,26 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
       Sv = s_v;
       Zv = half_hi(r.vsz) + kMid * s_v;
     }
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(base + kSzOff + 16 * tid), "f"(Sk),
-                 "f"(Zk), "f"(Sv), "f"(Zv)
-                 : "memory");
-    sts32(base + kOkOff + 4 * tid, r.ok ? 1u : 0u);
+    sts32(sz + 4 * tid, __float_as_uint(Sk));
+    sts32(sz + 4 * kTcTok + 4 * tid, __float_as_uint(Zk));
+    sts32(sz + 8 * kTcTok + 4 * tid, __float_as_uint(Sv));
+    sts32(sz + 12 * kTcTok + 4 * tid, __float_as_uint(Zv));
     float mx = Sv;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    if ((tid & 31) == 0) sts32(base + kSvMaxOff + 4 * (tid >> 5), __float_as_uint(mx));
+    const uint32_t miss = __ballot_sync(kFull, r.miss);
+    if ((tid & 31) == 0) {
+      sts32(info + 4 * (tid >> 5), __float_as_uint(mx));
+      sts32(info + 8 + 4 * (tid >> 5), miss);
+    }
   }
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
-    const int e = tid + kTcThreads * i;
+    const int e = tid + kStageThreads * i;
     const int t = e / kChunks, ch = e % kChunks;
     const uint32_t x[4] = {r.k[i].x, r.k[i].y, r.k[i].z, r.k[i].w};
     if constexpr (KV == kF16) {
-      sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
+      sts128(kt + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
     } else if constexpr (KV == kI8) {
       // c - 128 exactly: fp16 by a byte permute into 1024 + c and one packed
       // subtract; bf16 through fp32
@@ -265,8 +277,7 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
             v[q] = bytes_to_f16(word, (q & 1) ? 0x4342u : 0x4140u);
           }
         }
-        sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 16 * ch + 8 * hf), v[0], v[1], v[2],
-               v[3]);
+        sts128(kt + umma_kmajor_offset(kTcTok, t, 16 * ch + 8 * hf), v[0], v[1], v[2], v[3]);
       }
     } else {
 #pragma unroll
@@ -277,8 +288,7 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
           const uint32_t byte = (x[qt] >> (8 * q)) & 0xFF;
           v[q] = centred_pair<QBF>(byte & 0xF, byte >> 4, kMid);
         }
-        sts128(base + kKOff + umma_kmajor_offset(kTcTok, t, 32 * ch + 8 * qt), v[0], v[1], v[2],
-               v[3]);
+        sts128(kt + umma_kmajor_offset(kTcTok, t, 32 * ch + 8 * qt), v[0], v[1], v[2], v[3]);
       }
     }
   }
@@ -295,32 +305,414 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
       lo[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x5410u);
       hi[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x7632u);
     }
-    sts128(base + kVOff + umma_kmajor_offset(128, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2],
-           lo[3]);
-    sts128(base + kVOff + umma_kmajor_offset(128, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1],
-           hi[2], hi[3]);
+    sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2], lo[3]);
+    sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1], hi[2], hi[3]);
   }
 }
 
-// Bounded wait on an mbarrier phase by every thread, with one verdict for the
-// whole CTA.
-__device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
-  return __syncthreads_and(ok ? 1 : 0) != 0;
+// ---- waits --------------------------------------------------------------------
+
+// One thread's bounded wait on a barrier phase that also gives up when another
+// role has aborted the CTA (the flag at `abort_flag`); on its own timeout it
+// sets the flag and reports KVQ_DEV_ERR_TIMEOUT.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, int32_t* dev_err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      report(dev_err, KVQ_DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// The same for a whole warp, with one verdict for all its lanes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* dev_err) {
+  const bool ok = wait_or_abort(bar, parity, abort_flag, dev_err);
+  return __all_sync(kFull, ok);
+}
+
+__device__ __forceinline__ void mbar_init_count(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_one(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait;
+// the second half passes through an empty asm placed after the wait so that no
+// use of it can move above the wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]),
+          "=r"(r[32 * h + 4]), "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]),
+          "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]), "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]),
+          "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]), "=r"(r[32 * h + 14]),
+          "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]),
+          "=r"(r[32 * h + 21]), "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]),
+          "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]), "=r"(r[32 * h + 26]),
+          "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32u * h));
+  }
+  // the wait, tied to the first half's registers
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+  asm volatile(""
+               : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]),
+                 "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]),
+                 "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]),
+                 "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+                 "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]),
+                 "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- work units -----------------------------------------------------------------
+
+struct TcUnit {
+  int b, h, qt, ntiles;
+  TcReq s;
+};
+
+// Unit u: request b (by the prefix sums of units per request), kv head h and
+// 256-row tile qt (longest first), with the number of 64-token context tiles
+// its last query attends.
+__device__ __forceinline__ TcUnit tc_unit(const ExtendArgs& a, const int32_t* ucum, int u) {
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ucum[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  TcUnit w;
+  w.b = lo;
+  w.s = tc_req(a, lo);
+  const int r = u - ucum[lo];
+  w.h = r % a.kv_heads;
+  w.qt = w.s.tiles - 1 - r / a.kv_heads;
+  const int i_max = min(w.s.C - 1, (w.qt * kUnitRows + kUnitRows - 1) / a.group);
+  const int n_tok = w.s.L - w.s.C + i_max + 1;
+  w.ntiles = (n_tok + kTcTok - 1) / kTcTok;
+  return w;
+}
+
+struct TcShared {
+  uint32_t base, tmem;
+  volatile int* abort_flag;
+  volatile int* unit_slot;
+  const int32_t* ucum;
+  int total;
+  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return base + kBarOff + 8u * i; }
+};
+
+// ---- roles ------------------------------------------------------------------------
+
+// Staging warpgroup: hands out the units and fills the K/V ring.
+template <int KV, bool QBF>
+__device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared& c, int tid) {
+  const int lane = tid & 31;
+  uint32_t tc = 0;  // tiles staged so far
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t slot = k & 1u;
+    if (tid == 0) {
+      // the slot of unit k - 2 must have been read by all 13 warps
+      if (k < 2 || wait_or_abort(c.bar(kBarUnitEmpty + slot), ((k >> 1) - 1u) & 1u, c.abort_flag,
+                                 a.dev_err)) {
+        c.unit_slot[slot] = atomicAdd(a.counter, 1);
+        mbar_arrive_one(c.bar(kBarUnitFull + slot));
+      }
+    }
+    __syncwarp();
+    if (!warp_wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u, c.abort_flag, a.dev_err)) return;
+    const int u = c.unit_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
+    if (u >= c.total) return;
+    const TcUnit w = tc_unit(a, c.ucum, u);
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks;
+    RawTile<KV> raw;
+    load_tile<KV>(a, bt, 0, w.s.L, w.h, tid, raw);
+    for (int j = 0; j < w.ntiles; ++j, ++tc) {
+      const uint32_t st = tc & 1u, use = tc >> 1;
+      if (use > 0 &&
+          !warp_wait(c.bar(kBarKvEmpty + st), (use - 1u) & 1u, c.abort_flag, a.dev_err))
+        return;
+      store_tile<KV, QBF>(a, raw, c.base + kKOff + st * kKBytes, c.base + kVOff + st * kVBytes,
+                          c.base + kSzOff + st * kSzBytes, c.base + kInfoOff + st * 16u, tid);
+      fence_async_smem();
+      mbar_arrive_one(c.bar(kBarKvFull + st));
+      if (j + 1 < w.ntiles) load_tile<KV>(a, bt, (j + 1) * kTcTok, w.s.L, w.h, tid, raw);
+    }
+  }
+}
+
+// The MMA thread.
+template <bool QBF>
+__device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c) {
+  constexpr uint32_t idesc_s = umma_idesc_f16(QBF, kWgRows, kTcTok);
+  constexpr uint32_t idesc_o = umma_idesc_f16(false, kWgRows, kHeadDim);
+  auto issue_s = [&](int g, uint32_t st) {
+    const uint32_t qa = c.base + kQOff + g * kQBytes, ka = c.base + kKOff + st * kKBytes;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      umma_f16(c.tmem + 64u * g,
+               umma_desc_sw128(qa + (k >> 2) * (kWgRows * 128) + (k & 3) * 32, 1024),
+               umma_desc_sw128(ka + (k >> 2) * (kTcTok * 128) + (k & 3) * 32, 1024), idesc_s,
+               k > 0);
+    umma_commit(c.bar(kBarSFull + g));
+  };
+  auto issue_o = [&](int g, uint32_t st, bool acc) {
+    const uint32_t pa = c.base + kPOff + g * kPBytes, va = c.base + kVOff + st * kVBytes;
+#pragma unroll
+    for (int k = 0; k < kTcTok / 16; ++k)
+      umma_f16(c.tmem + 128u + 128u * g, umma_desc_sw128(pa + k * 32, 1024),
+               umma_desc_sw128(va + k * 32, 1024), idesc_o, acc || k > 0);
+    umma_commit(c.bar(kBarODone + g));
+  };
+  auto wait = [&](uint32_t b, uint32_t parity) {
+    const bool ok = wait_or_abort(b, parity, c.abort_flag, a.dev_err);
+    tc_fence_after();
+    return ok;
+  };
+  uint32_t tc = 0;  // tiles issued so far
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t slot = k & 1u;
+    if (!wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u)) return;
+    const int u = c.unit_slot[slot];
+    mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
+    if (u >= c.total) return;
+    const int n = tc_unit(a, c.ucum, u).ntiles;
+    if (!wait(c.bar(kBarQFull + 0), k & 1u) || !wait(c.bar(kBarQFull + 1), k & 1u)) return;
+    if (!wait(c.bar(kBarKvFull + (tc & 1u)), (tc >> 1) & 1u)) return;
+    issue_s(0, tc & 1u);
+    issue_s(1, tc & 1u);
+    for (int j = 0; j < n; ++j, ++tc) {
+      const uint32_t st = tc & 1u;
+      const bool more = j + 1 < n;
+      if (!wait(c.bar(kBarPFull + 0), tc & 1u)) return;
+      issue_o(0, st, j > 0);
+      if (more) {
+        if (!wait(c.bar(kBarKvFull + (st ^ 1u)), ((tc + 1u) >> 1) & 1u)) return;
+        issue_s(0, st ^ 1u);
+      }
+      if (!wait(c.bar(kBarPFull + 1), tc & 1u)) return;
+      issue_o(1, st, j > 0);
+      umma_commit(c.bar(kBarKvEmpty + st));  // the stage is free once these products finish
+      if (more) issue_s(1, st ^ 1u);
+    }
+  }
+}
+
+// A softmax warpgroup: warps 4 g .. 4 g + 3, one thread per row i of the
+// unit's half g.
+template <int KV, bool QBF>
+__device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared& c, int g,
+                                             int i, int warp) {
+  constexpr bool kQuant = KvTraits<KV>::kQuant;
+  const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  const uint32_t s_addr = lane_addr + 64u * g, o_addr = lane_addr + 128u + 128u * g;
+  const uint32_t q_tile = c.base + kQOff + g * kQBytes, p_tile = c.base + kPOff + g * kPBytes;
+  const int lane = i & 31;
+  auto wait = [&](uint32_t b, uint32_t parity) {
+    return warp_wait(b, parity, c.abort_flag, a.dev_err);
+  };
+  uint32_t tc = 0;
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t slot = k & 1u;
+    if (!wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u)) return;
+    const int u = c.unit_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
+    if (u >= c.total) return;
+    const TcUnit w = tc_unit(a, c.ucum, u);
+    const int row = w.qt * kUnitRows + g * kWgRows + i;
+    const int qi = row / a.group;
+    const int hq = w.h * a.group + row % a.group;
+    const bool valid = qi < w.s.C;
+    const int pos = w.s.L - w.s.C + qi;
+
+    // Q row of this thread into the K-major tile (zeros for a padding row)
+    float qsum = 0.f;
+    {
+      const uint4* qp = reinterpret_cast<const uint4*>(
+          static_cast<const uint16_t*>(a.q) +
+          ((static_cast<int64_t>(w.s.q0) + qi) * a.q_heads + hq) * kHeadDim);
+#pragma unroll 4
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 x = valid ? qp[ch] : make_uint4(0u, 0u, 0u, 0u);
+        sts128(q_tile + umma_kmajor_offset(kWgRows, i, 8 * ch), x.x, x.y, x.z, x.w);
+        if constexpr (kQuant) {
+          qsum += lo_to_float<QBF>(x.x) + hi_to_float<QBF>(x.x) + lo_to_float<QBF>(x.y) +
+                  hi_to_float<QBF>(x.y) + lo_to_float<QBF>(x.z) + hi_to_float<QBF>(x.z) +
+                  lo_to_float<QBF>(x.w) + hi_to_float<QBF>(x.w);
+        }
+      }
+    }
+    fence_async_smem();
+    mbar_arrive_one(c.bar(kBarQFull + g));
+
+    const float2 qs2 = make_float2(qsum, qsum);
+    float m = -INFINITY;
+    float2 l2 = make_float2(0.f, 0.f), z2 = make_float2(0.f, 0.f);
+    for (int j = 0; j < w.ntiles; ++j, ++tc) {
+      const uint32_t st = tc & 1u;
+      if (!wait(c.bar(kBarSFull + g), tc & 1u)) return;
+      // the stage's scale arrays (already complete: S was computed from it)
+      if (!wait(c.bar(kBarKvFull + st), (tc >> 1) & 1u)) return;
+      tc_fence_after();
+      const uint32_t sz = c.base + kSzOff + st * kSzBytes;
+      float x[kTcTok];
+      tmem_ld64(s_addr, x);
+      // s = S_k' raw + Z_k' sum(q) (softmax scale folded in), two tokens per
+      // instruction
+#pragma unroll
+      for (int q = 0; q < kTcTok / 4; ++q) {
+        const float4 sk = lds_f4(sz + 16 * q), zk = lds_f4(sz + 4 * kTcTok + 16 * q);
+        const float2 b0 = __fmul2_rn(make_float2(zk.x, zk.y), qs2);
+        const float2 b1 = __fmul2_rn(make_float2(zk.z, zk.w), qs2);
+        const float2 r0 = __ffma2_rn(make_float2(sk.x, sk.y), make_float2(x[4 * q], x[4 * q + 1]), b0);
+        const float2 r1 =
+            __ffma2_rn(make_float2(sk.z, sk.w), make_float2(x[4 * q + 2], x[4 * q + 3]), b1);
+        x[4 * q] = r0.x;
+        x[4 * q + 1] = r0.y;
+        x[4 * q + 2] = r1.x;
+        x[4 * q + 3] = r1.y;
+      }
+      // positions past the row's own, and missing tokens, are masked
+      const int tok0 = j * kTcTok;
+      if (tok0 + kTcTok - 1 > pos) {
+#pragma unroll
+        for (int t = 0; t < kTcTok; ++t)
+          if (tok0 + t > pos) x[t] = -INFINITY;
+      }
+      const float4 info = lds_f4(c.base + kInfoOff + st * 16u);
+      const uint32_t miss0 = __float_as_uint(info.z), miss1 = __float_as_uint(info.w);
+      if ((miss0 | miss1) != 0u) {
+#pragma unroll
+        for (int t = 0; t < kTcTok; ++t)
+          if (((t < 32 ? miss0 : miss1) >> (t & 31)) & 1u) x[t] = -INFINITY;
+      }
+      float bm = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kTcTok; t += 2) bm = fmaxf(bm, fmaxf(x[t], x[t + 1]));
+      // the reference maximum moves only when a score exceeds it by more than
+      // tau (log2 units): p <= 2^tau then, and P' = p S_v stays within fp16
+      // when the tile's largest V scale is at most 240 (else tau = 0: exact)
+      const float tau = fmaxf(info.x, info.y) <= 240.f ? 8.f : 0.f;
+      const float mn = (m == -INFINITY || bm > m + tau) ? fmaxf(m, bm) : m;
+      const float al = (m == -INFINITY || mn == m) ? 1.f : ex2(m - mn);
+      if (j > 0) {
+        // O_g of the previous tile is complete (its P' buffer is free again)
+        if (!wait(c.bar(kBarODone + g), (tc - 1u) & 1u)) return;
+        tc_fence_after();
+        if (__any_sync(kFull, al != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float v[32];
+            tmem_ld32(o_addr + 32 * cc, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] *= al;
+            tmem_st32(o_addr + 32 * cc, v);
+          }
+        }
+      }
+      const float2 al2 = make_float2(al, al);
+      l2 = __fmul2_rn(l2, al2);
+      z2 = __fmul2_rn(z2, al2);
+      m = mn;
+      const float nref = m == -INFINITY ? 0.f : -m;
+      const float2 nref2 = make_float2(nref, nref);
+      // P' = p S_v (quantized) or p, fp16, into this row of the P' tile
+#pragma unroll
+      for (int c8 = 0; c8 < kTcTok / 8; ++c8) {
+        const float4 sva = lds_f4(sz + 8 * kTcTok + 32 * c8),
+                     svb = lds_f4(sz + 8 * kTcTok + 32 * c8 + 16);
+        const float4 zva = lds_f4(sz + 12 * kTcTok + 32 * c8),
+                     zvb = lds_f4(sz + 12 * kTcTok + 32 * c8 + 16);
+        const float2 sv[4] = {make_float2(sva.x, sva.y), make_float2(sva.z, sva.w),
+                              make_float2(svb.x, svb.y), make_float2(svb.z, svb.w)};
+        const float2 zv[4] = {make_float2(zva.x, zva.y), make_float2(zva.z, zva.w),
+                              make_float2(zvb.x, zvb.y), make_float2(zvb.z, zvb.w)};
+        uint32_t wd[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int t0 = 8 * c8 + 2 * q;
+          const float2 d = __fadd2_rn(make_float2(x[t0], x[t0 + 1]), nref2);
+          const float2 p = make_float2(ex2(d.x), ex2(d.y));
+          l2 = __fadd2_rn(l2, p);
+          if constexpr (kQuant) {
+            z2 = __ffma2_rn(p, zv[q], z2);
+            const float2 v = __fmul2_rn(p, sv[q]);
+            wd[q] = pack2<false>(v.x, v.y);
+          } else {
+            wd[q] = pack2<false>(p.x, p.y);
+          }
+        }
+        sts128(p_tile + umma_kmajor_offset(kWgRows, i, 8 * c8), wd[0], wd[1], wd[2], wd[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive_one(c.bar(kBarPFull + g));
+    }
+    // output row: (O + z) / l (every lane takes part in the TMEM reads)
+    if (!wait(c.bar(kBarODone + g), (tc - 1u) & 1u)) return;
+    tc_fence_after();
+    {
+      const float l = l2.x + l2.y, z = z2.x + z2.y;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(
+          static_cast<uint16_t*>(a.out) +
+          ((static_cast<int64_t>(w.s.q0) + qi) * a.q_heads + hq) * kHeadDim);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(o_addr + 32 * cc, v);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t wd[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wd[e] = pack2<QBF>((v[8 * q + 2 * e] + z) * inv, (v[8 * q + 2 * e + 1] + z) * inv);
+            dst[4 * cc + q] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
 }
 
 template <int KV, bool QBF>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    extend_tc_kernel(const __grid_constant__ ExtendArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendArgs a) {
   extern __shared__ __align__(1024) unsigned char dsmem[];
   __shared__ int32_t warp_sum[kTcThreads / 32];
-  constexpr bool kQuant = KvTraits<KV>::kQuant;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t base = (static_cast<uint32_t>(__cvta_generic_to_shared(dsmem)) + 1023u) & ~1023u;
-  int32_t* ucum = reinterpret_cast<int32_t*>(dsmem + (base - static_cast<uint32_t>(
-                                                          __cvta_generic_to_shared(dsmem))) +
-                                             kFixedBytes);
-  const uint32_t bar_s = base + kBarOff, bar_o = base + kBarOff + 8;
+  const uint32_t raw_base = static_cast<uint32_t>(__cvta_generic_to_shared(dsmem));
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  unsigned char* gbase = dsmem + (base - raw_base);
+  int32_t* ucum = reinterpret_cast<int32_t*>(gbase + kFixedBytes);
 
   // ---- work units per request, prefix-summed ----------------------------------
   {
@@ -349,230 +741,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (tid == kTcThreads - 1) ucum[a.batch] = basec + incl;
   }
+  TcShared c;
+  c.base = base;
+  c.abort_flag = reinterpret_cast<volatile int*>(gbase + kAbortOff);
+  c.unit_slot = reinterpret_cast<volatile int*>(gbase + kUnitOff);
+  c.ucum = ucum;
   if (tid == 0) {
-    mbar_init(bar_s);
-    mbar_init(bar_o);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init_count(c.bar(kBarKvFull + s), kStageThreads);
+      mbar_init_count(c.bar(kBarKvEmpty + s), 1);
+      mbar_init_count(c.bar(kBarSFull + s), 1);
+      mbar_init_count(c.bar(kBarPFull + s), kWgRows);
+      mbar_init_count(c.bar(kBarODone + s), 1);
+      mbar_init_count(c.bar(kBarQFull + s), kWgRows);
+      mbar_init_count(c.bar(kBarUnitFull + s), 1);
+      mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 1);  // every warp's lane 0
+    }
+    mbar_init_count(c.bar(kBarDrain), 1);
+    *c.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(base + kSlotOff, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  uint32_t tmem;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + kSlotOff));
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-  const int total = ucum[a.batch];
-  __shared__ int unit_s;
-  uint32_t ns = 0, no = 0;  // completed phases of bar_s and bar_o
-  bool alive = true;
-  uint32_t failed_bar = 0, failed_parity = 0;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c.tmem) : "r"(base + kSlotOff));
+  c.total = ucum[a.batch];
 
-  for (;;) {
-    if (tid == 0) unit_s = atomicAdd(a.counter, 1);
-    __syncthreads();
-    const int u = unit_s;
-    __syncthreads();
-    if (u >= total) break;
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ucum[mid] <= u) lo = mid; else hi = mid - 1;
-    }
-    const int b = lo;
-    const TcReq s = tc_req(a, b);
-    const int r = u - ucum[b];
-    const int h = r % a.kv_heads;
-    const int qt = s.tiles - 1 - r / a.kv_heads;  // longest tiles first
-    const int row = qt * kTcRows + tid;
-    const int qi = row / a.group;
-    const int hq = h * a.group + row % a.group;
-    const bool valid = qi < s.C;
-    const int pos = s.L - s.C + qi;
-    const int i_max = min(s.C - 1, (qt * kTcRows + kTcRows - 1) / a.group);
-    const int n_tok = s.L - s.C + i_max + 1;  // context the tile attends
-    const int ntiles = (n_tok + kTcTok - 1) / kTcTok;
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks;
-
-    // Q row of this thread into the K-major tile (zeros for a padding row)
-    float qsum = 0.f;
-    {
-      const uint4* qp = reinterpret_cast<const uint4*>(
-          static_cast<const uint16_t*>(a.q) +
-          ((static_cast<int64_t>(s.q0) + qi) * a.q_heads + hq) * kHeadDim);
-#pragma unroll 4
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint4 w = valid ? qp[ch] : make_uint4(0u, 0u, 0u, 0u);
-        sts128(base + kQOff + umma_kmajor_offset(kTcRows, tid, 8 * ch), w.x, w.y, w.z, w.w);
-        if constexpr (kQuant) {
-          qsum += lo_to_float<QBF>(w.x) + hi_to_float<QBF>(w.x) + lo_to_float<QBF>(w.y) +
-                  hi_to_float<QBF>(w.y) + lo_to_float<QBF>(w.z) + hi_to_float<QBF>(w.z) +
-                  lo_to_float<QBF>(w.w) + hi_to_float<QBF>(w.w);
-        }
-      }
-    }
-    float m = -INFINITY, l = 0.f, z = 0.f;
-
-    RawTile<KV> raw;
-    load_tile<KV>(a, bt, 0, s.L, h, tid, raw);
-    for (int j = 0; j < ntiles && alive; ++j) {
-      store_tile<KV, QBF>(a, raw, base, tid);
-      // the tile's missing tokens (rare: block ids outside the pool)
-      const bool holes = __syncthreads_or(tid < kTcTok && !raw.ok &&
-                                          j * kTcTok + tid < s.L) != 0;
-      if (j + 1 < ntiles) load_tile<KV>(a, bt, (j + 1) * kTcTok, s.L, h, tid, raw);
-      fence_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t idesc_s = umma_idesc_f16(QBF, kTcRows, kTcTok);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_f16(tmem, umma_desc_sw128(base + kQOff + (k >> 2) * (kTcRows * 128) + (k & 3) * 32,
-                                         1024),
-                   umma_desc_sw128(base + kKOff + (k >> 2) * (kTcTok * 128) + (k & 3) * 32, 1024),
-                   idesc_s, k > 0);
-        umma_commit(bar_s);
-      }
-      if (!cta_wait(bar_s, ns & 1u)) {
-        alive = false;
-        failed_bar = bar_s;
-        failed_parity = ns & 1u;
-        break;
-      }
-      ++ns;
-      tc_fence_after();
-      // this row's scores, scaled, masked, in the exp2 domain
-      float sc[kTcTok];
-      {
-        float v[32];
-        tmem_ld32(lane_base, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = v[i];
-        tmem_ld32(lane_base + 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[32 + i] = v[i];
-      }
-      // s = S_k' raw + Z_k' sum(q) (scale folded in); positions past the row's
-      // own, and missing tokens, are masked
-      float bm = -INFINITY;
-      const bool diag = j * kTcTok + kTcTok - 1 > pos;
-#pragma unroll
-      for (int i = 0; i < kTcTok; ++i) {
-        const float2 kz = lds_f2(base + kSzOff + 16 * i);
-        float x = kz.x * sc[i] + kz.y * qsum;
-        if (diag && j * kTcTok + i > pos) x = -INFINITY;
-        sc[i] = x;
-        bm = fmaxf(bm, x);
-      }
-      if (holes) {
-        bm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kTcTok; ++i) {
-          if (lds_u32(base + kOkOff + 4 * i) == 0u) sc[i] = -INFINITY;
-          bm = fmaxf(bm, sc[i]);
-        }
-      }
-      // the reference maximum moves only when a score exceeds it by more than
-      // tau (log2 units): p <= 2^tau then, and P' = p S_v stays within fp16
-      // when the tile's largest V scale is at most 240 (else tau = 0: exact)
-      const float sv_max = fmaxf(__uint_as_float(lds_u32(base + kSvMaxOff)),
-                                 __uint_as_float(lds_u32(base + kSvMaxOff + 4)));
-      const float tau = sv_max <= 240.f ? 8.f : 0.f;
-      const float mn = (m == -INFINITY || bm > m + tau) ? fmaxf(m, bm) : m;
-      const float al = (m == -INFINITY || mn == m) ? 1.f : ex2(m - mn);
-      // rescale this warp's rows of O when some row's maximum moved
-      if (j > 0 && __any_sync(kFull, al != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(lane_base + 64 + 32 * c, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= al;
-          tmem_st32(lane_base + 64 + 32 * c, v);
-        }
-      }
-      l *= al;
-      z *= al;
-      m = mn;
-      const float ref = m == -INFINITY ? 0.f : m;
-      // P' = p S_v (quantized) or p, fp16, into this row of the P tile
-#pragma unroll
-      for (int c8 = 0; c8 < kTcTok / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i0 = 8 * c8 + 2 * q;
-          const float p0 = ex2(sc[i0] - ref), p1 = ex2(sc[i0 + 1] - ref);
-          l += p0 + p1;
-          float v0 = p0, v1 = p1;
-          if constexpr (kQuant) {
-            const float4 s0 = lds_f4(base + kSzOff + 16 * i0);
-            const float4 s1 = lds_f4(base + kSzOff + 16 * i0 + 16);
-            z += p0 * s0.w + p1 * s1.w;
-            v0 = p0 * s0.z;
-            v1 = p1 * s1.z;
-          }
-          w[q] = pack2<false>(v0, v1);
-        }
-        sts128(base + kPOff + umma_kmajor_offset(kTcRows, tid, 8 * c8), w[0], w[1], w[2], w[3]);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t idesc_o = umma_idesc_f16(false, kTcRows, kHeadDim);
-#pragma unroll
-        for (int k = 0; k < kTcTok / 16; ++k)
-          umma_f16(tmem + 64, umma_desc_sw128(base + kPOff + k * 32, 1024),
-                   umma_desc_sw128(base + kVOff + k * 32, 1024), idesc_o, j > 0 || k > 0);
-        umma_commit(bar_o);
-      }
-      if (!cta_wait(bar_o, no & 1u)) {
-        alive = false;
-        failed_bar = bar_o;
-        failed_parity = no & 1u;
-        break;
-      }
-      ++no;
-      tc_fence_after();
-    }
-    if (!alive) break;
-    // output row: (O + z) / l (every lane takes part in the TMEM reads)
-    {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(
-          static_cast<uint16_t*>(a.out) +
-          ((static_cast<int64_t>(s.q0) + qi) * a.q_heads + hq) * kHeadDim);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(lane_base + 64 + 32 * c, v);
-        if (valid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack2<QBF>((v[8 * q + 2 * e] + z) * inv, (v[8 * q + 2 * e + 1] + z) * inv);
-            dst[4 * c + q] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
+  if (warp < kSoftWarps) {
+    softmax_role<KV, QBF>(a, c, warp >> 2, tid & (kWgRows - 1), warp);
+  } else if (warp < kMmaWarp) {
+    staging_role<KV, QBF>(a, c, tid - kSoftWarps * 32);
+  } else if (lane == 0) {
+    mma_role<QBF>(a, c);
+    // every product this thread issued completes before the TMEM is freed
+    umma_commit(c.bar(kBarDrain));
+    mbar_wait(c.bar(kBarDrain), 0);
   }
-  if (!alive) {
-    if (tid == 0) report(a.dev_err, KVQ_DEV_ERR_TIMEOUT);
-    // the product still in flight: one more bounded wait before freeing TMEM
-    mbar_wait(failed_bar, failed_parity);
-    tc_fence_before();
-    __syncthreads();
-  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(c.tmem, kTmemCols);
   }
 }
 
