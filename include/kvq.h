@@ -318,11 +318,12 @@ kvq_status paged_decode_attn_noalloc(const kvq_pool* pool, const void* q, int32_
  *  variant     : KVQ_EXTEND_AUTO, or a kernel to use:
  *                KVQ_EXTEND_MMA_SYNC (tiles of 16 rows on mma.sync; every pool
  *                kind; cuts long contexts into parts when the batch has few
- *                query tiles) or KVQ_EXTEND_TCGEN05 (tiles of 128 rows on
+ *                query tiles) or KVQ_EXTEND_TCGEN05 (units of 256 rows on
  *                tcgen05 with tensor-memory accumulators; INT8, INT4 and
- *                fp16 pools; KVQ_ERR_UNSUPPORTED otherwise). AUTO takes the
- *                tcgen05 kernel when the pool allows it and the batch has at
- *                least as many 128-row tiles as the device has SMs.
+ *                fp16 pools of at least one block, at most 4096 requests;
+ *                KVQ_ERR_UNSUPPORTED otherwise). AUTO takes the tcgen05 kernel when it accepts
+ *                the call and the batch has at least as many 256-row units
+ *                as the device has SMs.
  *  workspace   : at least *bytes of paged_extend_attn_workspace_size, 16-byte
  *                aligned; nothing in it needs to start at zero.
  * Chunk query i of request b (chunk length C) sits at position

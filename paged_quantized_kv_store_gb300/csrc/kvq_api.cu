@@ -558,8 +558,11 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   if (q_heads % pool->kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (variant < KVQ_EXTEND_AUTO || variant > KVQ_EXTEND_TCGEN05) return KVQ_ERR_INVALID_ARG;
-  if (variant == KVQ_EXTEND_TCGEN05 && !kvq::extend_tc_supported(pool->kv_dtype, q_dtype))
-    return KVQ_ERR_UNSUPPORTED;
+  // the tcgen05 kernel reads a missing block's rows from block 0 (and masks
+  // them), so it needs a pool with at least one block
+  const bool tc_ok = kvq::extend_tc_supported(pool->kv_dtype, q_dtype) &&
+                     batch <= kvq::extend_tc_max_batch() && pool->num_blocks > 0;
+  if (variant == KVQ_EXTEND_TCGEN05 && !tc_ok) return KVQ_ERR_UNSUPPORTED;
   if (batch > kvq::kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0) return KVQ_OK;
   if (q == nullptr || out == nullptr || qo_indptr == nullptr || kv_lens == nullptr ||
@@ -610,8 +613,7 @@ kvq_status paged_extend_attn(const kvq_pool* pool, const void* q, int32_t q_dtyp
   const int64_t tc_units = static_cast<int64_t>(pool->kv_heads) *
                            ((static_cast<int64_t>(total_q) * a.group + 255) / 256);
   const bool use_tc = variant == KVQ_EXTEND_TCGEN05 ||
-                      (variant == KVQ_EXTEND_AUTO &&
-                       kvq::extend_tc_supported(pool->kv_dtype, q_dtype) && tc_units >= sms);
+                      (variant == KVQ_EXTEND_AUTO && tc_ok && tc_units >= sms);
   if (use_tc) {
     // persistent CTAs, one per SM (each holds all 512 TMEM columns)
     if (kvq::extend_tc_ctas_per_sm(pool->kv_dtype, q_dtype, batch) <= 0) return KVQ_ERR_CUDA;

@@ -12,11 +12,12 @@
 //     (dims as rows), into a two-stage ring, with the per-token scale S and
 //     shifted zero Z + mid S in four small arrays; it also hands out the work
 //     units (an atomic counter, longest tiles first);
-//   * MMA thread (warp 12, lane 0): for each tile issues S_g = Q_g K^T
-//     (M 128, N 64, K 128) for both softmax warpgroups into their own TMEM
-//     columns, and O_g += P'_g V (M 128, N 128, K 64) as soon as warpgroup
-//     g's P' is ready, so the tensor core works on one warpgroup's products
-//     while the other runs its softmax (ping-pong);
+//   * MMA thread (warp 12, lane 0): issues S_g = Q_g K^T (M 128, N 64,
+//     K 128) for both softmax warpgroups into their own TMEM columns, the
+//     next tile's S_g as soon as warpgroup g has read the current one out of
+//     TMEM (so it runs during that warpgroup's exponentials), and
+//     O_g += P'_g V (M 128, N 128, K 64) as soon as warpgroup g's P' is
+//     ready; the two warpgroups' products interleave on the tensor core;
 //   * two softmax warpgroups (warps 0-3, 4-7), one thread per row: read the
 //     row of S (tcgen05.ld), apply s = S_k (q.(c - mid)) + (Z_k + mid S_k)
 //     sum(q), the causal mask and the online softmax; when the running
@@ -45,10 +46,17 @@ constexpr int kTcTok = 64;                // tokens per context tile (N of S, K 
 constexpr int kStageThreads = 128;        // staging warpgroup
 constexpr int kSoftWarps = 8;             // warps 0-7: softmax warpgroups 0 and 1
 constexpr int kMmaWarp = 12;              // warps 8-11 stage, warp 12 issues the MMAs
-constexpr int kTcThreads = 13 * 32;
+constexpr int kTcThreads = 16 * 32;       // four warpgroups; warps 13-15 only hold registers
+// Registers per thread after the split (setmaxnreg): the launch gives every
+// thread 65536 / 512 = 128; the staging and MMA warpgroups give theirs back
+// down to kLowRegs, the softmax warpgroups take them up to kHighRegs.
+constexpr uint32_t kLowRegs = 120, kHighRegs = 136;
+static_assert(2 * kLowRegs + 2 * kHighRegs == 4 * (65536 / kTcThreads),
+              "the split must add up to the launch's registers");
 constexpr uint32_t kTmemCols = 512;       // S_g: columns 64 g .. 64 g + 63; O_g: 128 + 128 g ..
 
 // shared memory, offsets from a 1024-byte aligned base
+constexpr int kStages = 3;                          // K/V ring depth (tiles)
 constexpr uint32_t kQBytes = kWgRows * 256;         // 2 column blocks of 128 rows x 128 B
 constexpr uint32_t kKBytes = kTcTok * 256;          // 2 column blocks of 64 rows x 128 B
 constexpr uint32_t kVBytes = 128 * kTcTok * 2;      // 128 dims x 64 tokens
@@ -56,26 +64,29 @@ constexpr uint32_t kPBytes = kWgRows * kTcTok * 2;  // 128 rows x 64 tokens
 constexpr uint32_t kSzBytes = 4 * kTcTok * 4;       // S_k'[64] Z_k'[64] S_v[64] Z_v'[64]
 constexpr uint32_t kQOff = 0;                       // Q of warpgroup g at g * kQBytes
 constexpr uint32_t kKOff = kQOff + 2 * kQBytes;     // K tile of stage s at s * kKBytes
-constexpr uint32_t kVOff = kKOff + 2 * kKBytes;
-constexpr uint32_t kPOff = kVOff + 2 * kVBytes;     // P' of warpgroup g
+constexpr uint32_t kVOff = kKOff + kStages * kKBytes;
+constexpr uint32_t kPOff = kVOff + kStages * kVBytes;  // P' of warpgroup g
 constexpr uint32_t kSzOff = kPOff + 2 * kPBytes;
-constexpr uint32_t kInfoOff = kSzOff + 2 * kSzBytes;  // per stage: max S_v (2 halves), missing masks
-constexpr uint32_t kBarOff = kInfoOff + 2 * 16;
-// mbarriers (index: pairs by stage or warpgroup)
-constexpr uint32_t kBarKvFull = 0;     // staging -> MMA, softmax (128 arrivals)
-constexpr uint32_t kBarKvEmpty = 2;    // MMA commit: the stage's products are done
-constexpr uint32_t kBarSFull = 4;      // MMA commit: S_g is in TMEM
-constexpr uint32_t kBarPFull = 6;      // softmax g -> MMA (128 arrivals)
-constexpr uint32_t kBarODone = 8;      // MMA commit: O_g += P'_g V done
-constexpr uint32_t kBarQFull = 10;     // softmax g -> MMA: the unit's Q rows (128 arrivals)
-constexpr uint32_t kBarUnitFull = 12;  // unit slot written
-constexpr uint32_t kBarUnitEmpty = 14; // unit slot read by all 13 warps
-constexpr uint32_t kBarDrain = 16;     // MMA commit before TMEM is freed
-constexpr uint32_t kNumBars = 17;
+constexpr uint32_t kInfoOff = kSzOff + kStages * kSzBytes;  // per stage: max S_v (2 halves), missing masks
+constexpr uint32_t kBarOff = kInfoOff + kStages * 16;
+// mbarriers (index: runs by stage or warpgroup)
+constexpr uint32_t kBarKvFull = 0;     // staging -> MMA, softmax (128 arrivals), per stage
+constexpr uint32_t kBarKvEmpty = 3;    // MMA commit: the stage's products are done
+constexpr uint32_t kBarSFull = 6;      // MMA commit: S_g is in TMEM
+constexpr uint32_t kBarPFull = 8;      // softmax g -> MMA (128 arrivals)
+constexpr uint32_t kBarODone = 10;     // MMA commit: O_g += P'_g V done
+constexpr uint32_t kBarQFull = 12;     // softmax g -> MMA: the unit's Q rows (128 arrivals)
+constexpr uint32_t kBarUnitFull = 14;  // unit slot written
+constexpr uint32_t kBarUnitEmpty = 16; // unit slot read by all 13 working warps
+constexpr uint32_t kBarSRead = 18;     // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
+constexpr uint32_t kBarDrain = 20;     // MMA commit before TMEM is freed
+constexpr uint32_t kNumBars = 21;
 constexpr uint32_t kSlotOff = kBarOff + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kUnitOff = kSlotOff + 4;            // 2 unit slots
 constexpr uint32_t kAbortOff = kUnitOff + 8;
 constexpr uint32_t kFixedBytes = kAbortOff + 4;
+// requests per launch (their unit prefix sums live in shared memory)
+constexpr int kTcMaxBatch = 4096;
 
 __host__ __device__ constexpr size_t tc_smem_bytes(int batch) {
   return 1024 + kFixedBytes + align128((batch + 1) * sizeof(int32_t));
@@ -133,92 +144,119 @@ struct RawTile {
   uint4 k[kKChunks];
   uint32_t v[8][kVWords];
   uint32_t ksz, vsz;
-  bool miss;  // token `tid` of the tile is in the context but its block id is outside the pool
+  bool sz_ok;  // token `tid` is in the context and its block in the pool
+  bool miss;   // token `tid` of the tile is in the context but its block id is outside the pool
 };
 
-// Global row (token t of the tile, kv head h) of a pool, or null when the
-// token is past the context or its block id is outside the pool.
+// The K chunk (16 bytes of codes: token t of the tile, chunk ch of its row)
+// that staging item e (= thread + 128 i) moves. Eight neighbouring lanes take
+// 2 tokens x 4 chunks (INT8), 4 x 2 (INT4) or 1 x 8 (fp16): under the 128-byte
+// swizzle their 16-byte stores then land in eight different bank groups, and
+// a warp still reads whole token rows.
 template <int KV>
-__device__ __forceinline__ const uint8_t* tc_row(const ExtendArgs& a, const int32_t* bt,
-                                                 const uint8_t* pool, int tt, int L, int h) {
-  constexpr int kRow = KvTraits<KV>::kRowBytes;
-  if (tt >= L) return nullptr;
-  const int32_t blk = bt[tt / kBlock];
-  if (blk < 0 || blk >= a.num_blocks) return nullptr;
-  return pool + ((static_cast<int64_t>(blk) * kBlock + tt % kBlock) * a.kv_heads + h) * kRow;
+__device__ __forceinline__ void k_item(int e, int& t, int& ch) {
+  constexpr int kChunks = RawTile<KV>::kRow / 16;  // 8 / 4 / 16 per token row
+  constexpr int kCpg = kChunks / 2;                // chunks per lane group of 8
+  constexpr int kTpg = 8 / kCpg;                   // tokens per lane group
+  const int lane8 = e & 7, grp = e >> 3;
+  t = kTpg * (grp >> 1) + lane8 / kCpg;
+  ch = kCpg * (grp & 1) + lane8 % kCpg;
 }
 
+// Table entries of the tile's four blocks (tokens tok0 .. tok0 + 63). The
+// index is clamped to the table row, so the loads are unconditional; an entry
+// of a block past the context is ignored where it is used. Staging fetches
+// them a tile ahead.
+__device__ __forceinline__ int4 tile_blocks(const int32_t* bt, int tok0, int max_blocks) {
+  const int b0 = tok0 / kBlock, last = max_blocks - 1;
+  int4 r;
+  r.x = __ldg(bt + min(b0, last));
+  r.y = __ldg(bt + min(b0 + 1, last));
+  r.z = __ldg(bt + min(b0 + 2, last));
+  r.w = __ldg(bt + min(b0 + 3, last));
+  return r;
+}
+
+__device__ __forceinline__ int pick4(const int4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+// Block of tile token t: its id when the block is inside the context and the
+// pool (ok), else 0 -- an address that is safe to read. Codes read from
+// there, and from the context's last block past its length, are never used:
+// those tokens are masked (p = 0), and their scale/zero words are zeroed.
+__device__ __forceinline__ int64_t safe_block(const ExtendArgs& a, const int4& blks, int t,
+                                              int tok0, int L, bool& ok) {
+  const int32_t blk = pick4(blks, t / kBlock);
+  ok = tok0 + (t & ~(kBlock - 1)) < L && blk >= 0 && blk < a.num_blocks;
+  return ok ? blk : 0;
+}
+
+// Issues the global loads of tile tok0 (table entries in `blks`) into r; no
+// instruction here waits for their data.
 template <int KV>
-__device__ __forceinline__ void load_tile(const ExtendArgs& a, const int32_t* bt, int tok0, int L,
+__device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks, int tok0, int L,
                                           int h, int tid, RawTile<KV>& r) {
   using R = RawTile<KV>;
-  constexpr int kChunks = R::kRow / 16;
+  const int64_t head_row = static_cast<int64_t>(a.kv_heads) * R::kRow;  // one token
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
-    const int e = tid + kStageThreads * i;
-    const uint8_t* src = tc_row<KV>(a, bt, a.k, tok0 + e / kChunks, L, h);
-    r.k[i] = src ? __ldg(reinterpret_cast<const uint4*>(src) + e % kChunks)
-                 : make_uint4(0u, 0u, 0u, 0u);
+    int t, ch;
+    k_item<KV>(tid + kStageThreads * i, t, ch);
+    bool ok;
+    const int64_t blk = safe_block(a, blks, t, tok0, L, ok);
+    const uint8_t* src = a.k + (blk * kBlock + t % kBlock) * head_row + h * R::kRow;
+    r.k[i] = __ldg(reinterpret_cast<const uint4*>(src) + ch);
   }
   // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
   const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
-  const int tv = tok0 + 8 * tg;
-  const int32_t vblk = tv < L ? bt[tv / kBlock] : -1;
-  const bool vok = vblk >= 0 && vblk < a.num_blocks;
+  const int tv = 8 * tg;
+  bool vok;
+  const int64_t vblk = safe_block(a, blks, tv, tok0, L, vok);
   const uint8_t* vrow =
-      a.v + ((static_cast<int64_t>(vok ? vblk : 0) * kBlock + tv % kBlock) * a.kv_heads + h) *
-                R::kRow +
-      dc * 4 * R::kVWords;
-  const int64_t vstride = static_cast<int64_t>(a.kv_heads) * R::kRow;
+      a.v + (vblk * kBlock + tv % kBlock) * head_row + h * R::kRow + dc * 4 * R::kVWords;
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
-    const bool ok = vok && tv + t < L;
-    const uint8_t* src = vrow + t * vstride;
+    const uint8_t* src = vrow + t * head_row;
     if constexpr (R::kVWords == 4) {
-      const uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
       r.v[t][0] = w.x; r.v[t][R::kVWords > 1 ? 1 : 0] = w.y;
       r.v[t][R::kVWords > 2 ? 2 : 0] = w.z; r.v[t][R::kVWords > 3 ? 3 : 0] = w.w;
     } else if constexpr (R::kVWords == 2) {
-      const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0u, 0u);
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
       r.v[t][0] = w.x; r.v[t][R::kVWords > 1 ? 1 : 0] = w.y;
     } else {
-      r.v[t][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
+      r.v[t][0] = __ldg(reinterpret_cast<const uint32_t*>(src));
     }
   }
   r.miss = false;
+  r.sz_ok = false;
   r.ksz = r.vsz = 0u;
   if (tid < kTcTok) {
-    const int tt = tok0 + tid;
-    if (tt < L) {
-      const int32_t blk = bt[tt / kBlock];
-      const bool ok = blk >= 0 && blk < a.num_blocks;
-      if (ok && KvTraits<KV>::kQuant) {
-        const int64_t i = (static_cast<int64_t>(blk) * a.kv_heads + h) * kBlock + tt % kBlock;
-        r.ksz = __ldg(a.k_sz + i);
-        r.vsz = __ldg(a.v_sz + i);
-      }
-      r.miss = !ok;
-      if (!ok) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+    bool ok;
+    const int64_t blk = safe_block(a, blks, tid, tok0, L, ok);
+    r.sz_ok = ok && tok0 + tid < L;
+    r.miss = tok0 + tid < L && !ok;
+    if constexpr (KvTraits<KV>::kQuant) {
+      const int64_t i = (blk * a.kv_heads + h) * kBlock + tid % kBlock;
+      r.ksz = __ldg(a.k_sz + i);
+      r.vsz = __ldg(a.v_sz + i);
     }
+    if (r.miss) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
   }
 }
 
-// The four 16-bit pairs (dims 0-1, 2-3, 4-5, 6-7) of one token's 8-dim piece.
+// 16-bit pair q (dims 2q, 2q + 1) of one token's 8-dim V piece, c - mid.
 template <int KV>
-__device__ __forceinline__ void piece_pairs(const uint32_t (&w)[RawTile<KV>::kVWords],
-                                            uint32_t (&p)[4]) {
+__device__ __forceinline__ uint32_t piece_pair(const uint32_t (&w)[RawTile<KV>::kVWords], int q) {
   constexpr int kMid = KV == kI8 ? 128 : 8;
   if constexpr (KV == kF16) {
-    p[0] = w[0]; p[1] = w[1]; p[2] = w[2]; p[3] = w[3];
+    return w[q];
   } else if constexpr (KV == kI8) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) p[q] = bytes_to_f16(w[q >> 1], (q & 1) ? 0x4342u : 0x4140u);
+    return bytes_to_f16(w[q >> 1], (q & 1) ? 0x4342u : 0x4140u);
   } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t byte = (w[0] >> (8 * q)) & 0xFF;
-      p[q] = centred_pair<false>(byte & 0xF, byte >> 4, kMid);
-    }
+    const uint32_t byte = (w[0] >> (8 * q)) & 0xFF;
+    return centred_pair<false>(byte & 0xF, byte >> 4, kMid);
   }
 }
 
@@ -236,11 +274,12 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
   if (tid < kTcTok) {  // whole warps: the first two of the staging group
     float Sk = a.sm_scale_log2, Zk = 0.f, Sv = 1.f, Zv = 0.f;
     if constexpr (KvTraits<KV>::kQuant) {
-      const float s_k = half_lo(r.ksz), s_v = half_lo(r.vsz);
+      const uint32_t ksz = r.sz_ok ? r.ksz : 0u, vsz = r.sz_ok ? r.vsz : 0u;
+      const float s_k = half_lo(ksz), s_v = half_lo(vsz);
       Sk = s_k * a.sm_scale_log2;
-      Zk = (half_hi(r.ksz) + kMid * s_k) * a.sm_scale_log2;
+      Zk = (half_hi(ksz) + kMid * s_k) * a.sm_scale_log2;
       Sv = s_v;
-      Zv = half_hi(r.vsz) + kMid * s_v;
+      Zv = half_hi(vsz) + kMid * s_v;
     }
     sts32(sz + 4 * tid, __float_as_uint(Sk));
     sts32(sz + 4 * kTcTok + 4 * tid, __float_as_uint(Zk));
@@ -257,8 +296,8 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
   }
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
-    const int e = tid + kStageThreads * i;
-    const int t = e / kChunks, ch = e % kChunks;
+    int t, ch;
+    k_item<KV>(tid + kStageThreads * i, t, ch);
     const uint32_t x[4] = {r.k[i].x, r.k[i].y, r.k[i].z, r.k[i].w};
     if constexpr (KV == kF16) {
       sts128(kt + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
@@ -294,32 +333,51 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
   }
   // V: 8 tokens x 8 dims -> 8 rows (dims) of 8 tokens, one 16-byte store each
   const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
-  uint32_t pr[8][4];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) piece_pairs<KV>(r.v[t], pr[t]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t lo[4], hi[4];
 #pragma unroll
     for (int tp = 0; tp < 4; ++tp) {
-      lo[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x5410u);
-      hi[tp] = prmt(pr[2 * tp][q], pr[2 * tp + 1][q], 0x7632u);
+      const uint32_t p0 = piece_pair<KV>(r.v[2 * tp], q), p1 = piece_pair<KV>(r.v[2 * tp + 1], q);
+      lo[tp] = prmt(p0, p1, 0x5410u);
+      hi[tp] = prmt(p0, p1, 0x7632u);
     }
     sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2], lo[3]);
     sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1], hi[2], hi[3]);
   }
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---- waits --------------------------------------------------------------------
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or up to 0.5 ms have passed, instead of polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(500000u)
+      : "memory");
+  return done != 0;
+}
 
 // One thread's bounded wait on a barrier phase that also gives up when another
 // role has aborted the CTA (the flag at `abort_flag`); on its own timeout it
-// sets the flag and reports KVQ_DEV_ERR_TIMEOUT.
+// sets the flag and reports KVQ_DEV_ERR_TIMEOUT. The flag and the clock are
+// read only between sleeps.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int32_t* dev_err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity)) {
     if (*abort_flag) return false;
     if (global_ns() - t0 > 2000000000ull) {
       *abort_flag = 1;
@@ -389,6 +447,31 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane, scaled by `f` in
+// place (load, wait, multiply, store, wait).
+__device__ __forceinline__ void tmem_scale16(uint32_t taddr, float f) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // ---- work units -----------------------------------------------------------------
 
 struct TcUnit {
@@ -451,18 +534,37 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
     if (u >= c.total) return;
     const TcUnit w = tc_unit(a, c.ucum, u);
     const int32_t* bt = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks;
-    RawTile<KV> raw;
-    load_tile<KV>(a, bt, 0, w.s.L, w.h, tid, raw);
-    for (int j = 0; j < w.ntiles; ++j, ++tc) {
-      const uint32_t st = tc & 1u, use = tc >> 1;
+    // tile t's codes are loaded two tiles before it is staged (two register
+    // sets; one for fp16 rows), its block ids one tile before that
+    const int n = w.ntiles, L = w.s.L;
+    constexpr int kSets = 1;  // raw register sets in flight
+    RawTile<KV> raw[kSets];
+    int4 blk = tile_blocks(bt, 0, a.max_blocks);
+#pragma unroll
+    for (int e = 0; e < kSets; ++e) {
+      if (e < n) load_tile<KV>(a, blk, e * kTcTok, L, w.h, tid, raw[e]);
+      blk = tile_blocks(bt, (e + 1) * kTcTok, a.max_blocks);
+    }
+    auto stage_one = [&](int j, RawTile<KV>& r) {
+      const uint32_t st = tc % kStages, use = tc / kStages;
       if (use > 0 &&
           !warp_wait(c.bar(kBarKvEmpty + st), (use - 1u) & 1u, c.abort_flag, a.dev_err))
-        return;
-      store_tile<KV, QBF>(a, raw, c.base + kKOff + st * kKBytes, c.base + kVOff + st * kVBytes,
+        return false;
+      store_tile<KV, QBF>(a, r, c.base + kKOff + st * kKBytes, c.base + kVOff + st * kVBytes,
                           c.base + kSzOff + st * kSzBytes, c.base + kInfoOff + st * 16u, tid);
       fence_async_smem();
       mbar_arrive_one(c.bar(kBarKvFull + st));
-      if (j + 1 < w.ntiles) load_tile<KV>(a, bt, (j + 1) * kTcTok, w.s.L, w.h, tid, raw);
+      ++tc;
+      if (j + kSets < n) {
+        load_tile<KV>(a, blk, (j + kSets) * kTcTok, L, w.h, tid, r);
+        blk = tile_blocks(bt, (j + kSets + 1) * kTcTok, a.max_blocks);
+      }
+      return true;
+    };
+    for (int j = 0; j < n; j += kSets) {
+#pragma unroll
+      for (int e = 0; e < kSets; ++e)
+        if (j + e < n && !stage_one(j + e, raw[e])) return;
     }
   }
 }
@@ -504,22 +606,26 @@ __device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c)
     if (u >= c.total) return;
     const int n = tc_unit(a, c.ucum, u).ntiles;
     if (!wait(c.bar(kBarQFull + 0), k & 1u) || !wait(c.bar(kBarQFull + 1), k & 1u)) return;
-    if (!wait(c.bar(kBarKvFull + (tc & 1u)), (tc >> 1) & 1u)) return;
-    issue_s(0, tc & 1u);
-    issue_s(1, tc & 1u);
+    if (!wait(c.bar(kBarKvFull + tc % kStages), (tc / kStages) & 1u)) return;
+    issue_s(0, tc % kStages);
+    issue_s(1, tc % kStages);
     for (int j = 0; j < n; ++j, ++tc) {
-      const uint32_t st = tc & 1u;
+      const uint32_t st = tc % kStages, nx = (tc + 1u) % kStages;
       const bool more = j + 1 < n;
+      // S_g of the next tile as soon as warpgroup g has read this one out of
+      // TMEM: it runs while the warpgroup computes this tile's P'
+      if (!wait(c.bar(kBarSRead + 0), tc & 1u)) return;
+      if (more) {
+        if (!wait(c.bar(kBarKvFull + nx), ((tc + 1u) / kStages) & 1u)) return;
+        issue_s(0, nx);
+      }
+      if (!wait(c.bar(kBarSRead + 1), tc & 1u)) return;
+      if (more) issue_s(1, nx);
       if (!wait(c.bar(kBarPFull + 0), tc & 1u)) return;
       issue_o(0, st, j > 0);
-      if (more) {
-        if (!wait(c.bar(kBarKvFull + (st ^ 1u)), ((tc + 1u) >> 1) & 1u)) return;
-        issue_s(0, st ^ 1u);
-      }
       if (!wait(c.bar(kBarPFull + 1), tc & 1u)) return;
       issue_o(1, st, j > 0);
       umma_commit(c.bar(kBarKvEmpty + st));  // the stage is free once these products finish
-      if (more) issue_s(1, st ^ 1u);
     }
   }
 }
@@ -574,16 +680,19 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
 
     const float2 qs2 = make_float2(qsum, qsum);
     float m = -INFINITY;
-    float2 l2 = make_float2(0.f, 0.f), z2 = make_float2(0.f, 0.f);
+    float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two chains each
+    float2 z2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     for (int j = 0; j < w.ntiles; ++j, ++tc) {
-      const uint32_t st = tc & 1u;
+      const uint32_t st = tc % kStages;
       if (!wait(c.bar(kBarSFull + g), tc & 1u)) return;
       // the stage's scale arrays (already complete: S was computed from it)
-      if (!wait(c.bar(kBarKvFull + st), (tc >> 1) & 1u)) return;
+      if (!wait(c.bar(kBarKvFull + st), (tc / kStages) & 1u)) return;
       tc_fence_after();
       const uint32_t sz = c.base + kSzOff + st * kSzBytes;
       float x[kTcTok];
       tmem_ld64(s_addr, x);
+      tc_fence_before();
+      mbar_arrive_one(c.bar(kBarSRead + g));  // S_g's columns may take the next tile
       // s = S_k' raw + Z_k' sum(q) (softmax scale folded in), two tokens per
       // instruction
 #pragma unroll
@@ -613,9 +722,10 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
         for (int t = 0; t < kTcTok; ++t)
           if (((t < 32 ? miss0 : miss1) >> (t & 31)) & 1u) x[t] = -INFINITY;
       }
-      float bm = -INFINITY;
+      float bq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
-      for (int t = 0; t < kTcTok; t += 2) bm = fmaxf(bm, fmaxf(x[t], x[t + 1]));
+      for (int t = 0; t < kTcTok; t += 2) bq[(t >> 1) & 3] = max3(bq[(t >> 1) & 3], x[t], x[t + 1]);
+      const float bm = fmaxf(max3(bq[0], bq[1], bq[2]), bq[3]);
       // the reference maximum moves only when a score exceeds it by more than
       // tau (log2 units): p <= 2^tau then, and P' = p S_v stays within fp16
       // when the tile's largest V scale is at most 240 (else tau = 0: exact)
@@ -628,18 +738,15 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
         tc_fence_after();
         if (__any_sync(kFull, al != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float v[32];
-            tmem_ld32(o_addr + 32 * cc, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= al;
-            tmem_st32(o_addr + 32 * cc, v);
-          }
+          for (int cc = 0; cc < kHeadDim / 16; ++cc) tmem_scale16(o_addr + 16 * cc, al);
         }
       }
       const float2 al2 = make_float2(al, al);
-      l2 = __fmul2_rn(l2, al2);
-      z2 = __fmul2_rn(z2, al2);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        l2[e] = __fmul2_rn(l2[e], al2);
+        z2[e] = __fmul2_rn(z2[e], al2);
+      }
       m = mn;
       const float nref = m == -INFINITY ? 0.f : -m;
       const float2 nref2 = make_float2(nref, nref);
@@ -660,9 +767,9 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
           const int t0 = 8 * c8 + 2 * q;
           const float2 d = __fadd2_rn(make_float2(x[t0], x[t0 + 1]), nref2);
           const float2 p = make_float2(ex2(d.x), ex2(d.y));
-          l2 = __fadd2_rn(l2, p);
+          l2[q & 1] = __fadd2_rn(l2[q & 1], p);
           if constexpr (kQuant) {
-            z2 = __ffma2_rn(p, zv[q], z2);
+            z2[q & 1] = __ffma2_rn(p, zv[q], z2[q & 1]);
             const float2 v = __fmul2_rn(p, sv[q]);
             wd[q] = pack2<false>(v.x, v.y);
           } else {
@@ -679,7 +786,8 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
     if (!wait(c.bar(kBarODone + g), (tc - 1u) & 1u)) return;
     tc_fence_after();
     {
-      const float l = l2.x + l2.y, z = z2.x + z2.y;
+      const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+      const float z = (z2[0].x + z2[0].y) + (z2[1].x + z2[1].y);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<uint16_t*>(a.out) +
@@ -747,15 +855,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
   c.unit_slot = reinterpret_cast<volatile int*>(gbase + kUnitOff);
   c.ucum = ucum;
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init_count(c.bar(kBarKvFull + s), kStageThreads);
       mbar_init_count(c.bar(kBarKvEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init_count(c.bar(kBarSFull + s), 1);
       mbar_init_count(c.bar(kBarPFull + s), kWgRows);
       mbar_init_count(c.bar(kBarODone + s), 1);
       mbar_init_count(c.bar(kBarQFull + s), kWgRows);
       mbar_init_count(c.bar(kBarUnitFull + s), 1);
       mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 1);  // every warp's lane 0
+      mbar_init_count(c.bar(kBarSRead + s), kWgRows);
     }
     mbar_init_count(c.bar(kBarDrain), 1);
     *c.abort_flag = 0;
@@ -769,14 +880,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
   c.total = ucum[a.batch];
 
   if (warp < kSoftWarps) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
     softmax_role<KV, QBF>(a, c, warp >> 2, tid & (kWgRows - 1), warp);
   } else if (warp < kMmaWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
     staging_role<KV, QBF>(a, c, tid - kSoftWarps * 32);
-  } else if (lane == 0) {
-    mma_role<QBF>(a, c);
-    // every product this thread issued completes before the TMEM is freed
-    umma_commit(c.bar(kBarDrain));
-    mbar_wait(c.bar(kBarDrain), 0);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
+    if (warp == kMmaWarp && lane == 0) {
+      mma_role<QBF>(a, c);
+      // every product this thread issued completes before the TMEM is freed
+      umma_commit(c.bar(kBarDrain));
+      mbar_wait(c.bar(kBarDrain), 0);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -795,7 +911,7 @@ cudaError_t launch_tc_t(const ExtendArgs& a, int grid, cudaStream_t s) {
   if (opted_in_device != dev) {
     e = cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(tc_smem_bytes(kMaxBatch)));
+                             static_cast<int>(tc_smem_bytes(kTcMaxBatch)));
     if (e != cudaSuccess) return e;
     // two CTAs per SM need the largest shared-memory carveout
     e = cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>,
@@ -815,7 +931,7 @@ int tc_occupancy_t(int batch) {
   thread_local int cached_dev = -1, cached_batch = -1, cached_n = 0;
   if (dev == cached_dev && batch == cached_batch) return cached_n;
   if (cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(tc_smem_bytes(kMaxBatch))) != cudaSuccess ||
+                           static_cast<int>(tc_smem_bytes(kTcMaxBatch))) != cudaSuccess ||
       cudaFuncSetAttribute(extend_tc_kernel<KV, QBF>,
                            cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
@@ -833,6 +949,8 @@ int tc_occupancy_t(int batch) {
 }  // namespace
 
 size_t extend_tc_smem_bytes(int batch) { return tc_smem_bytes(batch); }
+
+int extend_tc_max_batch() { return kTcMaxBatch; }
 
 bool extend_tc_supported(int kv_dtype, int q_dtype) {
   return kv_dtype == kI8 || kv_dtype == kI4 || (kv_dtype == kF16 && q_dtype == kF16);

@@ -172,6 +172,7 @@ cudaError_t launch_extend_tc(const ExtendArgs& a, int kv_dtype, int q_dtype, int
                              cudaStream_t s);
 int extend_tc_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
 size_t extend_tc_smem_bytes(int batch);  // dynamic shared memory of one CTA
+int extend_tc_max_batch();                // most requests the tcgen05 kernel takes
 cudaError_t launch_copy(const CopyArgs& a, int64_t n, cudaStream_t s);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
 // kv_dtype / q_dtype select the template instance
