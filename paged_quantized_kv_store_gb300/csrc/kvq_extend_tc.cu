@@ -12,7 +12,7 @@
 //     (dims as rows), into a two-stage ring, with the per-token scale S and
 //     shifted zero Z + mid S in four small arrays; it also hands out the work
 //     units (an atomic counter, longest tiles first);
-//   * MMA thread (warp 12, lane 0): issues S_g = Q_g K^T (M 128, N 64,
+//   * MMA warp (warp 12; one elected lane issues): S_g = Q_g K^T (M 128, N 64,
 //     K 128) for both softmax warpgroups into their own TMEM columns, the
 //     next tile's S_g as soon as warpgroup g has read the current one out of
 //     TMEM (so it runs during that warpgroup's exponentials), and
@@ -23,8 +23,9 @@
 //     sum(q), the causal mask and the online softmax; when the running
 //     maximum moves by more than a threshold, rescale the warp's rows of O in
 //     TMEM (a stale maximum only scales every term alike); write
-//     P' = p S_v to shared memory in fp16 and keep sum p (Z_v + mid S_v) in
-//     registers. At the end of the unit: (O + z) / l.
+//     P' = p S_v in fp16 to its own TMEM columns, from which the P' V product
+//     reads its A operand, and keep sum p (Z_v + mid S_v) in registers. At
+//     the end of the unit: (O + z) / l.
 // The per-token arithmetic runs on paired fp32 instructions (two tokens per
 // instruction). Roles meet only at mbarriers (no CTA-wide barrier inside the
 // work loop); every wait is bounded (2 s, then KVQ_DEV_ERR_TIMEOUT and every
@@ -53,20 +54,27 @@ constexpr int kTcThreads = 16 * 32;       // four warpgroups; warps 13-15 only h
 constexpr uint32_t kLowRegs = 120, kHighRegs = 136;
 static_assert(2 * kLowRegs + 2 * kHighRegs == 4 * (65536 / kTcThreads),
               "the split must add up to the launch's registers");
-constexpr uint32_t kTmemCols = 512;       // S_g: columns 64 g .. 64 g + 63; O_g: 128 + 128 g ..
+// TMEM columns: S_g at 64 g (64), O_g at 128 + o_cols g, P'_g at p_col + 32 g
+// (32: two fp16 per column). With fp16 queries O_g has 144 columns: the 128
+// output dims, then the row sum of P (V's tile carries a row of ones).
+constexpr uint32_t kTmemCols = 512;
+template <bool QBF>
+constexpr uint32_t o_cols() { return QBF ? 128u : 144u; }
+template <bool QBF>
+constexpr uint32_t p_col() { return 128u + 2u * o_cols<QBF>(); }
+static_assert(p_col<false>() + 64 <= kTmemCols && p_col<true>() + 64 <= kTmemCols, "TMEM map");
 
 // shared memory, offsets from a 1024-byte aligned base
 constexpr int kStages = 3;                          // K/V ring depth (tiles)
 constexpr uint32_t kQBytes = kWgRows * 256;         // 2 column blocks of 128 rows x 128 B
 constexpr uint32_t kKBytes = kTcTok * 256;          // 2 column blocks of 64 rows x 128 B
-constexpr uint32_t kVBytes = 128 * kTcTok * 2;      // 128 dims x 64 tokens
-constexpr uint32_t kPBytes = kWgRows * kTcTok * 2;  // 128 rows x 64 tokens
+constexpr int kVRows = 144;                         // 128 dims, a row of ones, 15 of zeros
+constexpr uint32_t kVBytes = kVRows * kTcTok * 2;   // V^T: kVRows x 64 tokens
 constexpr uint32_t kSzBytes = 4 * kTcTok * 4;       // S_k'[64] Z_k'[64] S_v[64] Z_v'[64]
 constexpr uint32_t kQOff = 0;                       // Q of warpgroup g at g * kQBytes
 constexpr uint32_t kKOff = kQOff + 2 * kQBytes;     // K tile of stage s at s * kKBytes
 constexpr uint32_t kVOff = kKOff + kStages * kKBytes;
-constexpr uint32_t kPOff = kVOff + kStages * kVBytes;  // P' of warpgroup g
-constexpr uint32_t kSzOff = kPOff + 2 * kPBytes;
+constexpr uint32_t kSzOff = kVOff + kStages * kVBytes;
 constexpr uint32_t kInfoOff = kSzOff + kStages * kSzBytes;  // per stage: max S_v (2 halves), missing masks
 constexpr uint32_t kBarOff = kInfoOff + kStages * 16;
 // mbarriers (index: runs by stage or warpgroup)
@@ -144,6 +152,10 @@ struct RawTile {
   uint4 k[kKChunks];
   uint32_t v[8][kVWords];
   uint32_t ksz, vsz;
+  uint32_t ksz4[KvTraits<KV>::kQuant ? kKChunks : 1];  // K scale/zero of each K chunk's token
+  uint32_t kmask;  // which K chunks belong to a token in the context (block in the pool)
+  uint32_t vsz8[KvTraits<KV>::kQuant ? 8 : 1];  // V scale/zero of this thread's 8 V tokens
+  uint32_t vmask;  // which of those 8 tokens are in the context (block in the pool)
   bool sz_ok;  // token `tid` is in the context and its block in the pool
   bool miss;   // token `tid` of the tile is in the context but its block id is outside the pool
 };
@@ -199,6 +211,7 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks,
                                           int h, int tid, RawTile<KV>& r) {
   using R = RawTile<KV>;
   const int64_t head_row = static_cast<int64_t>(a.kv_heads) * R::kRow;  // one token
+  r.kmask = 0u;
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
     int t, ch;
@@ -207,6 +220,9 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks,
     const int64_t blk = safe_block(a, blks, t, tok0, L, ok);
     const uint8_t* src = a.k + (blk * kBlock + t % kBlock) * head_row + h * R::kRow;
     r.k[i] = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+    r.kmask |= (ok && tok0 + t < L ? 1u : 0u) << i;
+    if constexpr (KvTraits<KV>::kQuant)
+      r.ksz4[i] = __ldg(a.k_sz + (blk * a.kv_heads + h) * kBlock + t % kBlock);
   }
   // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
   const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
@@ -215,6 +231,16 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks,
   const int64_t vblk = safe_block(a, blks, tv, tok0, L, vok);
   const uint8_t* vrow =
       a.v + (vblk * kBlock + tv % kBlock) * head_row + h * R::kRow + dc * 4 * R::kVWords;
+  r.vmask = 0u;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) r.vmask |= (vok && tok0 + tv + t < L ? 1u : 0u) << t;
+  if constexpr (KvTraits<KV>::kQuant) {  // 8 consecutive words: two 16-byte loads
+    const uint4* vs = reinterpret_cast<const uint4*>(a.v_sz + (vblk * a.kv_heads + h) * kBlock +
+                                                     tv % kBlock);
+    const uint4 w0 = __ldg(vs), w1 = __ldg(vs + 1);
+    r.vsz8[0] = w0.x; r.vsz8[1] = w0.y; r.vsz8[2] = w0.z; r.vsz8[3] = w0.w;
+    r.vsz8[4] = w1.x; r.vsz8[5] = w1.y; r.vsz8[6] = w1.z; r.vsz8[7] = w1.w;
+  }
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
     const uint8_t* src = vrow + t * head_row;
@@ -265,13 +291,24 @@ __device__ __forceinline__ uint32_t piece_pair(const uint32_t (&w)[RawTile<KV>::
 // `sz` (softmax scale folded into the K pair), and at `info` the largest S_v
 // of each half-tile and the two 32-token masks of missing tokens. `tid` is
 // the staging thread (0..127).
+// fp16 pair (mid, mid) of a pool kind: 128 for INT8 codes, 8 for INT4
+template <int KV>
+__device__ __forceinline__ uint32_t kMidPair() {
+  return KV == kI8 ? 0x58005800u : 0x48004800u;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <int KV, bool QBF>
 __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV>& r, uint32_t kt,
                                            uint32_t vt, uint32_t sz, uint32_t info, int tid) {
   using R = RawTile<KV>;
   constexpr int kMid = KV == kI8 ? 128 : 8;
-  constexpr int kChunks = R::kRow / 16;
-  if (tid < kTcTok) {  // whole warps: the first two of the staging group
+  constexpr bool VDEQ = !QBF;  // fp16 queries: V is staged dequantized
+  if (tid < kTcTok && !VDEQ) {  // whole warps: the first two of the staging group
     float Sk = a.sm_scale_log2, Zk = 0.f, Sv = 1.f, Zv = 0.f;
     if constexpr (KvTraits<KV>::kQuant) {
       const uint32_t ksz = r.sz_ok ? r.ksz : 0u, vsz = r.sz_ok ? r.vsz : 0u;
@@ -288,17 +325,29 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
     float mx = Sv;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    if ((tid & 31) == 0) sts32(info + 4 * (tid >> 5), __float_as_uint(mx));
+  }
+  if (tid < kTcTok) {
     const uint32_t miss = __ballot_sync(kFull, r.miss);
-    if ((tid & 31) == 0) {
-      sts32(info + 4 * (tid >> 5), __float_as_uint(mx));
-      sts32(info + 8 + 4 * (tid >> 5), miss);
-    }
+    if ((tid & 31) == 0) sts32(info + 8 + 4 * (tid >> 5), miss);
   }
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
     int t, ch;
     k_item<KV>(tid + kStageThreads * i, t, ch);
     const uint32_t x[4] = {r.k[i].x, r.k[i].y, r.k[i].z, r.k[i].w};
+    // dequantized K (fp16 queries): (c - mid) S + (Z + mid S), one rounding;
+    // zero for a token outside the context
+    uint32_t ks2 = 0u, kz2 = 0u;
+    if constexpr (VDEQ && KvTraits<KV>::kQuant) {
+      const uint32_t w = (r.kmask >> i) & 1u ? r.ksz4[i] : 0u;
+      ks2 = prmt(w, w, 0x1010u);
+      kz2 = hfma2(kMidPair<KV>(), ks2, prmt(w, w, 0x3232u));
+    }
+    auto kdeq = [&](uint32_t pair) {
+      if constexpr (VDEQ && KvTraits<KV>::kQuant) return hfma2(pair, ks2, kz2);
+      return pair;
+    };
     if constexpr (KV == kF16) {
       sts128(kt + umma_kmajor_offset(kTcTok, t, 8 * ch), x[0], x[1], x[2], x[3]);
     } else if constexpr (KV == kI8) {
@@ -313,7 +362,7 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
           if constexpr (QBF) {
             v[q] = (q & 1) ? bytes_to_bf16_pair(word, 2, 3) : bytes_to_bf16_pair(word, 0, 1);
           } else {
-            v[q] = bytes_to_f16(word, (q & 1) ? 0x4342u : 0x4140u);
+            v[q] = kdeq(bytes_to_f16(word, (q & 1) ? 0x4342u : 0x4140u));
           }
         }
         sts128(kt + umma_kmajor_offset(kTcTok, t, 16 * ch + 8 * hf), v[0], v[1], v[2], v[3]);
@@ -325,7 +374,7 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t byte = (x[qt] >> (8 * q)) & 0xFF;
-          v[q] = centred_pair<QBF>(byte & 0xF, byte >> 4, kMid);
+          v[q] = kdeq(centred_pair<QBF>(byte & 0xF, byte >> 4, kMid));
         }
         sts128(kt + umma_kmajor_offset(kTcTok, t, 32 * ch + 8 * qt), v[0], v[1], v[2], v[3]);
       }
@@ -333,6 +382,18 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
   }
   // V: 8 tokens x 8 dims -> 8 rows (dims) of 8 tokens, one 16-byte store each
   const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
+  // dequantized V (fp16 queries): per token pair, (S, S') and (Z + mid S, ..)
+  // as fp16 pairs, zero for tokens outside the context
+  uint32_t s2[4], z2[4];
+  if constexpr (VDEQ && KvTraits<KV>::kQuant) {
+#pragma unroll
+    for (int tp = 0; tp < 4; ++tp) {
+      const uint32_t wa = (r.vmask >> (2 * tp)) & 1u ? r.vsz8[2 * tp] : 0u;
+      const uint32_t wb = (r.vmask >> (2 * tp + 1)) & 1u ? r.vsz8[2 * tp + 1] : 0u;
+      s2[tp] = prmt(wa, wb, 0x5410u);
+      z2[tp] = hfma2(kMidPair<KV>(), s2[tp], prmt(wa, wb, 0x7632u));
+    }
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t lo[4], hi[4];
@@ -341,10 +402,33 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
       const uint32_t p0 = piece_pair<KV>(r.v[2 * tp], q), p1 = piece_pair<KV>(r.v[2 * tp + 1], q);
       lo[tp] = prmt(p0, p1, 0x5410u);
       hi[tp] = prmt(p0, p1, 0x7632u);
+      if constexpr (VDEQ && KvTraits<KV>::kQuant) {  // (c - mid) S + (Z + mid S), one rounding
+        lo[tp] = hfma2(lo[tp], s2[tp], z2[tp]);
+        hi[tp] = hfma2(hi[tp], s2[tp], z2[tp]);
+      }
     }
-    sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2], lo[3]);
-    sts128(vt + umma_kmajor_offset(128, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1], hi[2], hi[3]);
+    sts128(vt + umma_kmajor_offset(kVRows, 8 * dc + 2 * q, 8 * tg), lo[0], lo[1], lo[2], lo[3]);
+    sts128(vt + umma_kmajor_offset(kVRows, 8 * dc + 2 * q + 1, 8 * tg), hi[0], hi[1], hi[2], hi[3]);
   }
+}
+
+// 2^x of both fp16 halves, one instruction
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t h) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(h));
+  return r;
+}
+
+// One fp32 column of this thread's TMEM lane.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
 }
 
 // max(a, b, c) in one instruction
@@ -515,6 +599,17 @@ struct TcShared {
 template <int KV, bool QBF>
 __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared& c, int tid) {
   const int lane = tid & 31;
+  if constexpr (!QBF) {
+    // rows 128..143 of every V stage: ones, then zeros (the B columns that give
+    // each row's sum of P); published with each stage's first arrival
+    for (int e = tid; e < kStages * 16 * 8; e += kStageThreads) {
+      const int stg = e / 128, rr = (e / 8) % 16, ch = e % 8;
+      const uint32_t v = rr == 0 ? 0x3C003C00u : 0u;
+      sts128(c.base + kVOff + stg * kVBytes + umma_kmajor_offset(kVRows, 128 + rr, 8 * ch), v, v,
+             v, v);
+    }
+    fence_async_smem();
+  }
   uint32_t tc = 0;  // tiles staged so far
   for (uint32_t k = 0;; ++k) {
     const uint32_t slot = k & 1u;
@@ -569,31 +664,55 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
   }
 }
 
-// The MMA thread.
+// One lane of a converged warp (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// The MMA warp: all 32 lanes run the loop (so the descriptors stay
+// warp-uniform) and wait together; one elected lane issues each product and
+// commit.
 template <bool QBF>
-__device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c) {
+__device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c, int lane) {
   constexpr uint32_t idesc_s = umma_idesc_f16(QBF, kWgRows, kTcTok);
-  constexpr uint32_t idesc_o = umma_idesc_f16(false, kWgRows, kHeadDim);
+  constexpr uint32_t idesc_o = umma_idesc_f16(false, kWgRows, o_cols<QBF>());
+  // descriptors of k-step 0; a k-step adds its byte offset / 16 to the low field
+  const uint64_t q_desc0 = umma_desc_sw128(c.base + kQOff, 1024);
+  const uint64_t k_desc0 = umma_desc_sw128(c.base + kKOff, 1024);
+  const uint64_t v_desc0 = umma_desc_sw128(c.base + kVOff, 1024);
   auto issue_s = [&](int g, uint32_t st) {
-    const uint32_t qa = c.base + kQOff + g * kQBytes, ka = c.base + kKOff + st * kKBytes;
+    const uint64_t qd = q_desc0 + (g * kQBytes >> 4), kd = k_desc0 + (st * kKBytes >> 4);
+    if (elect_one()) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      umma_f16(c.tmem + 64u * g,
-               umma_desc_sw128(qa + (k >> 2) * (kWgRows * 128) + (k & 3) * 32, 1024),
-               umma_desc_sw128(ka + (k >> 2) * (kTcTok * 128) + (k & 3) * 32, 1024), idesc_s,
-               k > 0);
-    umma_commit(c.bar(kBarSFull + g));
+      for (int k = 0; k < 8; ++k)
+        umma_f16(c.tmem + 64u * g, qd + (((k >> 2) * (kWgRows * 128) + (k & 3) * 32) >> 4),
+                 kd + (((k >> 2) * (kTcTok * 128) + (k & 3) * 32) >> 4), idesc_s, k > 0);
+      umma_commit(c.bar(kBarSFull + g));
+    }
+    __syncwarp();
   };
   auto issue_o = [&](int g, uint32_t st, bool acc) {
-    const uint32_t pa = c.base + kPOff + g * kPBytes, va = c.base + kVOff + st * kVBytes;
+    const uint64_t vd = v_desc0 + (st * kVBytes >> 4);
+    if (elect_one()) {
 #pragma unroll
-    for (int k = 0; k < kTcTok / 16; ++k)
-      umma_f16(c.tmem + 128u + 128u * g, umma_desc_sw128(pa + k * 32, 1024),
-               umma_desc_sw128(va + k * 32, 1024), idesc_o, acc || k > 0);
-    umma_commit(c.bar(kBarODone + g));
+      for (int k = 0; k < kTcTok / 16; ++k)
+        umma_f16_tmem_a(c.tmem + 128u + o_cols<QBF>() * g,
+                        c.tmem + p_col<QBF>() + 32u * g + 8u * k, vd + ((k * 32) >> 4), idesc_o,
+                        acc || k > 0);
+      umma_commit(c.bar(kBarODone + g));
+    }
+    __syncwarp();
+  };
+  auto commit = [&](uint32_t bar) {
+    if (elect_one()) umma_commit(bar);
+    __syncwarp();
   };
   auto wait = [&](uint32_t b, uint32_t parity) {
-    const bool ok = wait_or_abort(b, parity, c.abort_flag, a.dev_err);
+    const bool ok = warp_wait(b, parity, c.abort_flag, a.dev_err);
     tc_fence_after();
     return ok;
   };
@@ -602,7 +721,8 @@ __device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c)
     const uint32_t slot = k & 1u;
     if (!wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u)) return;
     const int u = c.unit_slot[slot];
-    mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
     if (u >= c.total) return;
     const int n = tc_unit(a, c.ucum, u).ntiles;
     if (!wait(c.bar(kBarQFull + 0), k & 1u) || !wait(c.bar(kBarQFull + 1), k & 1u)) return;
@@ -625,7 +745,7 @@ __device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c)
       issue_o(0, st, j > 0);
       if (!wait(c.bar(kBarPFull + 1), tc & 1u)) return;
       issue_o(1, st, j > 0);
-      umma_commit(c.bar(kBarKvEmpty + st));  // the stage is free once these products finish
+      commit(c.bar(kBarKvEmpty + st));  // the stage is free once these products finish
     }
   }
 }
@@ -636,9 +756,11 @@ template <int KV, bool QBF>
 __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared& c, int g,
                                              int i, int warp) {
   constexpr bool kQuant = KvTraits<KV>::kQuant;
+  constexpr bool kVDeq = !QBF;  // K and V staged dequantized: P = p, no scale arrays
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-  const uint32_t s_addr = lane_addr + 64u * g, o_addr = lane_addr + 128u + 128u * g;
-  const uint32_t q_tile = c.base + kQOff + g * kQBytes, p_tile = c.base + kPOff + g * kPBytes;
+  const uint32_t s_addr = lane_addr + 64u * g, o_addr = lane_addr + 128u + o_cols<QBF>() * g;
+  const uint32_t q_tile = c.base + kQOff + g * kQBytes;
+  const uint32_t p_addr = lane_addr + p_col<QBF>() + 32u * g;
   const int lane = i & 31;
   auto wait = [&](uint32_t b, uint32_t parity) {
     return warp_wait(b, parity, c.abort_flag, a.dev_err);
@@ -668,7 +790,7 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
       for (int ch = 0; ch < 16; ++ch) {
         const uint4 x = valid ? qp[ch] : make_uint4(0u, 0u, 0u, 0u);
         sts128(q_tile + umma_kmajor_offset(kWgRows, i, 8 * ch), x.x, x.y, x.z, x.w);
-        if constexpr (kQuant) {
+        if constexpr (kQuant && !kVDeq) {
           qsum += lo_to_float<QBF>(x.x) + hi_to_float<QBF>(x.x) + lo_to_float<QBF>(x.y) +
                   hi_to_float<QBF>(x.y) + lo_to_float<QBF>(x.z) + hi_to_float<QBF>(x.z) +
                   lo_to_float<QBF>(x.w) + hi_to_float<QBF>(x.w);
@@ -693,6 +815,22 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
       tmem_ld64(s_addr, x);
       tc_fence_before();
       mbar_arrive_one(c.bar(kBarSRead + g));  // S_g's columns may take the next tile
+      // kVDeq: K was staged dequantized; s = raw * softmax scale (log2 units).
+      // A positive scale goes into the exponent's FMA below (the maximum of
+      // raw scores then gives the maximum of s); any other scale is applied
+      // here.
+      const float cs = a.sm_scale_log2;
+      if constexpr (kVDeq) {
+        if (!(cs > 0.f)) {
+          const float2 c2 = make_float2(cs, cs);
+#pragma unroll
+          for (int q = 0; q < kTcTok / 2; ++q) {
+            const float2 r = __fmul2_rn(make_float2(x[2 * q], x[2 * q + 1]), c2);
+            x[2 * q] = r.x;
+            x[2 * q + 1] = r.y;
+          }
+        }
+      } else {
       // s = S_k' raw + Z_k' sum(q) (softmax scale folded in), two tokens per
       // instruction
 #pragma unroll
@@ -707,6 +845,7 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
         x[4 * q + 1] = r0.y;
         x[4 * q + 2] = r1.x;
         x[4 * q + 3] = r1.y;
+      }
       }
       // positions past the row's own, and missing tokens, are masked
       const int tok0 = j * kTcTok;
@@ -725,11 +864,12 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
       float bq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
       for (int t = 0; t < kTcTok; t += 2) bq[(t >> 1) & 3] = max3(bq[(t >> 1) & 3], x[t], x[t + 1]);
-      const float bm = fmaxf(max3(bq[0], bq[1], bq[2]), bq[3]);
+      const float cm = (kVDeq && cs > 0.f) ? cs : 1.f;  // scale still to apply
+      const float bm = fmaxf(max3(bq[0], bq[1], bq[2]), bq[3]) * cm;
       // the reference maximum moves only when a score exceeds it by more than
       // tau (log2 units): p <= 2^tau then, and P' = p S_v stays within fp16
       // when the tile's largest V scale is at most 240 (else tau = 0: exact)
-      const float tau = fmaxf(info.x, info.y) <= 240.f ? 8.f : 0.f;
+      const float tau = (kVDeq || fmaxf(info.x, info.y) <= 240.f) ? 8.f : 0.f;
       const float mn = (m == -INFINITY || bm > m + tau) ? fmaxf(m, bm) : m;
       const float al = (m == -INFINITY || mn == m) ? 1.f : ex2(m - mn);
       if (j > 0) {
@@ -738,7 +878,8 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
         tc_fence_after();
         if (__any_sync(kFull, al != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < kHeadDim / 16; ++cc) tmem_scale16(o_addr + 16 * cc, al);
+          for (int cc = 0; cc < static_cast<int>(o_cols<QBF>()) / 16; ++cc)
+            tmem_scale16(o_addr + 16 * cc, al);
         }
       }
       const float2 al2 = make_float2(al, al);
@@ -750,35 +891,49 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
       m = mn;
       const float nref = m == -INFINITY ? 0.f : -m;
       const float2 nref2 = make_float2(nref, nref);
-      // P' = p S_v (quantized) or p, fp16, into this row of the P' tile
+      uint32_t pw[kTcTok / 2];
+      if constexpr (kVDeq) {
+        // P = 2^(s - m) straight in fp16 pairs: the exponent pair rounded to
+        // fp16 and one packed exponential; the row sum comes from the P V
+        // product (V's row of ones), over the same fp16 values
+        const float2 cm2 = make_float2(cm, cm);
+#pragma unroll
+        for (int q = 0; q < kTcTok / 2; ++q) {
+          const float2 d = __ffma2_rn(make_float2(x[2 * q], x[2 * q + 1]), cm2, nref2);
+          pw[q] = ex2_h2(pack2<false>(d.x, d.y));
+        }
+      } else {
+      // P' = p S_v (quantized) or p, fp16, into this row of P'_g in TMEM
 #pragma unroll
       for (int c8 = 0; c8 < kTcTok / 8; ++c8) {
-        const float4 sva = lds_f4(sz + 8 * kTcTok + 32 * c8),
-                     svb = lds_f4(sz + 8 * kTcTok + 32 * c8 + 16);
-        const float4 zva = lds_f4(sz + 12 * kTcTok + 32 * c8),
-                     zvb = lds_f4(sz + 12 * kTcTok + 32 * c8 + 16);
+        float4 sva = make_float4(1.f, 1.f, 1.f, 1.f), svb = sva, zva = sva, zvb = sva;
+        if constexpr (!kVDeq) {
+          sva = lds_f4(sz + 8 * kTcTok + 32 * c8);
+          svb = lds_f4(sz + 8 * kTcTok + 32 * c8 + 16);
+          zva = lds_f4(sz + 12 * kTcTok + 32 * c8);
+          zvb = lds_f4(sz + 12 * kTcTok + 32 * c8 + 16);
+        }
         const float2 sv[4] = {make_float2(sva.x, sva.y), make_float2(sva.z, sva.w),
                               make_float2(svb.x, svb.y), make_float2(svb.z, svb.w)};
         const float2 zv[4] = {make_float2(zva.x, zva.y), make_float2(zva.z, zva.w),
                               make_float2(zvb.x, zvb.y), make_float2(zvb.z, zvb.w)};
-        uint32_t wd[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int t0 = 8 * c8 + 2 * q;
           const float2 d = __fadd2_rn(make_float2(x[t0], x[t0 + 1]), nref2);
           const float2 p = make_float2(ex2(d.x), ex2(d.y));
           l2[q & 1] = __fadd2_rn(l2[q & 1], p);
-          if constexpr (kQuant) {
+          if constexpr (kQuant && !kVDeq) {
             z2[q & 1] = __ffma2_rn(p, zv[q], z2[q & 1]);
             const float2 v = __fmul2_rn(p, sv[q]);
-            wd[q] = pack2<false>(v.x, v.y);
+            pw[4 * c8 + q] = pack2<false>(v.x, v.y);
           } else {
-            wd[q] = pack2<false>(p.x, p.y);
+            pw[4 * c8 + q] = pack2<false>(p.x, p.y);
           }
         }
-        sts128(p_tile + umma_kmajor_offset(kWgRows, i, 8 * c8), wd[0], wd[1], wd[2], wd[3]);
       }
-      fence_async_smem();
+      }
+      tmem_st32u(p_addr, pw);
       tc_fence_before();
       mbar_arrive_one(c.bar(kBarPFull + g));
     }
@@ -786,8 +941,9 @@ __device__ __forceinline__ void softmax_role(const ExtendArgs& a, const TcShared
     if (!wait(c.bar(kBarODone + g), (tc - 1u) & 1u)) return;
     tc_fence_after();
     {
-      const float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+      float l = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
       const float z = (z2[0].x + z2[0].y) + (z2[1].x + z2[1].y);
+      if constexpr (kVDeq) l = tmem_ld1(o_addr + kHeadDim);  // the row-sum column
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<uint16_t*>(a.out) +
@@ -887,11 +1043,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
     staging_role<KV, QBF>(a, c, tid - kSoftWarps * 32);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
-    if (warp == kMmaWarp && lane == 0) {
-      mma_role<QBF>(a, c);
-      // every product this thread issued completes before the TMEM is freed
-      umma_commit(c.bar(kBarDrain));
-      mbar_wait(c.bar(kBarDrain), 0);
+    if (warp == kMmaWarp) {
+      mma_role<QBF>(a, c, lane);
+      // every product this warp issued completes before the TMEM is freed
+      __syncwarp();
+      if (elect_one()) {
+        umma_commit(c.bar(kBarDrain));
+        mbar_wait(c.bar(kBarDrain), 0);
+      }
+      __syncwarp();
     }
   }
   tc_fence_before();
