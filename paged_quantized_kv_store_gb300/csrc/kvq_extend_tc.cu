@@ -193,50 +193,87 @@ __device__ __forceinline__ int pick4(const int4& v, int k) {
   return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }
 
-// Block of tile token t: its id when the block is inside the context and the
-// pool (ok), else 0 -- an address that is safe to read. Codes read from
-// there, and from the context's last block past its length, are never used:
-// those tokens are masked (p = 0), and their scale/zero words are zeroed.
-__device__ __forceinline__ int64_t safe_block(const ExtendArgs& a, const int4& blks, int t,
-                                              int tok0, int L, bool& ok) {
-  const int32_t blk = pick4(blks, t / kBlock);
-  ok = tok0 + (t & ~(kBlock - 1)) < L && blk >= 0 && blk < a.num_blocks;
-  return ok ? blk : 0;
+// Per-thread constants of a staging thread's loads, fixed for a unit (kv
+// head h): which tile block and token each K item reads and its byte offset
+// from the block's first row; the same for the thread's 8 V tokens.
+template <int KV>
+struct StageMap {
+  using R = RawTile<KV>;
+  int kb[R::kKChunks];         // tile block (0..3) of K item i
+  int kt[R::kKChunks];         // tile token of K item i
+  uint32_t koff[R::kKChunks];  // bytes from the block's first row (token row, head, chunk)
+  uint32_t kszo[R::kKChunks];  // scale word index within the block's words (head, token)
+  int vb;                      // tile block of the V tokens 8 tg .. 8 tg + 7
+  uint32_t voff, vszo;
+  __device__ __forceinline__ void init(const ExtendArgs& a, int h, int tid) {
+    const uint32_t head_row = static_cast<uint32_t>(a.kv_heads) * R::kRow;  // one token
+#pragma unroll
+    for (int i = 0; i < R::kKChunks; ++i) {
+      int t, ch;
+      k_item<KV>(tid + kStageThreads * i, t, ch);
+      kb[i] = t / kBlock;
+      kt[i] = t;
+      koff[i] = (t % kBlock) * head_row + h * R::kRow + 16 * ch;
+      kszo[i] = h * kBlock + t % kBlock;
+    }
+    const int tv = 8 * (tid & 7), dc = tid >> 3;
+    vb = tv / kBlock;
+    voff = (tv % kBlock) * head_row + h * R::kRow + dc * 4 * R::kVWords;
+    vszo = h * kBlock + tv % kBlock;
+  }
+};
+
+// The tile's four blocks: each id when the block is inside the context and
+// the pool (bit b of *valid), else 0 -- an address that is safe to read.
+// Codes read from there, and from the context's last block past its length,
+// are never used: those tokens are masked (p = 0), and their scale/zero words
+// are zeroed.
+__device__ __forceinline__ int4 safe_blocks(const ExtendArgs& a, const int4& blks, int tok0,
+                                            int L, uint32_t* valid) {
+  const int e[4] = {blks.x, blks.y, blks.z, blks.w};
+  int o[4];
+  uint32_t v = 0u;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const bool ok = tok0 + b * kBlock < L && e[b] >= 0 && e[b] < a.num_blocks;
+    o[b] = ok ? e[b] : 0;
+    v |= (ok ? 1u : 0u) << b;
+  }
+  *valid = v;
+  return make_int4(o[0], o[1], o[2], o[3]);
 }
 
-// Issues the global loads of tile tok0 (table entries in `blks`) into r; no
-// instruction here waits for their data.
-template <int KV>
-__device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks, int tok0, int L,
-                                          int h, int tid, RawTile<KV>& r) {
+// Issues the global loads of tile tok0 into r; no instruction here waits for
+// their data.
+template <int KV, bool QBF>
+__device__ __forceinline__ void load_tile(const ExtendArgs& a, const StageMap<KV>& m,
+                                          const int4& blks, int tok0, int L, int h, int tid,
+                                          RawTile<KV>& r) {
   using R = RawTile<KV>;
-  const int64_t head_row = static_cast<int64_t>(a.kv_heads) * R::kRow;  // one token
+  uint32_t valid;
+  const int4 sb = safe_blocks(a, blks, tok0, L, &valid);
+  const int64_t blk_bytes = static_cast<int64_t>(kBlock) * a.kv_heads * R::kRow;
+  const int64_t blk_words = static_cast<int64_t>(kBlock) * a.kv_heads;
   r.kmask = 0u;
 #pragma unroll
   for (int i = 0; i < R::kKChunks; ++i) {
-    int t, ch;
-    k_item<KV>(tid + kStageThreads * i, t, ch);
-    bool ok;
-    const int64_t blk = safe_block(a, blks, t, tok0, L, ok);
-    const uint8_t* src = a.k + (blk * kBlock + t % kBlock) * head_row + h * R::kRow;
-    r.k[i] = __ldg(reinterpret_cast<const uint4*>(src) + ch);
-    r.kmask |= (ok && tok0 + t < L ? 1u : 0u) << i;
-    if constexpr (KvTraits<KV>::kQuant)
-      r.ksz4[i] = __ldg(a.k_sz + (blk * a.kv_heads + h) * kBlock + t % kBlock);
+    const int64_t blk = pick4(sb, m.kb[i]);
+    r.k[i] = __ldg(reinterpret_cast<const uint4*>(a.k + blk * blk_bytes + m.koff[i]));
+    r.kmask |= ((valid >> m.kb[i]) & 1u && tok0 + m.kt[i] < L ? 1u : 0u) << i;
+    if constexpr (KvTraits<KV>::kQuant && !QBF)
+      r.ksz4[i] = __ldg(a.k_sz + blk * blk_words + m.kszo[i]);
   }
   // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
-  const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
-  const int tv = 8 * tg;
-  bool vok;
-  const int64_t vblk = safe_block(a, blks, tv, tok0, L, vok);
-  const uint8_t* vrow =
-      a.v + (vblk * kBlock + tv % kBlock) * head_row + h * R::kRow + dc * 4 * R::kVWords;
+  const int tv = 8 * (tid & 7);
+  const int64_t vblk = pick4(sb, m.vb);
+  const uint8_t* vrow = a.v + vblk * blk_bytes + m.voff;
+  const int64_t head_row = static_cast<int64_t>(a.kv_heads) * R::kRow;
+  const bool vok = (valid >> m.vb) & 1u;
   r.vmask = 0u;
 #pragma unroll
   for (int t = 0; t < 8; ++t) r.vmask |= (vok && tok0 + tv + t < L ? 1u : 0u) << t;
-  if constexpr (KvTraits<KV>::kQuant) {  // 8 consecutive words: two 16-byte loads
-    const uint4* vs = reinterpret_cast<const uint4*>(a.v_sz + (vblk * a.kv_heads + h) * kBlock +
-                                                     tv % kBlock);
+  if constexpr (KvTraits<KV>::kQuant && !QBF) {  // 8 consecutive words: two 16-byte loads
+    const uint4* vs = reinterpret_cast<const uint4*>(a.v_sz + vblk * blk_words + m.vszo);
     const uint4 w0 = __ldg(vs), w1 = __ldg(vs + 1);
     r.vsz8[0] = w0.x; r.vsz8[1] = w0.y; r.vsz8[2] = w0.z; r.vsz8[3] = w0.w;
     r.vsz8[4] = w1.x; r.vsz8[5] = w1.y; r.vsz8[6] = w1.z; r.vsz8[7] = w1.w;
@@ -259,12 +296,11 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const int4& blks,
   r.sz_ok = false;
   r.ksz = r.vsz = 0u;
   if (tid < kTcTok) {
-    bool ok;
-    const int64_t blk = safe_block(a, blks, tid, tok0, L, ok);
+    const bool ok = (valid >> (tid / kBlock)) & 1u;
     r.sz_ok = ok && tok0 + tid < L;
     r.miss = tok0 + tid < L && !ok;
-    if constexpr (KvTraits<KV>::kQuant) {
-      const int64_t i = (blk * a.kv_heads + h) * kBlock + tid % kBlock;
+    if constexpr (KvTraits<KV>::kQuant && QBF) {  // the scale arrays of the exact path
+      const int64_t i = pick4(sb, tid / kBlock) * blk_words + h * kBlock + tid % kBlock;
       r.ksz = __ldg(a.k_sz + i);
       r.vsz = __ldg(a.v_sz + i);
     }
@@ -633,11 +669,13 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
     // sets; one for fp16 rows), its block ids one tile before that
     const int n = w.ntiles, L = w.s.L;
     constexpr int kSets = 1;  // raw register sets in flight
+    StageMap<KV> map;
+    map.init(a, w.h, tid);
     RawTile<KV> raw[kSets];
     int4 blk = tile_blocks(bt, 0, a.max_blocks);
 #pragma unroll
     for (int e = 0; e < kSets; ++e) {
-      if (e < n) load_tile<KV>(a, blk, e * kTcTok, L, w.h, tid, raw[e]);
+      if (e < n) load_tile<KV, QBF>(a, map, blk, e * kTcTok, L, w.h, tid, raw[e]);
       blk = tile_blocks(bt, (e + 1) * kTcTok, a.max_blocks);
     }
     auto stage_one = [&](int j, RawTile<KV>& r) {
@@ -651,7 +689,7 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
       mbar_arrive_one(c.bar(kBarKvFull + st));
       ++tc;
       if (j + kSets < n) {
-        load_tile<KV>(a, blk, (j + kSets) * kTcTok, L, w.h, tid, r);
+        load_tile<KV, QBF>(a, map, blk, (j + kSets) * kTcTok, L, w.h, tid, r);
         blk = tile_blocks(bt, (j + kSets + 1) * kTcTok, a.max_blocks);
       }
       return true;
