@@ -68,7 +68,7 @@ def test_split_counts_agree(gpu, name, splits):
 @pytest.mark.parametrize("kv_dtype,in_dtype", [("int8", "f16"), ("int4", "f16"),
                                                ("int8", "bf16"), ("int4", "bf16"),
                                                ("f16", "f16"), ("bf16", "bf16")])
-@pytest.mark.parametrize("heads", [(8, 8), (16, 4), (12, 4), (16, 1), (32, 2)])
+@pytest.mark.parametrize("heads", [(8, 8), (16, 4), (12, 4), (16, 1), (32, 2), (64, 16)])
 def test_dtypes_and_groups(gpu, kv_dtype, in_dtype, heads):
     Hq, Hkv = heads
     lens = [1, 15, 16, 17, 31, 33, 250, 513]
