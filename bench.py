@@ -46,7 +46,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="cfg3", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5"])
+    p.add_argument("--workload", default="cfg3",
+                   choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "cfg4_long_prefix"])
     p.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
@@ -502,21 +503,11 @@ def time_store(kvq, pool, wl, d_k, d_v, d_slots, dev, peak: float, reps: int = 1
             "l2": "flushed before every call", "cuda_graph": True, "reps": reps}
 
 
-def measure_workload(kvq, name: str, dev, peak: float, reps: int = 100) -> dict:
-    """One workload's decode call (paged_decode_attn: decode + combine kernels,
-    graph-replayed, CUDA events on the launching stream) and its store
-    (kv_store_quant of the step's tokens: each request's new token and, for
-    the mixed step, the 4096-token prefill chunk).
-
-    The decode is timed with a cold L2: a pool larger than L2 is read anew by
-    every call; a pool that fits is replicated R times (R x bytes >= 3 x L2)
-    and the calls rotate over the replicas, as the layers of a model would.
-    The warm-L2 time (one pool, back to back) is reported beside it. The
-    store is timed with L2 flushed (a write larger than L2) before every
-    call, outside the timed events."""
+def stored_workload(kvq, wl, dev):
+    """The workload's pool with its context and the step's new tokens stored
+    through kv_store_quant, its block tables from kvq_block_tables_from_req_to_token,
+    and the step's queries and lengths on the device."""
     import torch
-
-    wl = synthetic.by_name(name)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
 
     def to_dev(bits, dt):
@@ -535,21 +526,135 @@ def measure_workload(kvq, name: str, dev, peak: float, reps: int = 100) -> dict:
     bt = torch.empty((wl.batch, wl.max_blocks_per_seq), dtype=torch.int32, device=dev)
     kvq.kvq_block_tables_from_req_to_token(i32(wl.req_to_token), i32(wl.req_pool_indices),
                                            i32(wl.seq_lens), bt, err)
-    q = to_dev(wl.q(), wl.q_dtype)
-    sl = i32(wl.seq_lens)
-    out = torch.empty_like(q)
-    ws = torch.empty(max(16, kvq.paged_decode_attn_workspace_size(
-        wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, 0)), dtype=torch.uint8, device=dev)
-    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
-    alg, logical = decode_algorithmic_bytes(wl), decode_logical_bytes(wl)
-    pool_bytes = pool.nbytes()
-    R = 1 if pool_bytes > 3 * l2 else -(-3 * l2 // pool_bytes)
+    return pool, bt, to_dev(wl.q(), wl.q_dtype), i32(wl.seq_lens), err, (d_k, d_v, d_slots)
+
+
+def replica_pools(kvq, pool, l2: int):
+    """The pool and enough copies of it that the copies together hold at least
+    3 x L2 (just the pool when it alone is larger): calls rotated over them
+    start with a cold L2."""
+    nb = pool.nbytes()
+    R = 1 if nb > 3 * l2 else -(-3 * l2 // nb)
     pools = [pool]
     for _ in range(R - 1):
         pools.append(kvq.KVPool(pool.k.clone(), pool.v.clone(),
                                 None if pool.k_sz is None else pool.k_sz.clone(),
                                 None if pool.v_sz is None else pool.v_sz.clone(),
                                 pool.num_blocks, pool.kv_heads, pool.kv_dtype))
+    return pools
+
+
+def time_rotated(graphs, reps: int, stream) -> list:
+    """CUDA-event times (ms) of `reps` graph replays rotated over `graphs`,
+    after a warm-up in the same rotation."""
+    import torch
+    R = len(graphs)
+    for i in range(3 * R):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i, (e0, e1) in enumerate(ev):
+        e0.record(stream)
+        graphs[i % R].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def measure_shared_prefix(kvq, dev, peak: float, reps: int = 60) -> dict:
+    """The shared-prefix (cascade) decode against the plain decode on the
+    same pool and GPU: cfg4's structure with an 8192-token prefix that all 64
+    requests hold ("pymllm Runtime Design", KV cache and prefix cache: a
+    radix hit shares leading blocks). Both graph-replayed over replica pools
+    (cold L2); the two outputs are checked against each other."""
+    import torch
+
+    wl = synthetic.cfg4_long_prefix()
+    members, shared = prefix_groups(wl)
+    pool, bt, q, sl, err, _ = stored_workload(kvq, wl, dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    groups = kvq.SharedPrefixGroups(i32([0, len(members)]), i32(members), i32([shared]), shared)
+    ws = torch.empty(max(16, kvq.paged_decode_attn_workspace_size(
+        wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, 0)), dtype=torch.uint8, device=dev)
+    sp_ws = torch.empty(kvq.paged_decode_attn_shared_prefix_workspace_size(
+        wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, shared, 0), dtype=torch.uint8,
+        device=dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    pools = replica_pools(kvq, pool, l2)
+    stream = torch.cuda.current_stream(dev)
+    outs, times = {}, {}
+    for mode in ("plain", "cascade"):
+        out = torch.empty_like(q)
+        graphs = []
+        for pl in pools:
+            if mode == "plain":
+                call = (lambda pl=pl: kvq.paged_decode_attn(pl, q, out, bt, sl, wl.max_seq_len,
+                                                            wl.sm_scale, 0, ws, err))
+            else:
+                call = (lambda pl=pl: kvq.paged_decode_attn_shared_prefix(
+                    pl, q, out, bt, sl, wl.max_seq_len, wl.sm_scale, groups, 0, sp_ws, err))
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            graphs.append(g)
+        times[mode] = time_rotated(graphs, reps, stream)
+        outs[mode] = out
+        del graphs
+    if kvq.kvq_check_error(err):
+        raise RuntimeError("device error word set by the shared-prefix measurement")
+    a, b = outs["plain"].double(), outs["cascade"].double()
+    diff = (a - b).abs()
+    agree = bool(((diff <= 2e-3) | (diff <= 1e-2 * b.abs())).all().item())
+    alg, logical = decode_algorithmic_bytes(wl), decode_logical_bytes(wl)
+    mp, mc = float(np.mean(times["plain"])), float(np.mean(times["cascade"]))
+    res = {
+        "workload": wl.description,
+        "members": len(members), "shared_tokens": 16 * shared,
+        "unique_bytes": alg, "logical_bytes": logical,
+        "plain": {"kernels": "decode_gqa_kernel + combine_kernel", "ms_mean": round(mp, 5),
+                  "unique_gbs": round(alg / (mp / 1e3) / 1e9, 1),
+                  "logical_gbs": round(logical / (mp / 1e3) / 1e9, 1)},
+        "cascade": {"kernels": "prefix_kernel + decode_kernel + combine_kernel",
+                    "ms_mean": round(mc, 5), "unique_gbs": round(alg / (mc / 1e3) / 1e9, 1),
+                    "frac": round(alg / (mc / 1e3) / 1e9 / peak, 4)},
+        "speedup": round(mp / mc, 3),
+        "outputs_agree": agree,
+        "l2": f"cold: {len(pools)} replica pools rotated ({pool.nbytes() / 1e6:.1f} MB each)",
+        "cuda_graph": True, "reps": reps,
+    }
+    del pools, pool, ws, sp_ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_workload(kvq, name: str, dev, peak: float, reps: int = 100) -> dict:
+    """One workload's decode call (paged_decode_attn: decode + combine kernels,
+    graph-replayed, CUDA events on the launching stream) and its store
+    (kv_store_quant of the step's tokens: each request's new token and, for
+    the mixed step, the 4096-token prefill chunk).
+
+    The decode is timed with a cold L2: a pool larger than L2 is read anew by
+    every call; a pool that fits is replicated R times (R x bytes >= 3 x L2)
+    and the calls rotate over the replicas, as the layers of a model would.
+    The warm-L2 time (one pool, back to back) is reported beside it. The
+    store is timed with L2 flushed (a write larger than L2) before every
+    call, outside the timed events."""
+    import torch
+
+    wl = synthetic.by_name(name)
+    pool, bt, q, sl, err, (d_k, d_v, d_slots) = stored_workload(kvq, wl, dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(16, kvq.paged_decode_attn_workspace_size(
+        wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, 0)), dtype=torch.uint8, device=dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    alg, logical = decode_algorithmic_bytes(wl), decode_logical_bytes(wl)
+    pool_bytes = pool.nbytes()
+    pools = replica_pools(kvq, pool, l2)
+    R = len(pools)
     graphs = []
     for pl in pools:
         call = (lambda pl=pl: kvq.paged_decode_attn(pl, q, out, bt, sl, wl.max_seq_len,
@@ -882,6 +987,7 @@ def run_ours(args, rank: int, world: int, dist):
                 extras["workloads"][name] = measure_workload(kvq, name, dev, peak)
         extras["kvq_copy_blocks"] = measure_block_copy(kvq, pool, wl, dev, peak)
         extras["paged_extend_attn"] = measure_extend(kvq, dev)
+        extras["shared_prefix"] = measure_shared_prefix(kvq, dev, peak)
         if fstep is not None:
             sep = kvq.DecodeStep(pool, wl.batch, wl.q_heads, wl.max_blocks_per_seq,
                                  wl.max_seq_len, tdt[wl.q_dtype], num_splits=args.num_splits,

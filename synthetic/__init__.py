@@ -427,6 +427,15 @@ def cfg4(seed: int = 3, batch: int = 64, median: int = 2048, sigma: float = 0.5,
                                f"sigma {sigma}) in [{lo},{hi}], shared {prefix_blocks}-block prefix")
 
 
+def cfg4_long_prefix(seed: int = 3, batch: int = 64) -> Workload:
+    """cfg4's structure (INT4 KV, 32q/8kv, one shared prefix) with an
+    8192-token (512-block) prefix that every request holds, lengths in
+    [8208, 9216]: the prefix is most of each request's context, so a
+    cascade that attends it once per group has most of the work to save."""
+    return cfg4(seed=seed, batch=batch, median=8704, sigma=0.05, lo=8208, hi=9216,
+                prefix_blocks=512)
+
+
 def cfg5(seed: int = 4, batch: int = 256, lo: int = 256, hi: int = 2048,
          chunk: int = 4096, slack_blocks: int = 256) -> Workload:
     lens = randint(seed, S_LENS, batch, lo, hi).astype(np.int32)
@@ -527,7 +536,8 @@ def cfg5_prefill(seed: int = 4, chunk: int = 4096) -> ExtendWorkload:
 
 
 def by_name(name: str, **kw) -> Workload:
-    return {"cfg1": cfg1, "cfg2": cfg2, "cfg3": cfg3, "cfg4": cfg4, "cfg5": cfg5}[name](**kw)
+    return {"cfg1": cfg1, "cfg2": cfg2, "cfg3": cfg3, "cfg4": cfg4, "cfg5": cfg5,
+            "cfg4_long_prefix": cfg4_long_prefix}[name](**kw)
 
 
 def custom(name: str, kv_dtype: str, lens, q_heads: int, kv_heads: int, seed: int = 7,
