@@ -78,17 +78,17 @@ constexpr uint32_t kSzOff = kVOff + kStages * kVBytes;
 constexpr uint32_t kInfoOff = kSzOff + kStages * kSzBytes;  // per stage: max S_v (2 halves), missing masks
 constexpr uint32_t kBarOff = kInfoOff + kStages * 16;
 // mbarriers (index: runs by stage or warpgroup)
-constexpr uint32_t kBarKvFull = 0;     // staging -> MMA, softmax (128 arrivals), per stage
-constexpr uint32_t kBarKvEmpty = 3;    // MMA commit: the stage's products are done
-constexpr uint32_t kBarSFull = 6;      // MMA commit: S_g is in TMEM
-constexpr uint32_t kBarPFull = 8;      // softmax g -> MMA (128 arrivals)
-constexpr uint32_t kBarODone = 10;     // MMA commit: O_g += P'_g V done
-constexpr uint32_t kBarQFull = 12;     // softmax g -> MMA: the unit's Q rows (128 arrivals)
-constexpr uint32_t kBarUnitFull = 14;  // unit slot written
-constexpr uint32_t kBarUnitEmpty = 16; // unit slot read by all 13 working warps
-constexpr uint32_t kBarSRead = 18;     // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
-constexpr uint32_t kBarDrain = 20;     // MMA commit before TMEM is freed
-constexpr uint32_t kNumBars = 21;
+constexpr uint32_t kBarKvFull = 0;                  // staging -> MMA, softmax (128 arrivals), per stage
+constexpr uint32_t kBarKvEmpty = kStages;           // MMA commit: the stage's products are done
+constexpr uint32_t kBarSFull = 2 * kStages;         // MMA commit: S_g is in TMEM
+constexpr uint32_t kBarPFull = kBarSFull + 2;       // softmax g -> MMA (128 arrivals)
+constexpr uint32_t kBarODone = kBarPFull + 2;       // MMA commit: O_g += P'_g V done
+constexpr uint32_t kBarQFull = kBarODone + 2;       // softmax g -> MMA: the unit's Q rows (128 arrivals)
+constexpr uint32_t kBarUnitFull = kBarQFull + 2;    // unit slot written
+constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by all 13 working warps
+constexpr uint32_t kBarSRead = kBarUnitEmpty + 2;   // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
+constexpr uint32_t kBarDrain = kBarSRead + 2;       // MMA commit before TMEM is freed
+constexpr uint32_t kNumBars = kBarDrain + 1;
 constexpr uint32_t kSlotOff = kBarOff + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kUnitOff = kSlotOff + 4;            // 2 unit slots
 constexpr uint32_t kAbortOff = kUnitOff + 8;
@@ -476,28 +476,17 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // ---- waits --------------------------------------------------------------------
 
-// try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or up to 0.5 ms have passed, instead of polling shared memory.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(500000u)
-      : "memory");
-  return done != 0;
-}
-
 // One thread's bounded wait on a barrier phase that also gives up when another
 // role has aborted the CTA (the flag at `abort_flag`); on its own timeout it
-// sets the flag and reports KVQ_DEV_ERR_TIMEOUT. The flag and the clock are
-// read only between sleeps.
+// sets the flag and reports KVQ_DEV_ERR_TIMEOUT. try_wait blocks in hardware
+// for a while; the flag and the clock are read only after 64 such tries.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int32_t* dev_err) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait_sleep(bar, parity)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
     if (global_ns() - t0 > 2000000000ull) {
       *abort_flag = 1;
