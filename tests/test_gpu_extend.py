@@ -179,3 +179,60 @@ def test_block_ids_outside_the_pool_are_skipped_and_reported(gpu, variant):
     assert np.isfinite(got).all()
     ref = _oracle(ew)
     assert_close(got[:300], ref[:300])
+
+
+@pytest.mark.parametrize("variant", ["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("kv_dtype,q_dtype", [("int8", "f16"), ("int4", "f16"), ("int8", "bf16")])
+@pytest.mark.parametrize("sm_scale", [0.0, -0.0625])
+def test_zero_and_negative_softmax_scales(gpu, kv_dtype, q_dtype, sm_scale, variant):
+    """A scale of 0 (uniform weights over the causal window) and a negative
+    scale (the maximum of s is the minimum of q.k): the fp16-query tcgen05
+    path applies such scales before the maximum instead of in the exponent."""
+    ew = synthetic.extend("exsc", kv_dtype, [300, 100], [300, 37], 32, 8, q_dtype=q_dtype)
+    wl = ew.wl
+    pool = _stored_pool(wl)
+    kvq = _kvq()
+    q = to_dev(ew.q_ext(), wl.q_dtype)
+    out = torch.full_like(q, float("nan"))
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = kvq.paged_extend_attn_workspace_size(wl.batch, ew.total_q, wl.q_heads, wl.kv_heads,
+                                              wl.max_seq_len)
+    w = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), i32(ew.kv_lens),
+                          i32(wl.block_tables), wl.max_seq_len, sm_scale, w, dev_err,
+                          variant=variant)
+    assert gpu.kvq_check_error(dev_err) == 0
+    opool, _ = oracle.run_workload(wl)
+    ref = oracle.paged_extend(opool, ew.q_ext(), wl.q_dtype, ew.qo_indptr, wl.block_tables,
+                              ew.kv_lens, sm_scale)
+    assert_close(out_to_f64(out), ref)
+
+
+def test_tcgen05_refuses_batches_above_4096(gpu):
+    """The tcgen05 variant keeps its per-request unit table in shared memory
+    and takes at most 4096 requests; a larger batch is refused before
+    anything launches (AUTO takes the mma.sync kernel for it)."""
+    kvq = _kvq()
+    n = 4097
+    ew = synthetic.extend("exr", "int8", [1] * n, [1] * n, 16, 8)
+    wl = ew.wl
+    pool = _stored_pool(wl)
+    q = to_dev(ew.q_ext(), wl.q_dtype)
+    out = torch.zeros_like(q)
+    ws = kvq.paged_extend_attn_workspace_size(wl.batch, ew.total_q, wl.q_heads, wl.kv_heads,
+                                              wl.max_seq_len)
+    w = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), i32(ew.kv_lens),
+                              i32(wl.block_tables), wl.max_seq_len, wl.sm_scale, w,
+                              variant="tcgen05")
+    assert e.value.status == 2  # KVQ_ERR_UNSUPPORTED
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.paged_extend_attn(pool, q, out, i32(ew.qo_indptr), i32(ew.kv_lens),
+                          i32(wl.block_tables), wl.max_seq_len, wl.sm_scale, w, dev_err)
+    assert gpu.kvq_check_error(dev_err) == 0
+    # one token attending itself: the output is that token's dequantized V
+    opool, _ = oracle.run_workload(wl)
+    ref = oracle.paged_extend(opool, ew.q_ext()[:64], wl.q_dtype, ew.qo_indptr[:65],
+                              wl.block_tables[:64], ew.kv_lens[:64], wl.sm_scale)
+    assert_close(out_to_f64(out[:64]), ref)
