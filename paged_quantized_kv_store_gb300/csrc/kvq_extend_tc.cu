@@ -5,19 +5,20 @@
 // extend / prefill; LMDeploy article §2.3: prefills split into chunks; §2.4:
 // per-token, per-head INT8/INT4 scale and zero). A work unit is 256 rows
 // (query, q head) of one kv head; the request's context is walked in tiles
-// of 64 tokens (4 blocks). One CTA per SM, thirteen warps in four roles:
+// of 64 tokens (4 blocks). One CTA per SM, fourteen working warps in four roles:
 //   * staging warpgroup (warps 8-11): reads each tile's codes from the pool
 //     and writes K as centred 16-bit values c - mid (exact; Q's type) in a
 //     K-major 128-byte-swizzled tile and V as c - mid in fp16, transposed
 //     (dims as rows), into a two-stage ring, with the per-token scale S and
 //     shifted zero Z + mid S in four small arrays; it also hands out the work
 //     units (an atomic counter, longest tiles first);
-//   * MMA warp (warp 12; one elected lane issues): S_g = Q_g K^T (M 128, N 64,
-//     K 128) for both softmax warpgroups into their own TMEM columns, the
-//     next tile's S_g as soon as warpgroup g has read the current one out of
-//     TMEM (so it runs during that warpgroup's exponentials), and
-//     O_g += P'_g V (M 128, N 128, K 64) as soon as warpgroup g's P' is
-//     ready; the two warpgroups' products interleave on the tensor core;
+//   * two MMA warps (warps 12 and 13, one per softmax warpgroup g, on
+//     different sub-partitions; one elected lane issues): S_g = Q_g K^T
+//     (M 128, N 64, K 128) into the warpgroup's own TMEM columns, the next
+//     tile's S_g as soon as warpgroup g has read the current one out of TMEM
+//     (so it runs during that warpgroup's exponentials), and O_g += P'_g V
+//     (M 128, K 64) as soon as warpgroup g's P' is ready; the two
+//     warpgroups' products interleave on the tensor core;
 //   * two softmax warpgroups (warps 0-3, 4-7), one thread per row: read the
 //     row of S (tcgen05.ld), apply s = S_k (q.(c - mid)) + (Z_k + mid S_k)
 //     sum(q), the causal mask and the online softmax; when the running
@@ -46,8 +47,8 @@ constexpr int kUnitRows = 2 * kWgRows;    // rows per work unit
 constexpr int kTcTok = 64;                // tokens per context tile (N of S, K of P V)
 constexpr int kStageThreads = 128;        // staging warpgroup
 constexpr int kSoftWarps = 8;             // warps 0-7: softmax warpgroups 0 and 1
-constexpr int kMmaWarp = 12;              // warps 8-11 stage, warp 12 issues the MMAs
-constexpr int kTcThreads = 16 * 32;       // four warpgroups; warps 13-15 only hold registers
+constexpr int kMmaWarp = 12;              // warps 8-11 stage, warps 12 and 13 issue the MMAs
+constexpr int kTcThreads = 16 * 32;       // four warpgroups; warps 14-15 only hold registers
 // Registers per thread after the split (setmaxnreg): the launch gives every
 // thread 65536 / 512 = 128; the staging and MMA warpgroups give theirs back
 // down to kLowRegs, the softmax warpgroups take them up to kHighRegs.
@@ -85,7 +86,7 @@ constexpr uint32_t kBarPFull = kBarSFull + 2;       // softmax g -> MMA (128 arr
 constexpr uint32_t kBarODone = kBarPFull + 2;       // MMA commit: O_g += P'_g V done
 constexpr uint32_t kBarQFull = kBarODone + 2;       // softmax g -> MMA: the unit's Q rows (128 arrivals)
 constexpr uint32_t kBarUnitFull = kBarQFull + 2;    // unit slot written
-constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by all 13 working warps
+constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by all 14 working warps
 constexpr uint32_t kBarSRead = kBarUnitEmpty + 2;   // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
 constexpr uint32_t kBarDrain = kBarSRead + 2;       // MMA commit before TMEM is freed
 constexpr uint32_t kNumBars = kBarDrain + 1;
@@ -639,7 +640,7 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
   for (uint32_t k = 0;; ++k) {
     const uint32_t slot = k & 1u;
     if (tid == 0) {
-      // the slot of unit k - 2 must have been read by all 13 warps
+      // the slot of unit k - 2 must have been read by all 14 working warps
       if (k < 2 || wait_or_abort(c.bar(kBarUnitEmpty + slot), ((k >> 1) - 1u) & 1u, c.abort_flag,
                                  a.dev_err)) {
         c.unit_slot[slot] = atomicAdd(a.counter, 1);
@@ -700,42 +701,43 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// The MMA warp: all 32 lanes run the loop (so the descriptors stay
-// warp-uniform) and wait together; one elected lane issues each product and
-// commit.
+// An MMA warp, one per softmax warpgroup g (warp 12 for g = 0, 13 for g = 1,
+// on different sub-partitions, so the two issue in parallel): all 32 lanes
+// run the loop (the descriptors stay warp-uniform) and wait together; one
+// elected lane issues each product and commit. The two warpgroups' products
+// need no order between them; a K/V stage is released when both MMA warps
+// have committed its products (the empty barrier takes two arrivals).
 template <bool QBF>
-__device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c, int lane) {
+__device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c, int g,
+                                         int lane) {
   constexpr uint32_t idesc_s = umma_idesc_f16(QBF, kWgRows, kTcTok);
   constexpr uint32_t idesc_o = umma_idesc_f16(false, kWgRows, o_cols<QBF>());
   // descriptors of k-step 0; a k-step adds its byte offset / 16 to the low field
-  const uint64_t q_desc0 = umma_desc_sw128(c.base + kQOff, 1024);
+  const uint64_t q_desc0 = umma_desc_sw128(c.base + kQOff + g * kQBytes, 1024);
   const uint64_t k_desc0 = umma_desc_sw128(c.base + kKOff, 1024);
   const uint64_t v_desc0 = umma_desc_sw128(c.base + kVOff, 1024);
-  auto issue_s = [&](int g, uint32_t st) {
-    const uint64_t qd = q_desc0 + (g * kQBytes >> 4), kd = k_desc0 + (st * kKBytes >> 4);
+  const uint32_t s_tmem = c.tmem + 64u * g, o_tmem = c.tmem + 128u + o_cols<QBF>() * g;
+  const uint32_t p_tmem = c.tmem + p_col<QBF>() + 32u * g;
+  auto issue_s = [&](uint32_t st) {
+    const uint64_t kd = k_desc0 + (st * kKBytes >> 4);
     if (elect_one()) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        umma_f16(c.tmem + 64u * g, qd + (((k >> 2) * (kWgRows * 128) + (k & 3) * 32) >> 4),
+        umma_f16(s_tmem, q_desc0 + (((k >> 2) * (kWgRows * 128) + (k & 3) * 32) >> 4),
                  kd + (((k >> 2) * (kTcTok * 128) + (k & 3) * 32) >> 4), idesc_s, k > 0);
       umma_commit(c.bar(kBarSFull + g));
     }
     __syncwarp();
   };
-  auto issue_o = [&](int g, uint32_t st, bool acc) {
+  auto issue_o = [&](uint32_t st, bool acc) {
     const uint64_t vd = v_desc0 + (st * kVBytes >> 4);
     if (elect_one()) {
 #pragma unroll
       for (int k = 0; k < kTcTok / 16; ++k)
-        umma_f16_tmem_a(c.tmem + 128u + o_cols<QBF>() * g,
-                        c.tmem + p_col<QBF>() + 32u * g + 8u * k, vd + ((k * 32) >> 4), idesc_o,
-                        acc || k > 0);
+        umma_f16_tmem_a(o_tmem, p_tmem + 8u * k, vd + ((k * 32) >> 4), idesc_o, acc || k > 0);
       umma_commit(c.bar(kBarODone + g));
+      umma_commit(c.bar(kBarKvEmpty + st));  // this warpgroup is done with the stage
     }
-    __syncwarp();
-  };
-  auto commit = [&](uint32_t bar) {
-    if (elect_one()) umma_commit(bar);
     __syncwarp();
   };
   auto wait = [&](uint32_t b, uint32_t parity) {
@@ -752,27 +754,20 @@ __device__ __forceinline__ void mma_role(const ExtendArgs& a, const TcShared& c,
     if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
     if (u >= c.total) return;
     const int n = tc_unit(a, c.ucum, u).ntiles;
-    if (!wait(c.bar(kBarQFull + 0), k & 1u) || !wait(c.bar(kBarQFull + 1), k & 1u)) return;
+    if (!wait(c.bar(kBarQFull + g), k & 1u)) return;
     if (!wait(c.bar(kBarKvFull + tc % kStages), (tc / kStages) & 1u)) return;
-    issue_s(0, tc % kStages);
-    issue_s(1, tc % kStages);
+    issue_s(tc % kStages);
     for (int j = 0; j < n; ++j, ++tc) {
       const uint32_t st = tc % kStages, nx = (tc + 1u) % kStages;
-      const bool more = j + 1 < n;
-      // S_g of the next tile as soon as warpgroup g has read this one out of
+      // S of the next tile as soon as the warpgroup has read this one out of
       // TMEM: it runs while the warpgroup computes this tile's P'
-      if (!wait(c.bar(kBarSRead + 0), tc & 1u)) return;
-      if (more) {
+      if (!wait(c.bar(kBarSRead + g), tc & 1u)) return;
+      if (j + 1 < n) {
         if (!wait(c.bar(kBarKvFull + nx), ((tc + 1u) / kStages) & 1u)) return;
-        issue_s(0, nx);
+        issue_s(nx);
       }
-      if (!wait(c.bar(kBarSRead + 1), tc & 1u)) return;
-      if (more) issue_s(1, nx);
-      if (!wait(c.bar(kBarPFull + 0), tc & 1u)) return;
-      issue_o(0, st, j > 0);
-      if (!wait(c.bar(kBarPFull + 1), tc & 1u)) return;
-      issue_o(1, st, j > 0);
-      commit(c.bar(kBarKvEmpty + st));  // the stage is free once these products finish
+      if (!wait(c.bar(kBarPFull + g), tc & 1u)) return;
+      issue_o(st, j > 0);
     }
   }
 }
@@ -1040,7 +1035,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init_count(c.bar(kBarKvFull + s), kStageThreads);
-      mbar_init_count(c.bar(kBarKvEmpty + s), 1);
+      mbar_init_count(c.bar(kBarKvEmpty + s), 2);  // one commit per MMA warp
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init_count(c.bar(kBarSFull + s), 1);
@@ -1048,10 +1043,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
       mbar_init_count(c.bar(kBarODone + s), 1);
       mbar_init_count(c.bar(kBarQFull + s), kWgRows);
       mbar_init_count(c.bar(kBarUnitFull + s), 1);
-      mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 1);  // every warp's lane 0
+      mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 2);  // every warp's lane 0
       mbar_init_count(c.bar(kBarSRead + s), kWgRows);
     }
-    mbar_init_count(c.bar(kBarDrain), 1);
+    mbar_init_count(c.bar(kBarDrain), 2);  // one commit per MMA warp
     *c.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1070,9 +1065,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
     staging_role<KV, QBF>(a, c, tid - kSoftWarps * 32);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
-    if (warp == kMmaWarp) {
-      mma_role<QBF>(a, c, lane);
-      // every product this warp issued completes before the TMEM is freed
+    if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      mma_role<QBF>(a, c, warp - kMmaWarp, lane);
+      // every product either MMA warp issued completes before the TMEM is freed
       __syncwarp();
       if (elect_one()) {
         umma_commit(c.bar(kBarDrain));
