@@ -296,16 +296,21 @@ def measure_block_copy(kvq, pool, wl, dev, peak: float, n_cow: int = 4096, n_swa
                            .astype(np.int32)).to(dev)
 
     def timed(fn):
+        # 5 warm-up calls, then three batches of `reps` back-to-back calls,
+        # each batch bracketed by CUDA events; the median batch's mean
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        batches = []
         for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            batches.append(e0.elapsed_time(e1) / reps)
+        return sorted(batches)[1]
 
     out = {"block_bytes": block_bytes}
     dst = kvq.KVPool.allocate(n_cow, wl.kv_heads, wl.kv_dtype, device=dev)
@@ -388,7 +393,7 @@ def measured_tensor_peak():
     return 1900.0, "fallback"
 
 
-def measure_extend(kvq, dev, reps: int = 10) -> dict:
+def measure_extend(kvq, dev, reps: int = 20) -> dict:
     """paged_extend_attn on the mixed step's prefill chunk alone: one fresh
     4096-token prompt chunk over INT8 KV (GQA 32q/8kv), stored, then attended
     causally. FLOPs: 4 * head_dim * q_heads * sum over queries of (position + 1);
@@ -421,16 +426,21 @@ def measure_extend(kvq, dev, reps: int = 10) -> dict:
     err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def timed(fn):
+        # 5 warm-up calls, then three batches of `reps` back-to-back calls,
+        # each batch bracketed by CUDA events; the median batch's mean
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        batches = []
         for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            batches.append(e0.elapsed_time(e1) / reps)
+        return sorted(batches)[1]
 
     C = ew.total_q
     flops = 4.0 * wl.head_dim * wl.q_heads * (C * (C + 1) / 2)
