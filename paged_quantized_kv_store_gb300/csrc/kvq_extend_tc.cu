@@ -7,31 +7,34 @@
 // (query, q head) of one kv head; the request's context is walked in tiles
 // of 64 tokens (4 blocks). One CTA per SM, fourteen working warps in four roles:
 //   * staging warpgroup (warps 8-11): reads each tile's codes from the pool
-//     and writes K as centred 16-bit values c - mid (exact; Q's type) in a
-//     K-major 128-byte-swizzled tile and V as c - mid in fp16, transposed
-//     (dims as rows), into a two-stage ring, with the per-token scale S and
-//     shifted zero Z + mid S in four small arrays; it also hands out the work
-//     units (an atomic counter, longest tiles first);
+//     (per-thread addresses fixed for the unit, the tile's four block ids
+//     fetched a tile ahead) and writes K in a K-major 128-byte-swizzled tile
+//     and V transposed (dims as rows) into a three-stage ring; it also hands
+//     out the work units (an atomic counter, longest tiles first);
 //   * two MMA warps (warps 12 and 13, one per softmax warpgroup g, on
 //     different sub-partitions; one elected lane issues): S_g = Q_g K^T
 //     (M 128, N 64, K 128) into the warpgroup's own TMEM columns, the next
 //     tile's S_g as soon as warpgroup g has read the current one out of TMEM
-//     (so it runs during that warpgroup's exponentials), and O_g += P'_g V
-//     (M 128, K 64) as soon as warpgroup g's P' is ready; the two
-//     warpgroups' products interleave on the tensor core;
+//     (so it runs during that warpgroup's exponentials), and O_g += P_g V
+//     (M 128, K 64, A read from TMEM) as soon as warpgroup g's P is ready;
 //   * two softmax warpgroups (warps 0-3, 4-7), one thread per row: read the
-//     row of S (tcgen05.ld), apply s = S_k (q.(c - mid)) + (Z_k + mid S_k)
-//     sum(q), the causal mask and the online softmax; when the running
-//     maximum moves by more than a threshold, rescale the warp's rows of O in
-//     TMEM (a stale maximum only scales every term alike); write
-//     P' = p S_v in fp16 to its own TMEM columns, from which the P' V product
-//     reads its A operand, and keep sum p (Z_v + mid S_v) in registers. At
-//     the end of the unit: (O + z) / l.
-// The per-token arithmetic runs on paired fp32 instructions (two tokens per
-// instruction). Roles meet only at mbarriers (no CTA-wide barrier inside the
-// work loop); every wait is bounded (2 s, then KVQ_DEV_ERR_TIMEOUT and every
-// role leaves its loop), and the MMA thread waits for its products in flight
-// before the CTA frees its TMEM.
+//     row of S (tcgen05.ld), mask (causal, missing blocks), apply the online
+//     softmax with a lazily moved maximum (a stale maximum only scales every
+//     term alike; O is rescaled in TMEM when it moves), and write P to their
+//     own TMEM columns (tcgen05.st).
+// Numerics by query type:
+//   * fp16 queries: K and V are staged dequantized, (c - mid) S + (Z + mid S)
+//     in fp16 with one rounding; P = 2^(s - m) is computed as fp16 pairs, and
+//     V's tile carries a row of ones, so the P V product also gives the row
+//     sum over the same fp16 P. Output: O / l.
+//   * bf16 queries: the codes stay exact (K as c - mid in bf16, V as c - mid
+//     in fp16); s = S_k (q.(c - mid)) + (Z_k + mid S_k) sum(q) from per-token
+//     arrays, P' = p S_v in fp16, and sum p and sum p (Z_v + mid S_v) in fp32
+//     registers. Output: (O + z) / l.
+// Roles meet only at mbarriers (no CTA-wide barrier inside the work loop);
+// every wait is bounded (2 s, then KVQ_DEV_ERR_TIMEOUT and every role leaves
+// its loop), and the MMA warps wait for their products in flight before the
+// CTA frees its TMEM.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
