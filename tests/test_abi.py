@@ -231,6 +231,11 @@ def test_extend_validation(lib):
     assert call(q=p + 8) == 1              # misaligned
     assert call(var=3) == 1 and call(var=-1) == 1
     assert call(var=2, pool=_pool(kv_dtype=kvq.KVQ_BF16), q_dtype=kvq.KVQ_BF16) == 2
+    # the tcgen05 kernel: at most 4096 requests (its unit table lives in shared
+    # memory), and a pool with at least one block (a missing block is read
+    # from block 0 and masked); both refused before anything launches
+    assert call(var=2, batch=4097) == 2
+    assert call(var=2, pool=_pool(num_blocks=0)) == 2
 
 
 def test_decode_step_validation(lib):
