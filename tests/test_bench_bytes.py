@@ -50,3 +50,20 @@ def test_shared_prefix_is_counted_once():
             extra += (readers - 1) * 16 * wl.kv_token_bytes()
     assert extra > 0
     assert (bench.decode_logical_bytes(wl) - bench.decode_algorithmic_bytes(wl)) == extra
+
+
+def test_long_prefix_is_read_once_by_the_cascade_workload():
+    """The cascade comparison's workload: 64 INT4 requests that all hold the
+    same 512-block (8192-token) prefix. Algorithmic bytes count the prefix
+    once, logical bytes 64 times, so they differ by 63 prefixes; the prefix
+    is the one group prefix_groups returns."""
+    wl = synthetic.cfg4_long_prefix()
+    assert wl.batch == 64 and wl.kv_dtype == "int4"
+    assert np.all(np.asarray(wl.shared_tokens) == 8192)
+    assert np.all((wl.seq_lens >= 8208) & (wl.seq_lens <= 9216))
+    token = wl.kv_token_bytes()
+    assert token == 2 * 8 * (64 + 4)
+    gap = bench.decode_logical_bytes(wl) - bench.decode_algorithmic_bytes(wl)
+    assert gap == 63 * 8192 * token
+    members, shared = bench.prefix_groups(wl)
+    assert shared == 512 and sorted(members) == list(range(64))
