@@ -1199,7 +1199,7 @@ def main():
 
         import paged_quantized_kv_store_gb300 as kvq
         kvq.load()
-        res = {"paged_extend_attn": measure_extend(kvq, torch.device("cuda"), reps=3)}
+        res = {"paged_extend_attn": measure_extend(kvq, torch.device("cuda"))}
     elif args.impl == "reference":
         res = run_reference(args, rank)
     else:

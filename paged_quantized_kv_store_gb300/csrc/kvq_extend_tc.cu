@@ -5,12 +5,18 @@
 // extend / prefill; LMDeploy article §2.3: prefills split into chunks; §2.4:
 // per-token, per-head INT8/INT4 scale and zero). A work unit is 256 rows
 // (query, q head) of one kv head; the request's context is walked in tiles
-// of 64 tokens (4 blocks). One CTA per SM, fourteen working warps in four roles:
-//   * staging warpgroup (warps 8-11): reads each tile's codes from the pool
-//     (per-thread addresses fixed for the unit, the tile's four block ids
-//     fetched a tile ahead) and writes K in a K-major 128-byte-swizzled tile
-//     and V transposed (dims as rows) into a three-stage ring; it also hands
-//     out the work units (an atomic counter, longest tiles first);
+// of 64 tokens (4 blocks). One CTA per SM, fourteen working warps (fifteen
+// for INT8 pools) in five roles:
+//   * raw-ring producer (warp 14, INT8 pools): hands out the work units (an
+//     atomic counter, longest tiles first) and copies each tile's raw codes
+//     and scale/zero words by TMA into a two-stage raw ring, one box per
+//     (block, K or V), two tiles ahead of the staging warpgroup;
+//   * staging warpgroup (warps 8-11): takes each tile's codes from the raw
+//     ring (INT8) or straight from the pool (other kinds: per-thread
+//     addresses fixed for the unit, the tile's four block ids fetched a tile
+//     ahead; these pools' units are handed out here) and writes K in a
+//     K-major 128-byte-swizzled tile and V transposed (dims as rows) into a
+//     three-stage ring;
 //   * two MMA warps (warps 12 and 13, one per softmax warpgroup g, on
 //     different sub-partitions; one elected lane issues): S_g = Q_g K^T
 //     (M 128, N 64, K 128) into the warpgroup's own TMEM columns, the next
@@ -51,7 +57,8 @@ constexpr int kTcTok = 64;                // tokens per context tile (N of S, K 
 constexpr int kStageThreads = 128;        // staging warpgroup
 constexpr int kSoftWarps = 8;             // warps 0-7: softmax warpgroups 0 and 1
 constexpr int kMmaWarp = 12;              // warps 8-11 stage, warps 12 and 13 issue the MMAs
-constexpr int kTcThreads = 16 * 32;       // four warpgroups; warps 14-15 only hold registers
+constexpr int kTcThreads = 16 * 32;       // four warpgroups; warp 14 copies the raw codes of
+                                          // INT8 pools, warp 15 only holds registers
 // Registers per thread after the split (setmaxnreg): the launch gives every
 // thread 65536 / 512 = 128; the staging and MMA warpgroups give theirs back
 // down to kLowRegs, the softmax warpgroups take them up to kHighRegs.
@@ -80,7 +87,21 @@ constexpr uint32_t kKOff = kQOff + 2 * kQBytes;     // K tile of stage s at s * 
 constexpr uint32_t kVOff = kKOff + kStages * kKBytes;
 constexpr uint32_t kSzOff = kVOff + kStages * kVBytes;
 constexpr uint32_t kInfoOff = kSzOff + kStages * kSzBytes;  // per stage: max S_v (2 halves), missing masks
-constexpr uint32_t kBarOff = kInfoOff + kStages * 16;
+// Raw ring (INT8 pools): a tile's codes as the TMA copies land them. Stage:
+// the K rows of its four blocks (one box per block: 16 rows of 128 bytes,
+// 128-byte swizzle, so tile token t sits at row t), the V rows likewise,
+// the 64 K and 64 V scale/zero words, and the four blocks' valid bits.
+constexpr int kRawStages = 2;
+constexpr uint32_t kRawBox = kBlock * 128;                 // one (block, kv head) box
+constexpr uint32_t kRawVOff = 4 * kRawBox;
+constexpr uint32_t kRawSzOff = 8 * kRawBox;                // K words [64], then V words [64]
+constexpr uint32_t kRawValidOff = kRawSzOff + 2 * kTcTok * 4;
+constexpr uint32_t kRawTx = 8 * kRawBox + 2 * kTcTok * 4;  // bytes the copies of a stage bring
+constexpr uint32_t kRawBytes = (kRawValidOff + 16 + 1023) / 1024 * 1024;
+constexpr uint32_t kRawOff = (kInfoOff + kStages * 16 + 1023) / 1024 * 1024;
+template <int KV>
+constexpr bool raw_ring() { return KV == kI8; }
+constexpr uint32_t kBarOff = kRawOff + kRawStages * kRawBytes;
 // mbarriers (index: runs by stage or warpgroup)
 constexpr uint32_t kBarKvFull = 0;                  // staging -> MMA, softmax (128 arrivals), per stage
 constexpr uint32_t kBarKvEmpty = kStages;           // MMA commit: the stage's products are done
@@ -92,7 +113,9 @@ constexpr uint32_t kBarUnitFull = kBarQFull + 2;    // unit slot written
 constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by all 14 working warps
 constexpr uint32_t kBarSRead = kBarUnitEmpty + 2;   // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
 constexpr uint32_t kBarDrain = kBarSRead + 2;       // MMA commit before TMEM is freed
-constexpr uint32_t kNumBars = kBarDrain + 1;
+constexpr uint32_t kBarRawFull = kBarDrain + 1;     // raw stage landed (TMA bytes), per raw stage
+constexpr uint32_t kBarRawEmpty = kBarRawFull + kRawStages;  // raw stage read (128 arrivals)
+constexpr uint32_t kNumBars = kBarRawEmpty + kRawStages;
 constexpr uint32_t kSlotOff = kBarOff + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kUnitOff = kSlotOff + 4;            // 2 unit slots
 constexpr uint32_t kAbortOff = kUnitOff + 8;
@@ -103,6 +126,9 @@ constexpr int kTcMaxBatch = 4096;
 __host__ __device__ constexpr size_t tc_smem_bytes(int batch) {
   return 1024 + kFixedBytes + align128((batch + 1) * sizeof(int32_t));
 }
+// the opt-in shared-memory limit of a CTA on sm_100-class GPUs (227 KB),
+// with the kernel's static shared memory (1 KB as placed)
+static_assert(tc_smem_bytes(kTcMaxBatch) + 1024 <= 232448, "shared memory over the CTA limit");
 
 struct TcReq {
   int q0, C, L, tiles;
@@ -168,7 +194,9 @@ struct RawTile {
 // that staging item e (= thread + 128 i) moves. Eight neighbouring lanes take
 // 2 tokens x 4 chunks (INT8), 4 x 2 (INT4) or 1 x 8 (fp16): under the 128-byte
 // swizzle their 16-byte stores then land in eight different bank groups, and
-// a warp still reads whole token rows.
+// a warp still reads whole token rows. For INT8 the second token of a lane
+// group takes the other half of its row, so that the group's 16-byte reads
+// from the swizzled raw stage also fall in eight different bank groups.
 template <int KV>
 __device__ __forceinline__ void k_item(int e, int& t, int& ch) {
   constexpr int kChunks = RawTile<KV>::kRow / 16;  // 8 / 4 / 16 per token row
@@ -176,7 +204,25 @@ __device__ __forceinline__ void k_item(int e, int& t, int& ch) {
   constexpr int kTpg = 8 / kCpg;                   // tokens per lane group
   const int lane8 = e & 7, grp = e >> 3;
   t = kTpg * (grp >> 1) + lane8 / kCpg;
-  ch = kCpg * (grp & 1) + lane8 % kCpg;
+  const int half = KV == kI8 ? (grp & 1) ^ (lane8 / kCpg) : (grp & 1);
+  ch = kCpg * half + lane8 % kCpg;
+}
+
+// The V piece (8 consecutive tokens 8 tg .., 8 dims 8 dc ..) that staging
+// thread tid (0..127) transposes. The eight lanes of a quarter warp always
+// take eight different token groups, so their 16-byte stores of V^T rows hit
+// eight bank groups; for INT8 the sixteen lanes of a half warp also take the
+// sixteen dim groups, so that their 8-byte reads of one token row from the
+// raw stage are conflict-free.
+template <int KV>
+__device__ __forceinline__ void v_item(int tid, int& tg, int& dc) {
+  if constexpr (KV == kI8) {
+    dc = tid & 15;
+    tg = ((tid & 7) + (tid >> 4)) & 7;
+  } else {
+    tg = tid & 7;
+    dc = tid >> 3;
+  }
 }
 
 // Table entries of the tile's four blocks (tokens tok0 .. tok0 + 63). The
@@ -220,7 +266,9 @@ struct StageMap {
       koff[i] = (t % kBlock) * head_row + h * R::kRow + 16 * ch;
       kszo[i] = h * kBlock + t % kBlock;
     }
-    const int tv = 8 * (tid & 7), dc = tid >> 3;
+    int tg, dc;
+    v_item<KV>(tid, tg, dc);
+    const int tv = 8 * tg;
     vb = tv / kBlock;
     voff = (tv % kBlock) * head_row + h * R::kRow + dc * 4 * R::kVWords;
     vszo = h * kBlock + tv % kBlock;
@@ -268,7 +316,10 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const StageMap<KV
       r.ksz4[i] = __ldg(a.k_sz + blk * blk_words + m.kszo[i]);
   }
   // V: tokens 8 tg .. 8 tg + 7 (one block: 8 divides 16), dims 8 dc .. 8 dc + 7
-  const int tv = 8 * (tid & 7);
+  int tg, dc;
+  v_item<KV>(tid, tg, dc);
+  (void)dc;  // the V address is the map's
+  const int tv = 8 * tg;
   const int64_t vblk = pick4(sb, m.vb);
   const uint8_t* vrow = a.v + vblk * blk_bytes + m.voff;
   const int64_t head_row = static_cast<int64_t>(a.kv_heads) * R::kRow;
@@ -307,6 +358,58 @@ __device__ __forceinline__ void load_tile(const ExtendArgs& a, const StageMap<KV
       const int64_t i = pick4(sb, tid / kBlock) * blk_words + h * kBlock + tid % kBlock;
       r.ksz = __ldg(a.k_sz + i);
       r.vsz = __ldg(a.v_sz + i);
+    }
+    if (r.miss) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
+  }
+}
+
+// The same registers as load_tile, for an INT8 pool, read from raw stage
+// `st` (shared address) where the copies of tile tok0 have landed: row t of
+// the K and V regions is tile token t, its 16-byte chunk c at c ^ (t mod 8).
+template <bool QBF>
+__device__ __forceinline__ void read_tile(const ExtendArgs& a, uint32_t st, int tok0, int L,
+                                          int tid, RawTile<kI8>& r) {
+  using R = RawTile<kI8>;
+  const uint32_t valid = lds32(st + kRawValidOff);
+  r.kmask = 0u;
+#pragma unroll
+  for (int i = 0; i < R::kKChunks; ++i) {
+    int t, ch;
+    k_item<kI8>(tid + kStageThreads * i, t, ch);
+    r.k[i] = lds128(st + t * 128 + ((ch ^ (t & 7)) << 4));
+    r.kmask |= ((valid >> (t / kBlock)) & 1u && tok0 + t < L ? 1u : 0u) << i;
+    if constexpr (!QBF) r.ksz4[i] = lds32(st + kRawSzOff + 4 * t);
+  }
+  int tg, dc;
+  v_item<kI8>(tid, tg, dc);
+  const bool vok = (valid >> (tg >> 1)) & 1u;  // tokens 8 tg .. 8 tg + 7: block tg / 2
+  r.vmask = 0u;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) r.vmask |= (vok && tok0 + 8 * tg + t < L ? 1u : 0u) << t;
+  if constexpr (!QBF) {
+    const uint4 w0 = lds128(st + kRawSzOff + 4 * kTcTok + 32 * tg);
+    const uint4 w1 = lds128(st + kRawSzOff + 4 * kTcTok + 32 * tg + 16);
+    r.vsz8[0] = w0.x; r.vsz8[1] = w0.y; r.vsz8[2] = w0.z; r.vsz8[3] = w0.w;
+    r.vsz8[4] = w1.x; r.vsz8[5] = w1.y; r.vsz8[6] = w1.z; r.vsz8[7] = w1.w;
+  }
+  // row 8 tg + t has t mod 8 = t: its chunk dc / 2 sits at (dc / 2) ^ t
+  const uint32_t vrow = st + kRawVOff + 8 * tg * 128 + 8 * (dc & 1);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const uint2 w = lds64(vrow + t * 128 + (((dc >> 1) ^ t) << 4));
+    r.v[t][0] = w.x;
+    r.v[t][1] = w.y;
+  }
+  r.miss = false;
+  r.sz_ok = false;
+  r.ksz = r.vsz = 0u;
+  if (tid < kTcTok) {
+    const bool ok = (valid >> (tid / kBlock)) & 1u;
+    r.sz_ok = ok && tok0 + tid < L;
+    r.miss = tok0 + tid < L && !ok;
+    if constexpr (QBF) {
+      r.ksz = lds32(st + kRawSzOff + 4 * tid);
+      r.vsz = lds32(st + kRawSzOff + 4 * kTcTok + 4 * tid);
     }
     if (r.miss) report(a.dev_err, KVQ_DEV_ERR_BLOCK_ID);
   }
@@ -421,7 +524,8 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
     }
   }
   // V: 8 tokens x 8 dims -> 8 rows (dims) of 8 tokens, one 16-byte store each
-  const int tg = tid & 7, dc = tid >> 3;  // 8 token groups across lanes: no bank conflicts
+  int tg, dc;
+  v_item<KV>(tid, tg, dc);
   // dequantized V (fp16 queries): per token pair, (S, S') and (Z + mid S, ..)
   // as fp16 pairs, zero for tokens outside the context
   uint32_t s2[4], z2[4];
@@ -624,7 +728,22 @@ struct TcShared {
 
 // ---- roles ------------------------------------------------------------------------
 
-// Staging warpgroup: hands out the units and fills the K/V ring.
+// Hands out unit k (an atomic counter) through slot k mod 2 once every
+// working warp has read unit k - 2 from it. The one thread that runs it is
+// the raw-ring producer's lane 0 (INT8 pools: it runs furthest ahead, so the
+// copies of a unit's first tiles start while the previous unit is staged),
+// else thread 0 of the staging warpgroup.
+__device__ __forceinline__ void publish_unit(const ExtendArgs& a, const TcShared& c, uint32_t k) {
+  const uint32_t slot = k & 1u;
+  if (k < 2 || wait_or_abort(c.bar(kBarUnitEmpty + slot), ((k >> 1) - 1u) & 1u, c.abort_flag,
+                             a.dev_err)) {
+    c.unit_slot[slot] = atomicAdd(a.counter, 1);
+    mbar_arrive_one(c.bar(kBarUnitFull + slot));
+  }
+}
+
+// Staging warpgroup: fills the K/V ring (and hands out the units when there
+// is no raw-ring producer).
 template <int KV, bool QBF>
 __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared& c, int tid) {
   const int lane = tid & 31;
@@ -640,16 +759,10 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
     fence_async_smem();
   }
   uint32_t tc = 0;  // tiles staged so far
+  uint32_t rc = 0;  // raw stages consumed so far (INT8 pools)
   for (uint32_t k = 0;; ++k) {
     const uint32_t slot = k & 1u;
-    if (tid == 0) {
-      // the slot of unit k - 2 must have been read by all 14 working warps
-      if (k < 2 || wait_or_abort(c.bar(kBarUnitEmpty + slot), ((k >> 1) - 1u) & 1u, c.abort_flag,
-                                 a.dev_err)) {
-        c.unit_slot[slot] = atomicAdd(a.counter, 1);
-        mbar_arrive_one(c.bar(kBarUnitFull + slot));
-      }
-    }
+    if (!raw_ring<KV>() && tid == 0) publish_unit(a, c, k);
     __syncwarp();
     if (!warp_wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u, c.abort_flag, a.dev_err)) return;
     const int u = c.unit_slot[slot];
@@ -657,21 +770,9 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
     if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
     if (u >= c.total) return;
     const TcUnit w = tc_unit(a, c.ucum, u);
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks;
-    // tile t's codes are loaded two tiles before it is staged (two register
-    // sets; one for fp16 rows), its block ids one tile before that
     const int n = w.ntiles, L = w.s.L;
-    constexpr int kSets = 1;  // raw register sets in flight
-    StageMap<KV> map;
-    map.init(a, w.h, tid);
-    RawTile<KV> raw[kSets];
-    int4 blk = tile_blocks(bt, 0, a.max_blocks);
-#pragma unroll
-    for (int e = 0; e < kSets; ++e) {
-      if (e < n) load_tile<KV, QBF>(a, map, blk, e * kTcTok, L, w.h, tid, raw[e]);
-      blk = tile_blocks(bt, (e + 1) * kTcTok, a.max_blocks);
-    }
-    auto stage_one = [&](int j, RawTile<KV>& r) {
+    // registers -> the next K/V stage
+    auto store_one = [&](const RawTile<KV>& r) {
       const uint32_t st = tc % kStages, use = tc / kStages;
       if (use > 0 &&
           !warp_wait(c.bar(kBarKvEmpty + st), (use - 1u) & 1u, c.abort_flag, a.dev_err))
@@ -681,18 +782,97 @@ __device__ __forceinline__ void staging_role(const ExtendArgs& a, const TcShared
       fence_async_smem();
       mbar_arrive_one(c.bar(kBarKvFull + st));
       ++tc;
-      if (j + kSets < n) {
-        load_tile<KV, QBF>(a, map, blk, (j + kSets) * kTcTok, L, w.h, tid, r);
-        blk = tile_blocks(bt, (j + kSets + 1) * kTcTok, a.max_blocks);
-      }
       return true;
     };
-    for (int j = 0; j < n; j += kSets) {
-#pragma unroll
-      for (int e = 0; e < kSets; ++e)
-        if (j + e < n && !stage_one(j + e, raw[e])) return;
+    if constexpr (raw_ring<KV>()) {
+      // the producer warp's copies land tile j in raw stage rc mod kRawStages
+      for (int j = 0; j < n; ++j) {
+        const uint32_t rs = rc % kRawStages, use = rc / kRawStages;
+        if (!warp_wait(c.bar(kBarRawFull + rs), use & 1u, c.abort_flag, a.dev_err)) return;
+        RawTile<KV> r;
+        read_tile<QBF>(a, c.base + kRawOff + rs * kRawBytes, j * kTcTok, L, tid, r);
+        mbar_arrive_one(c.bar(kBarRawEmpty + rs));
+        ++rc;
+        if (!store_one(r)) return;
+      }
+    } else {
+      // tile j's codes are loaded while tile j - 1 is staged, its block ids
+      // a tile before that
+      const int32_t* bt = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks;
+      StageMap<KV> map;
+      map.init(a, w.h, tid);
+      RawTile<KV> r;
+      int4 blk = tile_blocks(bt, 0, a.max_blocks);
+      if (n > 0) load_tile<KV, QBF>(a, map, blk, 0, L, w.h, tid, r);
+      blk = tile_blocks(bt, kTcTok, a.max_blocks);
+      for (int j = 0; j < n; ++j) {
+        if (!store_one(r)) return;
+        if (j + 1 < n) {
+          load_tile<KV, QBF>(a, map, blk, (j + 1) * kTcTok, L, w.h, tid, r);
+          blk = tile_blocks(bt, (j + 2) * kTcTok, a.max_blocks);
+        }
+      }
     }
   }
+}
+
+// Raw-ring producer (INT8 pools; warp 14): hands out the units, and for each
+// tile of each unit one lane writes which of the tile's four blocks are valid
+// into the next raw stage and copies, for the unit's kv head, the four
+// blocks' K and V rows (one TMA box per block and tensor) and their
+// scale/zero words (64-byte bulk copies); a block past the context or
+// outside the pool is read from block 0 and masked by the consumers. Before
+// the warp leaves, every copy it issued has landed (bounded waits), so none
+// is in flight when the CTA ends.
+template <int KV>
+__device__ __forceinline__ void producer_role(const ExtendArgs& a, const TcShared& c, int lane) {
+  uint32_t rt = 0;  // tiles issued
+  bool ok = true;
+  for (uint32_t k = 0; ok; ++k) {
+    const uint32_t slot = k & 1u;
+    if (lane == 0) publish_unit(a, c, k);
+    __syncwarp();
+    if (!warp_wait(c.bar(kBarUnitFull + slot), (k >> 1) & 1u, c.abort_flag, a.dev_err)) break;
+    const int u = c.unit_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(c.bar(kBarUnitEmpty + slot));
+    if (u >= c.total) break;
+    const TcUnit w = tc_unit(a, c.ucum, u);
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(w.b) * a.max_blocks;
+    int4 blk = tile_blocks(bt, 0, a.max_blocks);
+    for (int j = 0; j < w.ntiles; ++j) {
+      const uint32_t rs = rt % kRawStages, use = rt / kRawStages;
+      if (use > 0 &&
+          !warp_wait(c.bar(kBarRawEmpty + rs), (use - 1u) & 1u, c.abort_flag, a.dev_err)) {
+        ok = false;
+        break;
+      }
+      uint32_t valid;
+      const int4 sb = safe_blocks(a, blk, j * kTcTok, w.s.L, &valid);
+      if (lane == 0) {
+        const uint32_t st = c.base + kRawOff + rs * kRawBytes, bar = c.bar(kBarRawFull + rs);
+        sts32(st + kRawValidOff, valid);
+        fence_async_smem();  // after the consumers' reads of the stage's last use
+        mbar_arm(bar, kRawTx);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int phys = pick4(sb, b);
+          const int64_t szi = (static_cast<int64_t>(phys) * a.kv_heads + w.h) * kBlock;
+          tma_tile_4d(st + b * kRawBox, &a.k_map, 0, w.h, 0, phys, bar);
+          tma_tile_4d(st + kRawVOff + b * kRawBox, &a.v_map, 0, w.h, 0, phys, bar);
+          bulk_copy(st + kRawSzOff + 64 * b, a.k_sz + szi, 64, bar);
+          bulk_copy(st + kRawSzOff + 4 * kTcTok + 64 * b, a.v_sz + szi, 64, bar);
+        }
+      }
+      __syncwarp();
+      ++rt;
+      blk = tile_blocks(bt, (j + 1) * kTcTok, a.max_blocks);
+    }
+  }
+  if (lane == 0)
+    for (uint32_t i = rt > kRawStages ? rt - kRawStages : 0u; i < rt; ++i)
+      mbar_wait(c.bar(kBarRawFull + i % kRawStages), (i / kRawStages) & 1u);
+  __syncwarp();
 }
 
 // One lane of a converged warp (elect.sync).
@@ -1046,10 +1226,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
       mbar_init_count(c.bar(kBarODone + s), 1);
       mbar_init_count(c.bar(kBarQFull + s), kWgRows);
       mbar_init_count(c.bar(kBarUnitFull + s), 1);
-      mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 2);  // every warp's lane 0
+      // lane 0 of every working warp: softmax, staging, MMA (and the producer)
+      mbar_init_count(c.bar(kBarUnitEmpty + s), kSoftWarps + 4 + 2 + (raw_ring<KV>() ? 1 : 0));
       mbar_init_count(c.bar(kBarSRead + s), kWgRows);
     }
     mbar_init_count(c.bar(kBarDrain), 2);  // one commit per MMA warp
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init_count(c.bar(kBarRawFull + s), 1);  // the producer's arming arrival
+      mbar_init_count(c.bar(kBarRawEmpty + s), kStageThreads);
+    }
     *c.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1077,6 +1262,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const __grid_c
         mbar_wait(c.bar(kBarDrain), 0);
       }
       __syncwarp();
+    } else if (raw_ring<KV>() && warp == kMmaWarp + 2) {
+      producer_role<KV>(a, c, lane);
     }
   }
   tc_fence_before();
