@@ -543,9 +543,20 @@ __device__ __forceinline__ void store_tile(const ExtendArgs& a, const RawTile<KV
     uint32_t lo[4], hi[4];
 #pragma unroll
     for (int tp = 0; tp < 4; ++tp) {
-      const uint32_t p0 = piece_pair<KV>(r.v[2 * tp], q), p1 = piece_pair<KV>(r.v[2 * tp + 1], q);
-      lo[tp] = prmt(p0, p1, 0x5410u);
-      hi[tp] = prmt(p0, p1, 0x7632u);
+      if constexpr (KV == kI8) {
+        // transposed at the byte level first, [t0 d, t1 d, t0 d', t1 d'] for
+        // dims d = 2q, d' = 2q + 1 of tokens t0 = 2 tp, t1 = 2 tp + 1; then
+        // each half as the pair c - 128 (one permute fewer per two pairs)
+        const uint32_t tb = prmt(r.v[2 * tp][q >> 1], r.v[2 * tp + 1][q >> 1],
+                                 (q & 1) ? 0x7362u : 0x5140u);
+        lo[tp] = bytes_to_f16(tb, 0x4140u);
+        hi[tp] = bytes_to_f16(tb, 0x4342u);
+      } else {
+        const uint32_t p0 = piece_pair<KV>(r.v[2 * tp], q);
+        const uint32_t p1 = piece_pair<KV>(r.v[2 * tp + 1], q);
+        lo[tp] = prmt(p0, p1, 0x5410u);
+        hi[tp] = prmt(p0, p1, 0x7632u);
+      }
       if constexpr (VDEQ && KvTraits<KV>::kQuant) {  // (c - mid) S + (Z + mid S), one rounding
         lo[tp] = hfma2(lo[tp], s2[tp], z2[tp]);
         hi[tp] = hfma2(hi[tp], s2[tp], z2[tp]);
