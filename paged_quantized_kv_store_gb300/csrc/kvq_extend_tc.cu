@@ -110,7 +110,7 @@ constexpr uint32_t kBarPFull = kBarSFull + 2;       // softmax g -> MMA (128 arr
 constexpr uint32_t kBarODone = kBarPFull + 2;       // MMA commit: O_g += P'_g V done
 constexpr uint32_t kBarQFull = kBarODone + 2;       // softmax g -> MMA: the unit's Q rows (128 arrivals)
 constexpr uint32_t kBarUnitFull = kBarQFull + 2;    // unit slot written
-constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by all 14 working warps
+constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2; // unit slot read by every working warp
 constexpr uint32_t kBarSRead = kBarUnitEmpty + 2;   // softmax g -> MMA: S_g read out of TMEM (128 arrivals)
 constexpr uint32_t kBarDrain = kBarSRead + 2;       // MMA commit before TMEM is freed
 constexpr uint32_t kBarRawFull = kBarDrain + 1;     // raw stage landed (TMA bytes), per raw stage
