@@ -1331,8 +1331,6 @@ int tc_occupancy_t(int batch) {
 
 }  // namespace
 
-size_t extend_tc_smem_bytes(int batch) { return tc_smem_bytes(batch); }
-
 int extend_tc_max_batch() { return kTcMaxBatch; }
 
 bool extend_tc_supported(int kv_dtype, int q_dtype) {

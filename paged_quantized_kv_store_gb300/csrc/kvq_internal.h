@@ -166,12 +166,11 @@ cudaError_t launch_barrier_selftest(unsigned int* ctr, int32_t* dev_err, int gri
 cudaError_t launch_extend(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                           cudaStream_t s);
 int extend_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
-// the tcgen05 version (128-row tiles; INT8, INT4 and fp16 pools)
+// the tcgen05 version (256-row units; INT8, INT4 and fp16 pools)
 bool extend_tc_supported(int kv_dtype, int q_dtype);
 cudaError_t launch_extend_tc(const ExtendArgs& a, int kv_dtype, int q_dtype, int grid_ctas,
                              cudaStream_t s);
 int extend_tc_ctas_per_sm(int kv_dtype, int q_dtype, int batch);
-size_t extend_tc_smem_bytes(int batch);  // dynamic shared memory of one CTA
 int extend_tc_max_batch();                // most requests the tcgen05 kernel takes
 cudaError_t launch_copy(const CopyArgs& a, int64_t n, cudaStream_t s);
 cudaError_t launch_tables(const TablesArgs& a, cudaStream_t s);
